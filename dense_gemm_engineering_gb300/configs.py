@@ -1,0 +1,57 @@
+"""The five GEMM workloads: shapes, layouts, dtypes and input recipes.
+
+Sources of the shapes:
+  * 128 x 128 x 64: "TIRx GEMM on Blackwell", V1 (one tile, one MMA, no K loop).
+  * 256 x 256 x 1024: "TIRx GEMM on Blackwell", V2 (the K loop reuses the same
+    barrier across 16 chunks of 64).
+  * 4096^3 A.Bt FP16: "TIRx GEMM on Blackwell", The short version / V3-V9
+    (the headline measurement shape).
+  * 8192 x 17408 x 5120 A.B BF16: "Choosing schedules and instructions for a
+    backend", section 1 (the TileFoundry H200 workload, B stored K x N).
+  * 3000 x 5000 x 4000 A.Bt FP16: a ragged shape, not a multiple of any tile,
+    that exercises the out-of-bounds fill on loads and the clipped stores.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class GemmConfig:
+    name: str
+    layout: str  # "abt": D = A.Bt, B is N x K;  "ab": D = A.B, B is K x N
+    M: int
+    N: int
+    K: int
+    dtype: str  # "f16" or "bf16" (inputs and output)
+    dist: str  # "uniform" U[-1,1) or "normal" N(0, 0.02^2)
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def min_bytes(self) -> int:
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+    @property
+    def rtol(self) -> float:
+        # |got - ref| <= 1e-2 + rtol * |ref|
+        return 1e-3 if self.dtype == "f16" else 8e-3
+
+    atol: float = 1e-2
+
+
+CONFIGS = [
+    GemmConfig("single_tile_128x128x64_f16_abt", "abt", 128, 128, 64, "f16", "uniform", 0),
+    GemmConfig("kloop_256x256x1024_f16_abt", "abt", 256, 256, 1024, "f16", "uniform", 1),
+    GemmConfig("square_4096x4096x4096_f16_abt", "abt", 4096, 4096, 4096, "f16", "uniform", 2),
+    GemmConfig("rect_8192x17408x5120_bf16_ab", "ab", 8192, 17408, 5120, "bf16", "normal", 3),
+    GemmConfig("ragged_3000x5000x4000_f16_abt", "abt", 3000, 5000, 4000, "f16", "uniform", 4),
+]
+
+BY_NAME = {c.name: c for c in CONFIGS}
+
+# The measured workload: FP16 A.Bt at 4096^3.
+HEADLINE = CONFIGS[2]

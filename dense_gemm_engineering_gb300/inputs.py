@@ -1,0 +1,138 @@
+"""Seeded synthetic operands for the GEMM workloads.
+
+This module is shared by the CUDA path's tests and benchmark and by the CPU
+oracle's tests.  It holds no GEMM arithmetic: it only draws numbers and rounds
+them once to the 16-bit storage type, so that the GPU kernel and the oracle
+consume the very same bit patterns.
+
+Generator (counter-based SplitMix64, Steele, Lea and Flood, "Fast splittable
+pseudorandom number generators", OOPSLA 2014; the 64-bit finaliser is the one
+published with Vigna's reference implementation):
+
+    gamma  = 0x9E3779B97F4A7C15
+    mix(z) = z ^= z >> 30; z *= 0xBF58476D1CE4E5B9;
+             z ^= z >> 27; z *= 0x94D049BB133111EB; z ^ (z >> 31)   (mod 2^64)
+    key(seed, stream) = mix((seed * 2^16 + stream + 1) * gamma)
+    draw i            = mix(key + (i + 1) * gamma)          i = 0, 1, 2, ...
+
+Distributions (element i of a row-major matrix, i = row * cols + col):
+    uniform U[-1, 1):  u = (draw_i >> 40) * 2^-24;  v = 2u - 1     (exact in fp32)
+    normal  N(0, s^2): Box-Muller on draws 2i and 2i+1:
+                       u1 = ((d_2i >> 11) + 1) * 2^-53,  u2 = (d_2i+1 >> 11) * 2^-53
+                       v  = fp32(s * sqrt(-2 ln u1) * cos(2 pi u2))
+Then v is rounded once (nearest, ties to even) to binary16 or bfloat16.
+
+Stream 0 draws A, stream 1 draws B.  Padding columns (row stride > cols) are
+filled with a quiet NaN so that any read of padding poisons the result.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_C1 = np.uint64(0xBF58476D1CE4E5B9)
+_C2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 23
+
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = z ^ (z >> np.uint64(30))
+    z = z * _C1
+    z = z ^ (z >> np.uint64(27))
+    z = z * _C2
+    return z ^ (z >> np.uint64(31))
+
+
+def stream_key(seed: int, stream: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        base = np.array([(int(seed) * 65536 + int(stream) + 1) & ((1 << 64) - 1)],
+                        dtype=np.uint64)
+        return _mix(base * GAMMA)[0]
+
+
+def draws(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Draws start .. start+count-1 of stream (seed, stream) as uint64."""
+    key = stream_key(seed, stream)
+    with np.errstate(over="ignore"):
+        idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+        return _mix(key + idx * GAMMA)
+
+
+def splitmix64_sequence(state: int, count: int) -> np.ndarray:
+    """Plain SplitMix64 outputs from an initial state (used to pin the mixer)."""
+    with np.errstate(over="ignore"):
+        idx = np.arange(1, count + 1, dtype=np.uint64)
+        return _mix(np.uint64(state) + idx * GAMMA)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """binary32 -> bfloat16 pattern, nearest with ties to even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def _to_bits(v32: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f16":
+        return v32.astype(np.float16).view(np.uint16)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(v32)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def values_f32(seed: int, stream: int, start: int, count: int, dist: str,
+               sigma: float = 0.02) -> np.ndarray:
+    """Elements start .. start+count-1 of a stream, as binary32 before rounding."""
+    if dist == "uniform":
+        d = draws(seed, stream, start, count)
+        u = (d >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)
+        return np.float32(2.0) * u - np.float32(1.0)
+    if dist == "normal":
+        d = draws(seed, stream, 2 * start, 2 * count)
+        u1 = ((d[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+        return (sigma * z).astype(np.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def bits(seed: int, stream: int, count: int, dtype: str, dist: str,
+         sigma: float = 0.02) -> np.ndarray:
+    """First `count` elements of a stream as 16-bit patterns (uint16)."""
+    out = np.empty(count, dtype=np.uint16)
+    for s in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - s)
+        out[s:s + n] = _to_bits(values_f32(seed, stream, s, n, dist, sigma), dtype)
+    return out
+
+
+def matrix(seed: int, stream: int, rows: int, cols: int, dtype: str, dist: str,
+           ld: int | None = None, sigma: float = 0.02) -> np.ndarray:
+    """A rows x cols operand of 16-bit patterns, row-major with row stride ld.
+
+    Returns the (rows, cols) view of a (rows, ld) buffer; padding is NaN.
+    """
+    ld = cols if ld is None else ld
+    if ld < cols:
+        raise ValueError("ld < cols")
+    flat = bits(seed, stream, rows * cols, dtype, dist, sigma)
+    if ld == cols:
+        return flat.reshape(rows, cols)
+    buf = np.full((rows, ld), NAN_BITS[dtype], dtype=np.uint16)
+    buf[:, :cols] = flat.reshape(rows, cols)
+    return buf[:, :cols]
+
+
+def operands(M: int, N: int, K: int, layout: str, dtype: str, dist: str, seed: int,
+             lda: int | None = None, ldb: int | None = None):
+    """(A, B) for D = A.Bt (layout 'abt', B is N x K) or D = A.B ('ab', B is K x N)."""
+    A = matrix(seed, 0, M, K, dtype, dist, lda)
+    if layout == "abt":
+        B = matrix(seed, 1, N, K, dtype, dist, ldb)
+    elif layout == "ab":
+        B = matrix(seed, 1, K, N, dtype, dist, ldb)
+    else:
+        raise ValueError(f"unknown layout {layout!r}")
+    return A, B

@@ -1,0 +1,156 @@
+/*
+ * gemm_oracle.c -- CPU oracle for the dense GEMM.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load this file.  The product path (the CUDA library) shares no code,
+ * header, table or build flag with it and never calls it.
+ *
+ * What it computes (plain definition, no blocking, no reordering):
+ *
+ *   D[i,j] = round_RNE( sum_{k<K} A[i,k] * B'[j,k] )
+ *
+ *   - "TIRx GEMM on Blackwell" (jq-wei.github.io), section "The short version":
+ *     the operation is D = A @ B.T with 16-bit inputs and output and the
+ *     partial products accumulated in FP32 on the GPU.  Here B' = B and B is
+ *     stored N x K ("A.Bt" layout).
+ *   - "Choosing schedules and instructions for a backend" (TileFoundry tutorial),
+ *     section 1, the `gemm(a: (M,K), b: (K,N)) -> (M,N)` program: the plain
+ *     product with B stored K x N ("A.B" layout), B'[j,k] = B[k,j].
+ *   - "TIRx GEMM on Blackwell", Take away 1: tiling, pipelining and scheduling
+ *     do not change the arithmetic, only the order of the additions.  So the
+ *     oracle is the definition itself: the sum runs over k in increasing order
+ *     in IEEE binary64 from the exact 16-bit input values (every product of two
+ *     binary16 or two bfloat16 values is exact in binary64), and the result is
+ *     rounded ONCE to the output type with round-to-nearest-even.
+ *
+ * The 16-bit decode and the binary64 -> 16-bit rounding are written here from
+ * the IEEE 754-2008 binary16 definition (1 sign, 5 exponent bits with bias 15,
+ * 10 fraction bits, subnormals, inf/NaN at exponent 31) and from the bfloat16
+ * definition (the upper half of an IEEE binary32: 1 sign, 8 exponent bits with
+ * bias 127, 7 fraction bits).
+ *
+ * Parity pins (tests/test_oracle.py): hand-computed products, identity and
+ * permutation operands, the transpose invariant (A.Bt)t == B.At, closed forms
+ * for all-ones operands, exact small-integer products, agreement of the two
+ * layouts, the rounding rule against numpy's independent binary16 conversion,
+ * and torch.mm in float64 on small random cases.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F16 0
+#define ORACLE_BF16 1
+#define ORACLE_B_NK 0 /* B stored N x K row-major: D = A . B^T */
+#define ORACLE_B_KN 1 /* B stored K x N row-major: D = A . B   */
+
+/* ---- decode: 16-bit pattern -> exact binary64 value ---------------------- */
+
+static double f16_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24); /* subnormal (or zero): f * 2^-24 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+static double bf16_bits_to_double(uint16_t h) {
+    /* bfloat16 is the top half of a binary32 pattern. */
+    uint32_t w = ((uint32_t)h) << 16;
+    float x;
+    memcpy(&x, &w, sizeof x);
+    return (double)x;
+}
+
+double oracle_to_double(uint16_t bits, int dtype) {
+    return dtype == ORACLE_BF16 ? bf16_bits_to_double(bits) : f16_bits_to_double(bits);
+}
+
+/* ---- encode: binary64 -> 16-bit pattern, round to nearest, ties to even ---
+ *
+ * Generic for a format with `ebits` exponent bits and `fbits` fraction bits.
+ * Scaling by a power of two is exact in binary64 over the whole range used, so
+ * one nearbyint() (default rounding mode = to nearest, ties to even) performs
+ * the single rounding step.
+ */
+static uint16_t round_to_format(double x, int ebits, int fbits) {
+    const int bias = (1 << (ebits - 1)) - 1;
+    const int emax_field = (1 << ebits) - 1;
+    const uint16_t sign = signbit(x) ? (uint16_t)(1u << (ebits + fbits)) : 0;
+    const uint16_t inf = (uint16_t)(emax_field << fbits);
+    if (isnan(x)) return (uint16_t)(inf | (1u << (fbits - 1)));
+    double a = fabs(x);
+    if (isinf(a)) return sign | inf;
+    const int emin = 1 - bias; /* exponent of the smallest normal */
+    if (a < ldexp(1.0, emin)) {
+        /* subnormal range: quantum 2^(emin - fbits).  q == 2^fbits encodes
+         * the smallest normal, which the bit pattern below already does. */
+        double q = nearbyint(ldexp(a, fbits - emin));
+        return sign | (uint16_t)q;
+    }
+    int e2;
+    frexp(a, &e2); /* a = m * 2^e2, m in [0.5, 1): unbiased exponent is e2-1 */
+    int e = e2 - 1;
+    double q = nearbyint(ldexp(a, fbits - e)); /* in [2^fbits, 2^(fbits+1)] */
+    if (q == ldexp(1.0, fbits + 1)) { /* rounding carried into the exponent */
+        q = ldexp(1.0, fbits);
+        e += 1;
+    }
+    int field = e + bias;
+    if (field >= emax_field) return sign | inf; /* overflow rounds to infinity */
+    return sign | (uint16_t)(field << fbits) | (uint16_t)((uint32_t)q - (1u << fbits));
+}
+
+uint16_t oracle_from_double(double x, int dtype) {
+    return dtype == ORACLE_BF16 ? round_to_format(x, 8, 7) : round_to_format(x, 5, 10);
+}
+
+/* ---- the GEMM ------------------------------------------------------------
+ *
+ * Computes rows [i0,i1) x columns [j0,j1) of D.  A is M x K row-major with row
+ * stride lda (elements); B is N x K (b_layout 0) or K x N (b_layout 1)
+ * row-major with row stride ldb.  Results go to out[(i-i0)*ldo + (j-j0)].
+ * `out_f64` (may be NULL) receives the unrounded binary64 sums; `out16`
+ * (may be NULL) the rounded 16-bit patterns.
+ */
+void oracle_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int b_layout, int dtype,
+                 int64_t i0, int64_t i1, int64_t j0, int64_t j1,
+                 uint16_t* out16, double* out_f64, int64_t ldo) {
+    (void)M;
+    (void)N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = i0; i < i1; ++i) {
+        for (int64_t j = j0; j < j1; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = oracle_to_double(A[i * lda + k], dtype);
+                double b = (b_layout == ORACLE_B_NK) ? oracle_to_double(B[j * ldb + k], dtype)
+                                                     : oracle_to_double(B[k * ldb + j], dtype);
+                acc += a * b;
+            }
+            int64_t o = (i - i0) * ldo + (j - j0);
+            if (out_f64) out_f64[o] = acc;
+            if (out16) out16[o] = oracle_from_double(acc, dtype);
+        }
+    }
+}
+
+/* Number of threads the OpenMP runtime will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

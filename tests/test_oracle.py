@@ -1,0 +1,213 @@
+"""Pins for the CPU oracle, independent of the oracle's own code.
+
+Each check compares the oracle with something other than itself: products
+worked out by hand (tests/golden/hand_products.txt), identity and permutation
+operands, the transpose invariant (A.Bt)t = B.At, closed forms, exact integer
+products from numpy's int64 matmul, torch.mm in float64, and numpy's / torch's
+own 16-bit conversions for the rounding rule.
+
+The checks are plain functions of an oracle object so that
+tests/test_oracle_mutants.py can run them against copies of the oracle with
+planted mistakes and show that each mistake is caught.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_engineering_gb300 import inputs
+from golden_io import hand_products
+
+
+def enc(values, dtype):
+    """Exact decimal values -> 16-bit patterns through numpy / torch (not the oracle)."""
+    v = np.asarray(values, dtype=np.float64)
+    if dtype == "f16":
+        h = v.astype(np.float16)
+        assert np.array_equal(h.astype(np.float64), v, equal_nan=True), "not representable"
+        return h.view(np.uint16)
+    t = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(t.to(torch.float64).numpy(), v), "not representable"
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def dec(bits, dtype):
+    """16-bit patterns -> float64 through numpy / torch (not the oracle)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return b.view(np.float16).astype(np.float64)
+    return torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+CASES = hand_products()
+
+
+def pin_hand_products_abt(orc):
+    for case in CASES:
+        dt = case["dtype"]
+        A, B = enc(case["A"], dt), enc(case["B"], dt)
+        D = orc.gemm(A, B, layout="abt", dtype=dt)
+        assert np.array_equal(D, case["bits"]), (case["name"], D, case["bits"])
+        assert np.array_equal(dec(D, dt), case["D"]), case["name"]
+
+
+def pin_hand_products_ab(orc):
+    for case in CASES:
+        dt = case["dtype"]
+        A = enc(case["A"], dt)
+        Bkn = np.ascontiguousarray(enc(case["B"], dt).T)  # K x N storage
+        D = orc.gemm(A, Bkn, layout="ab", dtype=dt)
+        assert np.array_equal(D, case["bits"]), case["name"]
+
+
+def pin_identity(orc):
+    for dtype in ("f16", "bf16"):
+        A = inputs.matrix(11, 0, 7, 16, dtype, "uniform")
+        eye = enc(np.eye(16), dtype)
+        assert np.array_equal(orc.gemm(A, eye, layout="abt", dtype=dtype), A)
+        assert np.array_equal(orc.gemm(A, eye, layout="ab", dtype=dtype), A)
+
+
+def pin_permutation(orc):
+    rng = np.random.default_rng(5)
+    K = 24
+    perm = rng.permutation(K)
+    P = np.zeros((K, K))
+    P[np.arange(K), perm] = 1.0  # row j of P picks column perm[j] of A
+    for dtype in ("f16", "bf16"):
+        A = inputs.matrix(12, 0, 9, K, dtype, "uniform")
+        D = orc.gemm(A, enc(P, dtype), layout="abt", dtype=dtype)
+        assert np.array_equal(D, A[:, perm])
+        # A.P with P stored K x N: column j of D is column argsort(perm)[j] of A
+        D2 = orc.gemm(A, enc(P, dtype), layout="ab", dtype=dtype)
+        assert np.array_equal(D2, A[:, np.argsort(perm)])
+
+
+def pin_transpose_invariant(orc):
+    for dtype in ("f16", "bf16"):
+        A, B = inputs.operands(13, 21, 37, "abt", dtype, "uniform", seed=7)
+        D1 = orc.gemm(A, B, layout="abt", dtype=dtype)
+        D2 = orc.gemm(B, A, layout="abt", dtype=dtype)
+        assert np.array_equal(D1.T, D2)
+        # the A.B form on the transposed B gives the same bits
+        D3 = orc.gemm(A, np.ascontiguousarray(B.T), layout="ab", dtype=dtype)
+        assert np.array_equal(D1, D3)
+
+
+def pin_all_ones_closed_form(orc):
+    # D[i,j] = sum_k B[j,k].  Values are multiples of 2^-24 (binary16) or
+    # 2^-30 (bfloat16 of the uniform draws) with |v| <= 1, so every summation
+    # order is exact in binary64; numpy then rounds to binary16.
+    K = 300
+    for dtype in ("f16", "bf16"):
+        B = inputs.matrix(3, 1, 17, K, dtype, "uniform")
+        ones = enc(np.ones((5, K)), dtype)
+        D, D64 = orc.gemm(ones, B, layout="abt", dtype=dtype, want_f64=True)
+        s = dec(B, dtype).sum(axis=1)
+        assert np.array_equal(D64, np.broadcast_to(s, (5, 17)))
+        if dtype == "f16":
+            assert np.array_equal(D, np.broadcast_to(s.astype(np.float16).view(np.uint16), (5, 17)))
+
+
+def pin_small_integers_exact(orc):
+    # |D| <= lim^2 * K stays within the exactly representable integers
+    # (2048 for binary16, 256 for bfloat16), so D must equal numpy's int64 product.
+    rng = np.random.default_rng(9)
+    M, N, K = 19, 23, 64
+    for dtype, lim in (("f16", 4), ("bf16", 2)):
+        Ai = rng.integers(-lim, lim + 1, size=(M, K))
+        Bi = rng.integers(-lim, lim + 1, size=(N, K))
+        ref = (Ai @ Bi.T).astype(np.float64)
+        for layout in ("abt", "ab"):
+            Bstore = Bi if layout == "abt" else np.ascontiguousarray(Bi.T)
+            D = orc.gemm(enc(Ai, dtype), enc(Bstore, dtype), layout=layout, dtype=dtype)
+            assert np.array_equal(dec(D, dtype), ref), (dtype, layout)
+
+
+def pin_against_torch_float64(orc):
+    for dtype in ("f16", "bf16"):
+        for layout in ("abt", "ab"):
+            A, B = inputs.operands(33, 29, 200, layout, dtype, "uniform", seed=21)
+            D, D64 = orc.gemm(A, B, layout=layout, dtype=dtype, want_f64=True)
+            Bt = torch.from_numpy(dec(B, dtype))
+            Bt = Bt.T if layout == "abt" else Bt
+            ref = (torch.from_numpy(dec(A, dtype)) @ Bt).numpy()
+            np.testing.assert_allclose(D64, ref, rtol=1e-13, atol=1e-15)
+            if dtype == "f16":
+                assert np.array_equal(D, ref.astype(np.float16).view(np.uint16))
+
+
+def pin_strided_operands_ignore_padding(orc):
+    # Row strides larger than K; the padding holds NaN, which would poison any
+    # sum that read it.
+    A = inputs.matrix(40, 0, 10, 30, "f16", "uniform", ld=40)
+    B = inputs.matrix(40, 1, 12, 30, "f16", "uniform", ld=48)
+    D = orc.gemm(A, B, layout="abt", dtype="f16")
+    Dc = orc.gemm(np.ascontiguousarray(A), np.ascontiguousarray(B), layout="abt", dtype="f16")
+    assert np.array_equal(D, Dc)
+    assert np.isfinite(dec(D, "f16")).all()
+
+
+def pin_sub_block_matches_full(orc):
+    A, B = inputs.operands(40, 50, 33, "ab", "bf16", "normal", seed=3)
+    full = orc.gemm(A, B, layout="ab", dtype="bf16")
+    part = orc.gemm(A, B, layout="ab", dtype="bf16", rows=(7, 31), cols=(13, 47))
+    assert np.array_equal(part, full[7:31, 13:47])
+
+
+def pin_empty_k_gives_zero(orc):
+    A = np.zeros((3, 0), dtype=np.uint16)
+    B = np.zeros((4, 0), dtype=np.uint16)
+    D = orc.gemm(A, B, layout="abt", dtype="f16")
+    assert D.shape == (3, 4) and not D.any()
+
+
+# ---- the rounding rule, against independent conversions --------------------
+
+def pin_f16_decode_matches_numpy(orc):
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.to_double(allbits, "f16")
+    ref = allbits.view(np.float16).astype(np.float64)
+    assert np.array_equal(got, ref, equal_nan=True)
+
+
+def pin_bf16_decode_matches_torch(orc):
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.to_double(allbits, "bf16")
+    assert np.array_equal(got, dec(allbits, "bf16"), equal_nan=True)
+
+
+def pin_f16_rounding_matches_numpy(orc):
+    # numpy rounds binary64 -> binary16 directly (one rounding step).
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, size=20000),
+        (np.arange(-3000, 3000) + 0.5) * 2.0 ** -10,  # exact ties around 1..3
+        (np.arange(0, 2000) + 0.5) * 2.0 ** -24,  # ties in the subnormal range
+        np.array([65504.0, 65519.999, 65520.0, -65520.0, 1e6, 0.0, -0.0, 2.0 ** -25]),
+    ])
+    got = orc.from_double(x, "f16")
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def pin_bf16_rounding_matches_torch_on_binary32_values(orc):
+    # For values that are exact binary32 numbers, rounding binary64 -> bfloat16
+    # equals torch's binary32 -> bfloat16 rounding (nearest, ties to even).
+    rng = np.random.default_rng(2)
+    x32 = np.concatenate([
+        (rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, size=20000)),
+        (np.arange(-3000, 3000) + 0.5) * 2.0 ** -7,  # exact ties
+    ]).astype(np.float32)
+    got = orc.from_double(x32.astype(np.float64), "bf16")
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
+
+
+@pytest.mark.parametrize("name", sorted(PINS))
+def test_pin(name):
+    PINS[name](oracle.get())

@@ -1,0 +1,60 @@
+"""Planted mistakes in copies of the oracle source must each fail some pin.
+
+Every mutant below is a plausible slip in a plain GEMM (a wrong sign, a dropped
+term, a transposed operand, a wrong stride, binary32 accumulation, a wrong
+rounding rule, a wrong exponent bias).  The test compiles each mutant on the
+CPU and runs all pins of tests/test_oracle.py against it; at least one must
+fail, which shows the pins would catch that slip in the real oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+import test_oracle
+
+MUTANTS = {
+    "sign": ("acc += a * b;", "acc -= a * b;"),
+    "dropped_last_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
+    "dropped_first_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
+    "b_transposed_in_abt": ("oracle_to_double(B[j * ldb + k], dtype)", "oracle_to_double(B[k * ldb + j], dtype)"),
+    "b_transposed_in_ab": ("oracle_to_double(B[k * ldb + j], dtype)", "oracle_to_double(B[j * ldb + k], dtype)"),
+    "a_wrong_stride": ("A[i * lda + k]", "A[i * K + k]"),
+    "accumulate_binary32": ("double acc = 0.0;", "float acc = 0.0f;"),
+    "round_toward_zero": ("double q = nearbyint(ldexp(a, fbits - e));", "double q = trunc(ldexp(a, fbits - e));"),
+    "ties_away": ("double q = nearbyint(ldexp(a, fbits - e));", "double q = round(ldexp(a, fbits - e));"),
+    "f16_bias": ("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
+    "subnormal_scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "no_overflow_to_inf": ("if (field >= emax_field) return sign | inf;", "if (field > emax_field) return sign | inf;"),
+    "b_k_reversed": ("oracle_to_double(B[j * ldb + k], dtype)", "oracle_to_double(B[j * ldb + (K - 1 - k)], dtype)"),
+    "bf16_read_as_f16": ("return dtype == ORACLE_BF16 ? bf16_bits_to_double(bits) : f16_bits_to_double(bits);",
+                         "return f16_bits_to_double(bits);"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+def _failing_pins(orc):
+    failed = []
+    for name, fn in test_oracle.PINS.items():
+        try:
+            fn(orc)
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_mutant_is_caught(mutant, mutant_dir):
+    src = open(oracle.SOURCE).read()
+    old, new = MUTANTS[mutant]
+    assert src.count(old) >= 1, f"mutation anchor missing: {old!r}"
+    c_path = os.path.join(mutant_dir, f"{mutant}.c")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    so = oracle.compile_source(c_path, os.path.join(mutant_dir, f"lib{mutant}.so"))
+    failed = _failing_pins(oracle.Oracle(so))
+    assert failed, f"no pin caught the planted mistake {mutant!r}"
