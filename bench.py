@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Throughput of the sm_103a GEMM: FP16 D = A.B^T at M = N = K = 4096.
+
+One step = one GEMM call over the whole workload (all of the hot path: the
+persistent tile schedule, TMA ring, tcgen05 MMAs and the TMA-store epilogue
+run inside the one kernel launch).  The inputs sit in HBM before the timed
+region; the 96 MiB working set fits in the 129 MB L2, so a 512 MiB write
+flushes L2 before every timed step (outside the per-step CUDA events).
+
+Prints one JSON line (rank 0).  `--impl reference` instead times the CPU
+oracle, as it stands, on a bounded row sample of the same workload.
+
+Under torchrun every rank runs its own replica of the workload on its own GPU
+(the GEMM has no exchange step): value = all ranks' FLOPs / the slowest
+rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (FP16 A·Bᵀ, 4096³) and % of GB300 dense tensor peak"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 512 << 20
+# Dense FP16/BF16 tensor rate of one Blackwell SM: 8192 flop per clock (one
+# 128 x 256 x 16 MMA every 128 cycles); 152 SMs x 8192 x 2070 MHz at sm_max.
+FLOP_PER_CLK_PER_SM = 8192
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default=None, help="workload name (default: the 4096^3 FP16 A.Bt)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: ncu traffic figures are valid only for this hash."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_engineering_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "gemm.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str, src_hash: str):
+    """DRAM bytes per launch from an ncu summary under profiles/, if it was
+    taken on this exact kernel source.  Summary lines look like
+    `bench-traffic: workload=<name> kernel=<hash> bytes_per_launch=<int>`."""
+    pat = re.compile(r"bench-traffic:\s*workload=(\S+)\s+kernel=(\S+)\s+bytes_per_launch=(\d+)")
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(1) == workload and m.group(2) == src_hash:
+                    return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of one GPU while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, mx, power, reasons = [], [], [], set()
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+def make_inputs(cfg):
+    from dense_gemm_engineering_gb300 import inputs
+
+    return inputs.operands(cfg.M, cfg.N, cfg.K, cfg.layout, cfg.dtype, cfg.dist, cfg.seed)
+
+
+def oracle_sample(cfg, A, B, target_s: float):
+    """Time the oracle on the first rows of D, sized to about target_s seconds."""
+    import oracle
+
+    orc = oracle.get()
+    probe_rows = min(cfg.M, 8)
+    t0 = time.perf_counter()
+    orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, probe_rows))
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    rows = max(probe_rows, min(cfg.M, int(target_s / (t_probe / probe_rows))))
+    t0 = time.perf_counter()
+    orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, rows))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * cfg.N * cfg.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"rows 0..{rows} of D ({rows} x {cfg.N} outputs, K={cfg.K}), "
+                      f"{dt:.1f} s"}, rows, dt
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    A, B = make_inputs(cfg)
+    import oracle
+
+    orc = oracle.get()
+    # Size one step to ~1.5 s so warm-up + steps end within a few minutes.
+    _, rows, dt = oracle_sample(cfg, A, B, target_s=1.5)
+    step_rows = rows
+    times = []
+    for i in range(args.warmup + args.steps):
+        r0 = (i * step_rows) % max(1, cfg.M - step_rows + 1)
+        t0 = time.perf_counter()
+        orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(r0, r0 + step_rows))
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    flops = 2.0 * step_rows * cfg.N * cfg.K
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K,
+                   "layout": cfg.layout, "step": f"{step_rows} rows of D per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{step_rows} rows x {cfg.N} columns of D per step, "
+                                   f"K={cfg.K}, binary64 triple loop"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cfg):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from dense_gemm_engineering_gb300 import binding, build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    binding.load()
+
+    A, B = make_inputs(cfg)
+    tdt = torch.float16 if cfg.dtype == "f16" else torch.bfloat16
+    dA16 = torch.from_numpy(A.view(np.int16)).to(dev)
+    dB16 = torch.from_numpy(B.view(np.int16)).to(dev)
+    dA, dB = dA16.view(tdt), dB16.view(tdt)
+    dD = torch.empty((cfg.M, cfg.N), dtype=tdt, device=dev)
+    gemm = binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        gemm(dA, dB, dD)
+    torch.cuda.synchronize(dev)
+    if binding.gemm_device_status(clear=True) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = None if args.no_clocks else ClockSampler(f"GPU-{props.uuid}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # 512 MiB write evicts the previous step's operands from L2
+        starts[i].record(stream)
+        gemm(dA, dB, dD)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    barrier()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per_launch_ms) / len(per_launch_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = binding.gemm_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status word {status:#x} after the timed region")
+
+    flops = 2.0 * cfg.M * cfg.N * cfg.K
+    value = world * flops / (ms / 1e3) / 1e12
+    achieved = flops / (ms / 1e3) / 1e12
+
+    # ---- end to end through the public API, host buffers -------------------------
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.from_numpy(A.view(np.int16)).pin_memory()
+        hB = torch.from_numpy(B.view(np.int16)).pin_memory()
+        hD = torch.empty((cfg.M, cfg.N), dtype=torch.int16).pin_memory()
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            dA16.copy_(hA, non_blocking=True)
+            dB16.copy_(hB, non_blocking=True)
+            gemm(dA, dB, dD)
+            hD.copy_(dD.view(torch.int16), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "steps": n_e2e,
+               "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+               "d2h_bytes_per_step": int(cfg.M * cfg.N * 2),
+               "path": "pinned host A,B -> device (copy) -> gemm C ABI -> device D -> pinned host"}
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    src_hash = kernel_source_hash()
+    traffic = recorded_traffic(cfg.name, src_hash)
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    nominal = props.multi_processor_count * FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+    plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, 0 if cfg.dtype == "f16" else 1,
+                             0 if cfg.layout == "abt" else 1)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu, _, _ = oracle_sample(cfg, A, B, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K,
+                   "layout": cfg.layout, "inputs": f"{cfg.dist}, seed {cfg.seed}",
+                   "accumulate": "fp32 (TMEM)",
+                   "l2": "flushed before every timed step (512 MiB write, outside the events)",
+                   "plan": plan, "parallelism": f"replicas x{world}",
+                   "wall_s_timed_region": t_wall},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json); FP16:BF16 "
+                                    "nominal ratio 1:1",
+                     "kernel_source": src_hash},
+        "tensor_peak_nominal": {"tflops": nominal, "frac": achieved / nominal,
+                                "basis": f"{props.multi_processor_count} SMs x "
+                                         f"{FLOP_PER_CLK_PER_SM} flop/clk x {sm_max:.0f} MHz"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "per_launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
+                          "max": max(per_launch_ms)},
+    }
+    if clocks and clocks.get("sm_mhz"):
+        line["tensor_peak_nominal"]["frac_at_run_clock"] = (
+            achieved / (props.multi_processor_count * FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] / 1e6))
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.BY_NAME[args.config] if args.config else configs.HEADLINE
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,222 @@
+"""Python binding of the C ABI in include/gemm.h (argument marshalling only).
+
+Every function here forwards to libgb300gemm.so through ctypes: it reads data
+pointers, strides and the current CUDA stream from torch tensors and passes
+them on.  No arithmetic of the GEMM runs in Python and there is no fallback:
+if the library is missing or the call fails, a GemmError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+GEMM_F16, GEMM_BF16 = 0, 1
+LAYOUT_ABT, LAYOUT_AB = 0, 1
+
+STATUS_NAMES = {
+    0: "GEMM_OK",
+    -1: "GEMM_ERR_NULL",
+    -2: "GEMM_ERR_DTYPE",
+    -3: "GEMM_ERR_SHAPE",
+    -4: "GEMM_ERR_ALIGN",
+    -5: "GEMM_ERR_ALIAS",
+    -6: "GEMM_ERR_CUDA",
+    -7: "GEMM_ERR_DEVICE",
+    -8: "GEMM_ERR_OPTION",
+    -9: "GEMM_ERR_TIMEOUT",
+}
+
+# Every symbol include/gemm.h declares.
+EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_status_string", "gemm_plan",
+           "gemm_tile_origin", "gemm_device_status", "gemm_selftest_wait_timeout")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = f"{STATUS_NAMES.get(status, status)}: {gemm_status_string(status)}"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+class GemmOptions(ctypes.Structure):
+    """gemm_options_t."""
+    _fields_ = [("cta_group", ctypes.c_int), ("block_n", ctypes.c_int),
+                ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (built in-tree by build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library {p} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    for name in ("gemm_abt", "gemm_ab"):
+        f = getattr(lib, name)
+        f.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, vp]
+        f.restype = c_int
+    lib.gemm_run.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                             ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_run.restype = c_int
+    lib.gemm_status_string.argtypes = [c_int]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    ip = ctypes.POINTER(c_int)
+    lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions), ip, ip,
+                              ip, ip, ip, ctypes.POINTER(i64)]
+    lib.gemm_plan.restype = c_int
+    lib.gemm_tile_origin.argtypes = [i64, i64, c_int, c_int, c_int, i64, ctypes.POINTER(i64),
+                                     ctypes.POINTER(i64)]
+    lib.gemm_tile_origin.restype = c_int
+    lib.gemm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
+    lib.gemm_device_status.restype = c_int
+    lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.gemm_selftest_wait_timeout.restype = c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def gemm_status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+def _options(options) -> ctypes.POINTER(GemmOptions) | None:
+    if options is None:
+        return None
+    if isinstance(options, GemmOptions):
+        o = options
+    else:
+        o = GemmOptions(**{k: int(v) for k, v in dict(options).items()})
+    return ctypes.pointer(o)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float16:
+        return GEMM_F16
+    if t.dtype == torch.bfloat16:
+        return GEMM_BF16
+    raise GemmError(-2, f"tensor dtype {t.dtype}")
+
+
+def _ld(t) -> int:
+    # Row stride in elements of a row-major 2-D view (inner stride must be 1).
+    if t.dim() != 2:
+        raise GemmError(-3, "operands must be 2-D")
+    if t.shape[0] > 0 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise GemmError(-3, "inner dimension must be contiguous")
+    if t.shape[0] > 1:
+        return int(t.stride(0))
+    # one row (or none): the stride is never used; any legal value will do
+    return max(8, (int(t.shape[1]) + 7) // 8 * 8)
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=None):
+    """D = A.B^T (layout 0, B is N x K) or A.B (layout 1, B is K x N) on torch tensors.
+
+    Allocates D with torch when not given.  Enqueues on `stream` (default: the
+    current stream of A's device) and returns D without synchronising.
+    """
+    import torch
+
+    if A.device.type != "cuda" or B.device.type != "cuda":
+        raise GemmError(-1, "operands must be CUDA tensors")
+    M, K = A.shape
+    N = B.shape[0] if layout == LAYOUT_ABT else B.shape[1]
+    Kb = B.shape[1] if layout == LAYOUT_ABT else B.shape[0]
+    if Kb != K:
+        raise GemmError(-3, f"K mismatch ({K} vs {Kb})")
+    if A.dtype != B.dtype:
+        raise GemmError(-2, "A and B must share a dtype")
+    if D is None:
+        D = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    elif D.dtype != A.dtype or tuple(D.shape) != (M, N):
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    st = load().gemm_run(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _ld(A), _ld(B),
+                         _ld(D), _dtype_code(A), int(layout), _options(options),
+                         _stream_handle(stream, A.device))
+    if st != 0:
+        raise GemmError(st, "gemm_run")
+    return D
+
+
+def gemm_abt(A, B, D=None, *, options=None, stream=None):
+    """D[M, N] = A[M, K] . B[N, K]^T (FP16/BF16, FP32 accumulation)."""
+    return gemm_run(A, B, D, layout=LAYOUT_ABT, options=options, stream=stream)
+
+
+def gemm_ab(A, B, D=None, *, options=None, stream=None):
+    """D[M, N] = A[M, K] . B[K, N] (FP16/BF16, FP32 accumulation)."""
+    return gemm_run(A, B, D, layout=LAYOUT_AB, options=options, stream=stream)
+
+
+def gemm_run_ptr(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: int, ldd: int,
+                 dtype: int, layout: int = LAYOUT_ABT, options=None, stream: int = 0) -> int:
+    """The raw C call on integer addresses; returns the status code."""
+    return load().gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, layout, _options(options),
+                           stream)
+
+
+def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOUT_ABT,
+              options=None) -> dict:
+    """The tile shape and persistent grid a call would use on the current device."""
+    vals = [ctypes.c_int() for _ in range(5)]
+    tiles = ctypes.c_int64()
+    st = load().gemm_plan(M, N, K, dtype, layout, _options(options),
+                          *[ctypes.byref(v) for v in vals], ctypes.byref(tiles))
+    if st != 0:
+        raise GemmError(st, "gemm_plan")
+    keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
+    out = {k: v.value for k, v in zip(keys, vals)}
+    out["num_tiles"] = tiles.value
+    return out
+
+
+def gemm_tile_origin(M: int, N: int, block_m: int, block_n: int, group: int, task: int):
+    """(m0, n0) of the tile the persistent scheduler assigns to `task`."""
+    m0, n0 = ctypes.c_int64(), ctypes.c_int64()
+    st = load().gemm_tile_origin(M, N, block_m, block_n, group, task, ctypes.byref(m0),
+                                 ctypes.byref(n0))
+    if st != 0:
+        raise GemmError(st, "gemm_tile_origin")
+    return m0.value, n0.value
+
+
+def gemm_device_status(clear: bool = True) -> int:
+    """Synchronise and return the device error word (0 = no kernel wait gave up)."""
+    v = ctypes.c_uint32()
+    st = load().gemm_device_status(ctypes.byref(v), int(bool(clear)))
+    if st != 0:
+        raise GemmError(st, "gemm_device_status")
+    return v.value
+
+
+def gemm_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the failure-path self-test (a bounded wait that must run out)."""
+    import torch
+
+    st = load().gemm_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, torch.device("cuda")))
+    if st != 0:
+        raise GemmError(st, "gemm_selftest_wait_timeout")

@@ -1,0 +1,397 @@
+// gemm_api.cu -- the C ABI of include/gemm.h: validation, TMA tensor maps,
+// plan selection and the launch of the sm_103a kernel.
+//
+// The host builds three TMA tensor maps per call (A, B, D), picks the tile
+// configuration and sizes a persistent grid of as many co-resident clusters as
+// the device holds (capped by the tile count), then launches once on the
+// caller's stream with the cluster dimension as a launch attribute.  This is
+// the only host -> device step of a call.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+#include <utility>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// ---- driver entry point for tensor-map encoding ----------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major 2-D tensor of 16-bit elements: `inner` contiguous elements per row,
+// `outer` rows, row stride `ld` elements; boxes of box_inner x box_outer,
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_2d(CUtensorMap* map, const void* ptr, int dtype, uint64_t inner, uint64_t outer,
+               uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * 2u};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// ---- per-device facts, cached -------------------------------------------------
+
+struct DeviceInfo {
+    bool valid = false;
+    bool supported = false;
+    int sm_count = 0;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device(DeviceInfo* out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& di = g_dev[dev];
+    if (!di.valid) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        di.supported = (major == 10 && minor == 3);
+        di.sm_count = sms;
+        di.valid = true;
+    }
+    *out = di;
+    return di.supported ? GEMM_OK : GEMM_ERR_DEVICE;
+}
+
+// ---- kernel variants -----------------------------------------------------------
+
+template <class C>
+void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                    const GemmArgs& args, int clusters, cudaStream_t stream, cudaError_t* err) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(clusters * C::CG), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args);
+}
+
+// Co-resident clusters for a variant on the current device (queried once).
+template <class C>
+int query_max_clusters(int dev, int sm_count) {
+    const void* fn = reinterpret_cast<const void*>(gemm_tcgen05_kernel<C>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+        return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(C::CG * (sm_count / C::CG)), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return -1;
+    (void)dev;
+    return n;
+}
+
+// Stage counts: as many 128-byte-swizzled K slices as fit next to the
+// 32 KiB epilogue staging in 227 KiB.
+template <int CG, int BN>
+struct Stages;
+template <> struct Stages<2, 256> { static constexpr int value = 6; };  // 32 KiB / stage
+template <> struct Stages<1, 256> { static constexpr int value = 4; };  // 48 KiB / stage
+template <> struct Stages<2, 128> { static constexpr int value = 8; };  // 24 KiB / stage
+template <> struct Stages<1, 128> { static constexpr int value = 6; };  // 32 KiB / stage
+
+template <int CG, int BN, bool B_MN, bool BF16>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN>::value, B_MN, BF16>;
+
+struct Plan {
+    int cg, bm, bn, stages;
+    int clusters;
+    int64_t tiles;
+    int group;
+};
+
+template <class C>
+int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream) {
+    CUtensorMap ma, mb, md;
+    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, 128))
+        return GEMM_ERR_CUDA;
+    if constexpr (!C::B_MN) {
+        if (!encode_2d(&mb, B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, C::B_ROWS))
+            return GEMM_ERR_CUDA;
+    } else {
+        if (!encode_2d(&mb, B, dtype, uint64_t(N), uint64_t(K), uint64_t(ldb), 64, kBlockK))
+            return GEMM_ERR_CUDA;
+    }
+    if (!encode_2d(&md, D, dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
+        return GEMM_ERR_CUDA;
+    GemmArgs args;
+    args.M = int32_t(M);
+    args.N = int32_t(N);
+    args.K = int32_t(K);
+    args.k_blocks = int32_t((K + kBlockK - 1) / kBlockK);
+    args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
+    args.grid.n_tiles = int32_t((N + C::BN - 1) / C::BN);
+    args.grid.group = p.group;
+    cudaError_t err;
+    launch_variant<C>(ma, mb, md, args, p.clusters, stream, &err);
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Dispatch on (cta_group, block_n, layout, dtype) to one template instance.
+template <template <class> class Fn, class... Ts>
+int dispatch(int cg, int bn, bool b_mn, bool bf16, Ts&&... ts) {
+#define GB300_CASE(CG_, BN_, MN_, BF_)                                                   \
+    if (cg == CG_ && bn == BN_ && b_mn == MN_ && bf16 == BF_)                            \
+        return Fn<Cfg<CG_, BN_, MN_, BF_>>::call(std::forward<Ts>(ts)...);
+#define GB300_CASES(CG_, BN_) \
+    GB300_CASE(CG_, BN_, false, false) GB300_CASE(CG_, BN_, false, true) \
+    GB300_CASE(CG_, BN_, true, false) GB300_CASE(CG_, BN_, true, true)
+    GB300_CASES(2, 256)
+    GB300_CASES(1, 256)
+    GB300_CASES(2, 128)
+    GB300_CASES(1, 128)
+#undef GB300_CASES
+#undef GB300_CASE
+    return GEMM_ERR_OPTION;
+}
+
+template <class C>
+struct QueryFn {
+    static int call(int dev, int sms, int* out) {
+        static int cache[kMaxDevices] = {0};
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (cache[dev] == 0) {
+            const int n = query_max_clusters<C>(dev, sms);
+            if (n <= 0) return GEMM_ERR_CUDA;
+            cache[dev] = n;
+        }
+        *out = cache[dev];
+        return GEMM_OK;
+    }
+};
+
+template <class C>
+struct RunFn {
+    static int call(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                    cudaStream_t stream) {
+        return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, dtype, stream);
+    }
+};
+
+int check_sizes(int64_t M, int64_t N, int64_t K, int dtype, int b_layout) {
+    if (dtype != GEMM_F16 && dtype != GEMM_BF16) return GEMM_ERR_DTYPE;
+    if (b_layout != 0 && b_layout != 1) return GEMM_ERR_OPTION;
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return GEMM_ERR_SHAPE;
+    return GEMM_OK;
+}
+
+int check_options(const gemm_options_t* o) {
+    if (!o) return GEMM_OK;
+    if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_OPTION;
+    if (o->block_n != 0 && o->block_n != 128 && o->block_n != 256) return GEMM_ERR_OPTION;
+    if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
+    return GEMM_OK;
+}
+
+// Choose the tile shape and grid.  Needs the current device (for its SM count
+// and cluster occupancy).
+int make_plan(int64_t M, int64_t N, int dtype, int b_layout, const gemm_options_t* o,
+              Plan* p) {
+    DeviceInfo di;
+    int st = current_device(&di);
+    if (st != GEMM_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    p->cg = (o && o->cta_group) ? o->cta_group : (M <= 128 ? 1 : 2);
+    p->bn = (o && o->block_n) ? o->block_n : 256;
+    p->bm = 128 * p->cg;
+    p->group = (o && o->raster_group) ? o->raster_group : 16;
+    const int64_t m_tiles = (M + p->bm - 1) / p->bm;
+    const int64_t n_tiles = (N + p->bn - 1) / p->bn;
+    p->tiles = m_tiles * n_tiles;
+    if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
+    int max_clusters = 0;
+    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, dev, di.sm_count,
+                           &max_clusters);
+    if (st != GEMM_OK) return st;
+    if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
+    p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
+    if (p->cg == 2 && p->bn == 256) p->stages = Stages<2, 256>::value;
+    else if (p->cg == 1 && p->bn == 256) p->stages = Stages<1, 256>::value;
+    else if (p->cg == 2) p->stages = Stages<2, 128>::value;
+    else p->stages = Stages<1, 128>::value;
+    return GEMM_OK;
+}
+
+bool overlaps(const void* a, int64_t rows_a, int64_t cols_a, int64_t ld_a, const void* b,
+              int64_t rows_b, int64_t cols_b, int64_t ld_b) {
+    if (rows_a == 0 || cols_a == 0 || rows_b == 0 || cols_b == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t a1 = a0 + uintptr_t(((rows_a - 1) * ld_a + cols_a) * 2);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
+    const uintptr_t b1 = b0 + uintptr_t(((rows_b - 1) * ld_b + cols_b) * 2);
+    return a0 < b1 && b0 < a1;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+                        const gemm_options_t* opts, cudaStream_t stream) {
+    int st = check_sizes(M, N, K, dtype, b_layout);
+    if (st != GEMM_OK) return st;
+    if ((st = check_options(opts)) != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    const int64_t b_rows = b_layout == 0 ? N : K;
+    const int64_t b_cols = b_layout == 0 ? K : N;
+    if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
+    if (ldd < N || ldd <= 0) return GEMM_ERR_SHAPE;
+    if (K > 0 && (lda < K || ldb < b_cols || lda <= 0 || ldb <= 0)) return GEMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(D) & 15u) || (ldd & 7)) return GEMM_ERR_ALIGN;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+                  (lda & 7) || (ldb & 7)))
+        return GEMM_ERR_ALIGN;
+    if (K > 0 && (overlaps(D, M, N, ldd, A, M, K, lda) || overlaps(D, M, N, ldd, B, b_rows, b_cols, ldb)))
+        return GEMM_ERR_ALIAS;
+
+    if (K == 0) {
+        DeviceInfo di;
+        if ((st = current_device(&di)) != GEMM_OK) return st;
+        const int64_t total = M * N;
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > 4L * di.sm_count * 8) blocks = 4L * di.sm_count * 8;
+        zero_fill_kernel<<<unsigned(blocks), 256, 0, stream>>>(static_cast<uint16_t*>(D), M, N, ldd);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    Plan p;
+    if ((st = make_plan(M, N, dtype, b_layout, opts, &p)) != GEMM_OK) return st;
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p, A, B, D, M, N, K,
+                           lda, ldb, ldd, dtype, stream);
+}
+
+extern "C" int gemm_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream) {
+    return gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, 0, nullptr, stream);
+}
+
+extern "C" int gemm_ab(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream) {
+    return gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, 1, nullptr, stream);
+}
+
+extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
+                         const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
+                         int* stages, int* num_clusters, int64_t* num_tiles) {
+    int st = check_sizes(M, N, K, dtype, b_layout);
+    if (st != GEMM_OK) return st;
+    if ((st = check_options(opts)) != GEMM_OK) return st;
+    Plan p;
+    if ((st = make_plan(M, N, dtype, b_layout, opts, &p)) != GEMM_OK) return st;
+    if (cta_group) *cta_group = p.cg;
+    if (block_m) *block_m = p.bm;
+    if (block_n) *block_n = p.bn;
+    if (stages) *stages = p.stages;
+    if (num_clusters) *num_clusters = p.clusters;
+    if (num_tiles) *num_tiles = p.tiles;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
+                                int64_t task, int64_t* m0, int64_t* n0) {
+    if (M <= 0 || N <= 0 || block_m <= 0 || block_n <= 0 || group <= 0 || M > INT32_MAX ||
+        N > INT32_MAX)
+        return GEMM_ERR_SHAPE;
+    TileGrid g;
+    g.m_tiles = int32_t((M + block_m - 1) / block_m);
+    g.n_tiles = int32_t((N + block_n - 1) / block_n);
+    g.group = group;
+    if (task < 0 || task >= tile_count(g)) return GEMM_ERR_SHAPE;
+    int32_t mt, nt;
+    tile_of_task(g, task, mt, nt);
+    if (m0) *m0 = int64_t(mt) * block_m;
+    if (n0) *n0 = int64_t(nt) * block_n;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_device_status(uint32_t* status, int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof v) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (clear) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof zero) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    if (status) *status = v;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+    DeviceInfo di;
+    const int st = current_device(&di);
+    if (st != GEMM_OK) return st;
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+extern "C" const char* gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_NULL: return "null pointer";
+        case GEMM_ERR_DTYPE: return "unsupported dtype (GEMM_F16 or GEMM_BF16)";
+        case GEMM_ERR_SHAPE: return "invalid size or leading dimension";
+        case GEMM_ERR_ALIGN: return "pointer not 16-byte aligned or leading dimension not a multiple of 8";
+        case GEMM_ERR_ALIAS: return "output overlaps an input";
+        case GEMM_ERR_CUDA: return "CUDA call failed";
+        case GEMM_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case GEMM_ERR_OPTION: return "unsupported option";
+        case GEMM_ERR_TIMEOUT: return "a kernel wait timed out";
+        default: return "unknown status";
+    }
+}

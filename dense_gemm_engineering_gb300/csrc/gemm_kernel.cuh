@@ -1,0 +1,425 @@
+// gemm_kernel.cuh -- the sm_103a dense GEMM kernel (tcgen05 + TMA + TMEM).
+//
+// One persistent, warp-specialised kernel computes D = A.B^T (B stored N x K,
+// K-major) or D = A.B (B stored K x N, MN-major) with FP16/BF16 operands, an
+// FP32 accumulator in Tensor Memory and a 16-bit output.
+//
+// Structure, and the passages it follows:
+//   * Operands move GMEM -> SMEM by TMA into a ring of STAGES slots, 128-byte
+//     swizzled ("TIRx GEMM on Blackwell", V4 and V5; TileFoundry tutorial,
+//     section 5: SW128 TMA ring).  Stage s of the ring carries k-blocks
+//     s, s + STAGES, ...; the ring position and its phase bit run on across
+//     tiles (TileFoundry tutorial, section 6: the ring slot is a function of
+//     the running k-block count, not of the tile).
+//   * Four kinds of mbarrier hand buffers between the roles ("TIRx GEMM on
+//     Blackwell", V7): full[s] (operands landed, TMA -> MMA), empty[s] (slot
+//     free, MMA -> TMA), acc_full[b] (accumulator b ready, MMA -> epilogue),
+//     acc_empty[b] (accumulator b drained, epilogue -> MMA).  A waiter on a
+//     "free" barrier starts on the opposite parity, so the first pass through
+//     the ring does not block; every reuse flips the phase bit (V2, V7).
+//   * Warp 0: TMA producer (one thread).  Warp 1: allocates TMEM and, in the
+//     cluster's leader CTA, issues tcgen05.mma from one thread.  Warps 2-5:
+//     epilogue warpgroup (V7's writeback warpgroup).
+//   * Persistent CTAs walk the tile list of schedule.h (V6; TileFoundry
+//     sections 2-3).
+//   * CG == 2: a cluster of two CTAs computes a 256-row tile with
+//     tcgen05.mma.cta_group::2; CTA r holds rows 128r..128r+127 of the tile in
+//     its own TMEM, loads its own 128 rows of A and its own half of B's tile
+//     columns, and the leader's MMA reads both CTAs' shared memory (V8).
+//   * The accumulator is double-buffered in TMEM (2 x BN columns), so the
+//     epilogue of tile i overlaps the mainloop of tile i+1 ("write back without
+//     blocking the next tile", Take away 1).
+//   * Epilogue: tcgen05.ld -> FP32 registers -> cvt.rn to 16 bit -> 128-byte
+//     swizzled SMEM staging (two buffers per warp, outside the load ring) ->
+//     TMA store, which clips rows/columns outside D (TileFoundry section 5).
+//     D is never cleared: every tile is written exactly once (section 6).
+//
+// Every barrier wait is bounded (kWaitLimitNs).  A wait that runs out records
+// the reason in the device status word, raises a CTA-local abort flag that
+// the other roles poll, and all roles leave their loops; the CTA still frees
+// TMEM and takes part in the final cluster barrier, so the context survives.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace gb300 {
+
+// Device status word (read by gemm_device_status()).
+static __device__ uint32_t g_gemm_status;
+
+constexpr int kBlockK = 64;         // 64 x 16 bit = one 128-byte swizzle row
+constexpr int kNumThreads = 192;    // 6 warps: producer, MMA, 4 epilogue
+constexpr int kEpilogueWarps = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// Status word layout: bits 0..7 = reason, bits 8..15 = role.
+enum : uint32_t { kReasonTimeout = 1u };
+enum : uint32_t {
+    kRoleProducer = 1u,
+    kRoleMma = 2u,
+    kRoleEpilogue = 3u,
+    kRoleDrain = 4u,
+    kRoleSelfTest = 5u
+};
+
+template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_>
+struct KernelConfig {
+    static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
+    static constexpr int BM = 128 * CG;       // tile rows (MMA M)
+    static constexpr int BN = BN_;            // tile columns (MMA N)
+    static constexpr int STAGES = STAGES_;    // SMEM ring depth
+    static constexpr bool B_MN = B_MN_;       // B stored K x N (D = A.B)
+    static constexpr bool BF16 = BF16_;
+    static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
+
+    static constexpr uint32_t A_BYTES = 128u * kBlockK * 2u;            // 16 KiB
+    static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * kBlockK * 2u;
+    static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES);
+    static constexpr uint32_t TMEM_COLS = 2u * BN;                     // 2 accumulators
+    static constexpr uint32_t EPI_BUF_BYTES = 32u * 128u;              // 32 rows x 64 cols
+    static constexpr uint32_t MN_ATOM_BYTES = 64u * 128u;              // MN-major: 64 K x 64 N
+
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * 2u * EPI_BUF_BYTES;
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8u;
+    static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4u;
+    static constexpr uint32_t SMEM_USED = OFF_ABORT + 4u;
+    static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024u;  // slack to align the base
+
+    // tcgen05 instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1),
+    // A/B = F16 (0) or BF16 (1) at bits 7-9 / 10-12, A K-major (bit 15 = 0),
+    // B major at bit 16, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+    static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 0u) << 7) |
+                                      ((BF16 ? 1u : 0u) << 10) | ((B_MN ? 1u : 0u) << 16) |
+                                      (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+    static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
+    static_assert(BN == 128 || BN == 256, "tile N is 128 or 256");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
+    static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
+    static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
+    static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
+};
+
+struct GemmArgs {
+    int32_t M, N, K;
+    int32_t k_blocks;  // ceil(K / 64)
+    TileGrid grid;
+};
+
+// tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
+// start address >> 4 (bits 0-13), leading-dimension byte offset >> 4 (16-29),
+// stride-dimension byte offset >> 4 (32-45), the fixed version value 1 at bits
+// 46-48, base offset 0 (atoms are 1 KiB aligned), swizzle mode 2 = 128 B at
+// bits 61-63.
+//   K-major (A, and B of A.B^T): rows of 128 B = 64 K elements; SBO = 1 KiB
+//     between groups of 8 rows; LBO unused (one MMA reads 32 B of K, inside
+//     the swizzle row).  The k-th K=16 slice starts 32 B further.
+//   MN-major (B of A.B): rows of 128 B = 64 N elements, one row per k; SBO =
+//     1 KiB between groups of 8 k rows; LBO = 8 KiB between 64-column atoms.
+//     The k-th K=16 slice starts 16 rows = 2 KiB further.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = uint64_t((addr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+
+__device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint32_t role) {
+    *abort_flag = 1u;
+    atomicCAS(&g_gemm_status, 0u, kReasonTimeout | (role << 8));
+}
+
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs or when another
+// role of this CTA has aborted.  Returns false on give-up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag, uint32_t role,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 7u) == 0u) {
+            if (*abort_flag) return false;
+            if (ptx::global_timer_ns() - t0 > limit_ns) {
+                raise_abort(abort_flag, role);
+                return false;
+            }
+        }
+    }
+}
+
+// After an abort: give in-flight asynchronous copies and MMAs (which complete
+// in microseconds) time to land before shared memory and TMEM are released.
+__device__ __forceinline__ void settle_after_abort() {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (ptx::global_timer_ns() - t0 < 1000000ull) __nanosleep(10000);
+}
+
+template <class C>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
+    const uint32_t lane = threadIdx.x % 32u;
+    const uint32_t rank = (C::CG == 2) ? ptx::cluster_ctarank() : 0u;
+    const bool leader = (rank == 0u);
+    const int64_t cluster_id = blockIdx.x / C::CG;
+    const int64_t num_clusters = gridDim.x / C::CG;
+    const int64_t tiles = tile_count(args.grid);
+    const int kb_count = args.k_blocks;
+
+    auto full_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * (C::STAGES + s); };
+    auto acc_full_bar = [&](uint32_t b) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + b); };
+    auto acc_empty_bar = [&](uint32_t b) {
+        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
+    };
+    volatile uint32_t* const abort_flag =
+        reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
+
+    // ---- one-time setup -------------------------------------------------
+    if (warp == 0 && lane == 0) {
+        for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
+            ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
+            ptx::mbar_init(empty_bar(s), 1);  // one tcgen05.commit per use
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            ptx::mbar_init(acc_full_bar(b), 1);                          // one commit
+            ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
+        }
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+        ptx::prefetch_tensormap(&tmap_d);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<C::CG>(base + C::OFF_TMEM_SLOT, C::TMEM_COLS);
+        ptx::tmem_relinquish<C::CG>();
+    }
+    ptx::tc_fence_before();
+    if constexpr (C::CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
+
+    if (warp == 0) {
+        // ---- TMA producer ---------------------------------------------------
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            bool ok = true;
+            for (int64_t t = cluster_id; t < tiles && ok; t += num_clusters) {
+                int32_t mt, nt;
+                tile_of_task(args.grid, t, mt, nt);
+                const int32_t a_row = mt * C::BM + int32_t(rank) * 128;
+                const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_TX);
+                    const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
+                    const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
+                    const int32_t k0 = kb * kBlockK;
+                    if constexpr (C::CG == 1) {
+                        ptx::tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, a_row);
+                        if constexpr (!C::B_MN) {
+                            ptx::tma_load_2d(b_dst, &tmap_b, full_bar(s), k0, b_row);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < C::B_ROWS / 64; ++c)
+                                ptx::tma_load_2d(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, full_bar(s),
+                                                 b_row + 64 * c, k0);
+                        }
+                    } else {
+                        const uint32_t fb = ptx::map_to_rank(full_bar(s), 0);
+                        ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
+                        if constexpr (!C::B_MN) {
+                            ptx::tma_load_2d_pair(b_dst, &tmap_b, fb, k0, b_row);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < C::B_ROWS / 64; ++c)
+                                ptx::tma_load_2d_pair(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, fb,
+                                                      b_row + 64 * c, k0);
+                        }
+                    }
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (ok) {
+                // Drain: every slot must have been released by the MMA, so no
+                // tcgen05.commit arrives on this CTA's barriers after it exits.
+                for (int i = 0; i < C::STAGES; ++i) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleDrain)) {
+                        ok = false;
+                        break;
+                    }
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) settle_after_abort();
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer (leader CTA, one thread) ---------------------------
+        if (leader && lane == 0) {
+            uint32_t s = 0, ph = 0, ab = 0, aph = 0;
+            bool ok = true;
+            for (int64_t t = cluster_id; t < tiles && ok; t += num_clusters) {
+                if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + ab * uint32_t(C::BN);
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = base + C::OFF_A + s * C::A_BYTES;
+                    const uint32_t b_addr = base + C::OFF_B + s * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < kBlockK / 16; ++k) {
+                        const uint64_t ad = sw128_desc(a_addr + 32u * k, 16u, 1024u);
+                        const uint64_t bd = C::B_MN
+                                                ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
+                                                : sw128_desc(b_addr + 32u * k, 16u, 1024u);
+                        ptx::mma_f16<C::CG>(d_tmem, ad, bd, C::IDESC, uint32_t((kb | k) != 0));
+                    }
+                    ptx::mma_commit<C::CG>(empty_bar(s));  // slot free once these MMAs finish
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit<C::CG>(acc_full_bar(ab));  // accumulator ready
+                if (++ab == 2u) { ab = 0; aph ^= 1u; }
+            }
+            if (ok) {
+                // Drain: both accumulators released by every epilogue warp of the
+                // cluster (the peer's arrivals target this CTA's barriers).
+                for (int i = 0; i < 2; ++i) {
+                    if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
+                        ok = false;
+                        break;
+                    }
+                    if (++ab == 2u) { ab = 0; aph ^= 1u; }
+                }
+            }
+            if (!ok) settle_after_abort();
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue warps 2..5 ----------------------------------------------
+        const uint32_t quarter = warp & 3u;  // this warp may read TMEM lanes 32q..32q+31
+        const uint32_t buf0 = base + C::OFF_EPI + (warp - 2u) * 2u * C::EPI_BUF_BYTES;
+        uint32_t ab = 0, aph = 0, chunk = 0;
+        for (int64_t t = cluster_id; t < tiles; t += num_clusters) {
+            int32_t mt, nt;
+            tile_of_task(args.grid, t, mt, nt);
+            uint32_t ok = 1u;
+            if (lane == 0) ok = wait_bounded(acc_full_bar(ab), aph, abort_flag, kRoleEpilogue);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            while (!ptx::mbar_try_wait(acc_full_bar(ab), aph)) {
+            }  // completed already: gives every lane its own acquire
+            ptx::tc_fence_after();
+
+            const int32_t row0 = mt * C::BM + int32_t(rank) * 128 + int32_t(quarter) * 32;
+            const int32_t col0 = nt * C::BN;
+            const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * uint32_t(C::BN);
+#pragma unroll 1
+            for (int j = 0; j < C::BN / 64; ++j) {
+                uint32_t lo[32], hi[32];
+                ptx::tmem_ld_32x32b_x32(taddr + 64u * j, lo);
+                ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u, hi);
+                ptx::tmem_wait_ld();
+                if (j == C::BN / 64 - 1) {
+                    // All TMEM reads of this accumulator are done: hand it back.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (C::CG == 2)
+                            ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(ab), 0));
+                        else
+                            ptx::mbar_arrive(acc_empty_bar(ab));
+                    }
+                }
+                const uint32_t buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
+                if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
+                __syncwarp();
+                // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
+                // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
+                const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t* v = (c < 4) ? &lo[8 * c] : &hi[8 * (c - 4)];
+                    const uint32_t p0 = ptx::pack2<C::BF16>(v[0], v[1]);
+                    const uint32_t p1 = ptx::pack2<C::BF16>(v[2], v[3]);
+                    const uint32_t p2 = ptx::pack2<C::BF16>(v[4], v[5]);
+                    const uint32_t p3 = ptx::pack2<C::BF16>(v[6], v[7]);
+                    ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ (lane & 7u)) << 4), p0, p1, p2, p3);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t col = col0 + 64 * j;
+                    if (row0 < args.M && col < args.N) ptx::tma_store_2d(&tmap_d, buf, col, row0);
+                    ptx::bulk_commit_group();  // one group per chunk, even if empty
+                }
+                ++chunk;
+            }
+            if (++ab == 2u) { ab = 0; aph ^= 1u; }
+        }
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---- teardown ---------------------------------------------------------
+    ptx::tc_fence_before();
+    if constexpr (C::CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Failure-path self-test: one thread waits, through wait_bounded, on a
+// barrier that nothing arrives on; the wait must give up after `limit_ns` and
+// record (kReasonTimeout | kRoleSelfTest << 8) in the status word.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0u;
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        ptx::fence_mbar_init();
+        wait_bounded(ptx::smem_addr(&bar), 0u, &abort_flag, kRoleSelfTest, limit_ns);
+    }
+}
+
+// D = 0 for K == 0 (the empty sum).  One thread per 16-bit element.
+__global__ void zero_fill_kernel(uint16_t* __restrict__ d, int64_t M, int64_t N, int64_t ldd) {
+    const int64_t total = M * N;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        d[(i / N) * ldd + (i % N)] = 0;
+    }
+}
+
+}  // namespace gb300

@@ -1,0 +1,150 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library (libgb300gemm.so).
+ *
+ * The operation ("TIRx GEMM on Blackwell", section "The short version"):
+ *
+ *     D = A . B^T      A: M x K, B: N x K, D: M x N            (gemm_abt)
+ *     D = A . B        A: M x K, B: K x N, D: M x N            (gemm_ab)
+ *
+ * The A.B form is the program of "Choosing schedules and instructions for a
+ * backend" (TileFoundry tutorial), section 1: gemm(a: (M, K), b: (K, N)).
+ *
+ * A, B and D share one 16-bit storage type (FP16 or BF16).  Products are
+ * accumulated in FP32 in Blackwell Tensor Memory and each output is rounded
+ * once (round to nearest even) to the 16-bit type.  The order of the FP32
+ * additions is unspecified: it depends on the tiling, not on the values.
+ *
+ * Layout.  Every matrix is row-major with a leading dimension (row stride)
+ * given in ELEMENTS: element (i, j) of A is A[i * lda + j].  Requirements,
+ * which come from the Tensor Memory Accelerator that moves every tile:
+ *   - A, B and D are device pointers, 16-byte aligned;
+ *   - lda, ldb and ldd are multiples of 8 elements (16 bytes);
+ *   - lda >= K, ldb >= K (gemm_abt) or ldb >= N (gemm_ab), ldd >= N;
+ *   - M, N and K are at most 2^31 - 1.
+ * Violations return an error code; nothing is launched.  There is no slower
+ * fallback path.
+ *
+ * Ownership.  The caller allocates and owns A, B and D.  The library allocates
+ * no device memory on any call: tile descriptors travel as kernel parameters.
+ * D is written and never read, so it need not be initialised.  D must not
+ * overlap A or B (GEMM_ERR_ALIAS).
+ *
+ * Stream semantics.  Work is enqueued on `stream` (0 = the legacy default
+ * stream) and the call returns without synchronising; results are visible to
+ * later work on the same stream.  The current CUDA device must be the device
+ * that holds the buffers.
+ *
+ * Degenerate sizes.  M == 0 or N == 0: nothing to do, returns GEMM_OK.
+ * K == 0: D is filled with zeros (the empty sum), as torch.mm does.
+ *
+ * Errors.  Every entry point returns GEMM_OK (0) or a negative status;
+ * gemm_status_string() gives its text.  A launch error is GEMM_ERR_CUDA.
+ * Errors that occur while the kernel runs are reported asynchronously through
+ * gemm_device_status() (see below).
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
+
+enum {
+    GEMM_OK = 0,
+    GEMM_ERR_NULL = -1,    /* a null pointer with a non-empty extent           */
+    GEMM_ERR_DTYPE = -2,   /* dtype is not GEMM_F16 / GEMM_BF16                 */
+    GEMM_ERR_SHAPE = -3,   /* negative or too-large size, or ld < row length   */
+    GEMM_ERR_ALIGN = -4,   /* pointer not 16-B aligned or ld not a multiple of 8 */
+    GEMM_ERR_ALIAS = -5,   /* D overlaps A or B                                 */
+    GEMM_ERR_CUDA = -6,    /* a CUDA runtime or driver call failed              */
+    GEMM_ERR_DEVICE = -7,  /* the current device is not an sm_103 GPU           */
+    GEMM_ERR_OPTION = -8,  /* an unsupported gemm_options_t value               */
+    GEMM_ERR_TIMEOUT = -9  /* a kernel wait gave up (see gemm_device_status)    */
+};
+
+/* D[M x N] = A[M x K] . B[N x K]^T, all row-major (ld in elements). */
+int gemm_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream);
+
+/* D[M x N] = A[M x K] . B[K x N], all row-major (ld in elements). */
+int gemm_ab(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+            int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream);
+
+/* Text for a status code; never NULL, static storage. */
+const char* gemm_status_string(int status);
+
+/*
+ * Tuning and test controls.  gemm_abt/gemm_ab are gemm_run with opts = NULL.
+ *   cta_group     0 = automatic, 1 = one CTA per 128-row tile (tcgen05
+ *                 cta_group::1), 2 = a 2-CTA cluster per 256-row tile
+ *                 (cta_group::2, the two CTAs' tensor cores act as one).
+ *   block_n       0 = automatic, else the N extent of a tile: 128 or 256.
+ *   raster_group  0 = automatic, else the number of M tiles per raster group
+ *                 of the persistent scheduler (tiles are visited group by
+ *                 group, N-major inside a group, so consecutive tiles share B).
+ *   max_clusters  0 = as many co-resident clusters as fit, else an upper bound
+ *                 on the persistent grid (in clusters).
+ */
+typedef struct {
+    int cta_group;
+    int block_n;
+    int raster_group;
+    int max_clusters;
+} gemm_options_t;
+
+/* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */
+int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+             const gemm_options_t* opts, cudaStream_t stream);
+
+/*
+ * Plan of a call, without launching: the tile shape, grid and stage count
+ * gemm_run would use for these sizes on the current device.  Any out pointer
+ * may be NULL.  Returns the same argument errors as gemm_run (pointers are not
+ * checked).
+ */
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
+              const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
+              int* stages, int* num_clusters, int64_t* num_tiles);
+
+/*
+ * The persistent scheduler's task -> tile map (the same function the kernel
+ * runs), for host-side checks.  Tiles of block_m x block_n cover the M x N
+ * output; `group` M tiles form a raster group.  Writes the tile's first row
+ * and column.  Returns GEMM_ERR_SHAPE if task is outside [0, tiles).
+ */
+int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
+                     int64_t task, int64_t* m0, int64_t* n0);
+
+/*
+ * Device-side error word of the current device.  Every wait inside the kernel
+ * is bounded (about 2 s); a wait that runs out makes the kernel record the
+ * reason here, end all of its loops, release Tensor Memory and return, so the
+ * CUDA context stays usable.  The word is bits 0-7 = reason (1 = timeout),
+ * bits 8-15 = role that gave up (1 producer, 2 MMA issuer, 3 epilogue,
+ * 4 end-of-kernel drain, 5 self-test).  Synchronises the device, then writes the word
+ * to *status (0 = no error since the last clear) and clears it if `clear`.
+ * Returns GEMM_OK or GEMM_ERR_CUDA.
+ */
+int gemm_device_status(uint32_t* status, int clear);
+
+/*
+ * Self-test of that failure path.  Launches one thread that waits, through
+ * the same bounded wait the GEMM kernel uses, on an mbarrier that nothing
+ * ever arrives on, with a limit of `limit_ns` nanoseconds.  The wait runs
+ * out and records 0x501 (reason 1 = timeout, role 5 = self-test) in the
+ * device status word; the context stays usable.  Touches no user memory.
+ * Returns GEMM_OK once launched, GEMM_ERR_DEVICE or GEMM_ERR_CUDA otherwise.
+ */
+int gemm_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -76,6 +76,20 @@ double oracle_to_double(uint16_t bits, int dtype) {
     return dtype == ORACLE_BF16 ? bf16_bits_to_double(bits) : f16_bits_to_double(bits);
 }
 
+/* The same decode, tabulated once for all 65536 patterns of each type, so the
+ * GEMM loop below does not pay a libm call per operand. */
+static double g_decode[2][65536];
+static int g_decode_ready = 0;
+
+static void build_decode_tables(void) {
+    if (g_decode_ready) return;
+    for (uint32_t b = 0; b < 65536u; ++b) {
+        g_decode[ORACLE_F16][b] = oracle_to_double((uint16_t)b, ORACLE_F16);
+        g_decode[ORACLE_BF16][b] = oracle_to_double((uint16_t)b, ORACLE_BF16);
+    }
+    g_decode_ready = 1;
+}
+
 /* ---- encode: binary64 -> 16-bit pattern, round to nearest, ties to even ---
  *
  * Generic for a format with `ebits` exponent bits and `fbits` fraction bits.
@@ -129,14 +143,15 @@ void oracle_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int
                  uint16_t* out16, double* out_f64, int64_t ldo) {
     (void)M;
     (void)N;
+    build_decode_tables(); /* before the parallel region: written by one thread */
+    const double* dec = g_decode[dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_F16];
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = i0; i < i1; ++i) {
         for (int64_t j = j0; j < j1; ++j) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) {
-                double a = oracle_to_double(A[i * lda + k], dtype);
-                double b = (b_layout == ORACLE_B_NK) ? oracle_to_double(B[j * ldb + k], dtype)
-                                                     : oracle_to_double(B[k * ldb + j], dtype);
+                double a = dec[A[i * lda + k]];
+                double b = (b_layout == ORACLE_B_NK) ? dec[B[j * ldb + k]] : dec[B[k * ldb + j]];
                 acc += a * b;
             }
             int64_t o = (i - i0) * ldo + (j - j0);

@@ -1,0 +1,150 @@
+"""The C ABI without a GPU: exported symbols, argument checks, scheduler map.
+
+Argument validation runs before any CUDA call, so these checks need no GPU.
+The scheduler tests pin the tile counts the pages print.
+"""
+import ctypes
+import re
+
+import pytest
+
+from dense_gemm_engineering_gb300 import binding, build
+
+HEADER = build.INCLUDE + "/gemm.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert binding.gemm_status_string(code)
+    assert binding.gemm_status_string(12345) == "unknown status"
+
+
+P = 0x10000  # fake, 16-byte aligned "device" addresses: never dereferenced
+Q = 0x40000000
+R = 0x80000000
+
+
+def call(A=P, B=Q, D=R, M=128, N=128, K=64, lda=64, ldb=64, ldd=128, dtype=0, layout=0, opts=None):
+    return binding.gemm_run_ptr(A, B, D, M, N, K, lda, ldb, ldd, dtype, layout, opts, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=2), -2),
+    (dict(dtype=-1), -2),
+    (dict(M=-1), -3),
+    (dict(K=-5), -3),
+    (dict(N=2 ** 31), -3),
+    (dict(A=0), -1),
+    (dict(B=0), -1),
+    (dict(D=0), -1),
+    (dict(lda=32), -3),          # lda < K
+    (dict(ldd=64), -3),          # ldd < N
+    (dict(layout=1, ldb=64), -3),  # A.B: ldb < N
+    (dict(A=P + 8), -4),
+    (dict(D=R + 2), -4),
+    (dict(lda=68, K=64), -4),    # not a multiple of 8
+    (dict(ldd=130), -4),
+    (dict(D=P + 64), -5),        # D overlaps A
+    (dict(D=Q), -5),             # D overlaps B
+    (dict(layout=2), -8),
+    (dict(opts={"cta_group": 3, "block_n": 0, "raster_group": 0, "max_clusters": 0}), -8),
+    (dict(opts={"cta_group": 0, "block_n": 192, "raster_group": 0, "max_clusters": 0}), -8),
+])
+def test_argument_errors(lib, kw, status):
+    assert call(**kw) == status
+
+
+@pytest.mark.parametrize("kw", [dict(M=0), dict(N=0), dict(M=0, A=0, B=0, D=0)])
+def test_empty_output_is_a_no_op(lib, kw):
+    assert call(**kw) == 0
+
+
+def test_k_zero_needs_no_inputs_but_validates_output(lib):
+    assert call(K=0, A=0, B=0, D=0) == -1
+    assert call(K=0, A=0, B=0, D=R + 2) == -4
+
+
+# ---- the persistent scheduler's task -> tile map ---------------------------
+
+def cover(M, N, bm, bn, group):
+    tiles = -(-M // bm) * -(-N // bn)
+    seen = [binding.gemm_tile_origin(M, N, bm, bn, group, t) for t in range(tiles)]
+    return tiles, seen
+
+
+@pytest.mark.parametrize("M,N,bm,bn,group", [
+    (4096, 4096, 128, 128, 16),   # "TIRx GEMM on Blackwell", V3: 32 x 32 = 1,024 tiles
+    (4096, 4096, 256, 256, 16),
+    (3000, 5000, 256, 256, 16),   # ragged: last group and last tiles partial
+    (3000, 5000, 128, 256, 7),
+    (8192, 17408, 256, 256, 16),
+    (300, 100, 128, 128, 1),
+])
+def test_every_tile_exactly_once(lib, M, N, bm, bn, group):
+    tiles, seen = cover(M, N, bm, bn, group)
+    expect = {(m, n) for m in range(0, M, bm) for n in range(0, N, bn)}
+    assert len(seen) == tiles == len(expect)
+    assert set(seen) == expect
+
+
+def test_v3_tile_count(lib):
+    # "TIRx GEMM on Blackwell", V3: 4096 x 4096 with 128 x 128 tiles -> 32 x 32 = 1,024.
+    tiles, _ = cover(4096, 4096, 128, 128, 16)
+    assert tiles == 1024
+    with pytest.raises(binding.GemmError):
+        binding.gemm_tile_origin(4096, 4096, 128, 128, 16, 1024)
+    # V6: 148 persistent CTAs each take about 1024 / 148 = 6.9 tiles.
+    per_cta = [len(range(c, tiles, 148)) for c in range(148)]
+    assert sum(per_cta) == 1024 and min(per_cta) == 6 and max(per_cta) == 7
+    assert round(1024 / 148, 1) == 6.9
+
+
+def test_tilefoundry_group16_order(lib):
+    # "Choosing schedules and instructions for a backend", sections 1 and 3:
+    # 8192 x 17408 with 128 x 256 tiles is a 64 x 68 grid of 4352 tiles; with
+    # 132 resident CTAs a one-tile-per-CTA launch needs 33 waves.  The G = 16
+    # order maps task -> g = task // (68*16), bn = (task // 16) % 68,
+    # mi = task % 16, m = (g*16 + mi) * 128, n = bn * 256.
+    M, N, BM, BN, G, GN = 8192, 17408, 128, 256, 16, 68
+    tiles, seen = cover(M, N, BM, BN, G)
+    assert tiles == 4352 == 64 * 68
+    assert -(-4352 // 132) == 33
+    for task in list(range(0, 4352, 37)) + [4351]:
+        g, bn, mi = task // (GN * G), (task // G) % GN, task % G
+        assert seen[task] == ((g * G + mi) * BM, bn * BN)
+
+
+def test_smem_carve_up_is_disjoint():
+    # The kernel's shared-memory plan (ring of A slots, ring of B slots,
+    # epilogue staging, barriers) mirrors the TileFoundry tutorial's disjoint
+    # intervals (section 6: [0, 98304), [98304, 147456), [147456, 212992)).
+    for cg, bn, stages in ((2, 256, 6), (1, 256, 4), (2, 128, 8), (1, 128, 6)):
+        a = 128 * 64 * 2
+        b = (bn // cg) * 64 * 2
+        spans = [(0, stages * a), (stages * a, stages * (a + b)),
+                 (stages * (a + b), stages * (a + b) + 4 * 2 * 32 * 128)]
+        for (s0, e0), (s1, e1) in zip(spans, spans[1:]):
+            assert e0 == s1 and s0 < e0
+        assert spans[-1][1] + (2 * stages + 4) * 8 + 8 + 1024 <= 232448

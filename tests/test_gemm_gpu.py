@@ -1,0 +1,245 @@
+"""GPU parity: the sm_103a kernel through the C ABI against the CPU oracle.
+
+Every case draws seeded inputs, runs the CUDA path (binding -> libgb300gemm.so)
+and compares element by element with the oracle on the same 16-bit inputs,
+within |got - ref| <= 1e-2 + rtol * |ref| (rtol 1e-3 for FP16 output, 8e-3 for
+BF16 output).  Small-integer cases, whose FP32 sums are exact, must match the
+oracle bit for bit.  The five workloads are checked at full size in the launch
+configuration the benchmark uses: in full where the oracle takes seconds, and
+on seeded whole-tile samples (every scheduler position and ring stage/phase at
+tile start) for the 8192 x 17408 x 5120 shape.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_engineering_gb300 import binding, build, configs, inputs
+from gpu_util import check_close, decode, from_device, sample_tiles, to_device
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [
+    {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0},
+    {"cta_group": 1, "block_n": 256, "raster_group": 0, "max_clusters": 0},
+    {"cta_group": 2, "block_n": 128, "raster_group": 0, "max_clusters": 0},
+    {"cta_group": 1, "block_n": 128, "raster_group": 0, "max_clusters": 0},
+]
+VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.load()
+    major, minor = torch.cuda.get_device_capability(0)
+    assert (major, minor) == (10, 3), f"expected an sm_103 GPU, got sm_{major}{minor}"
+    torch.cuda.set_device(0)
+    yield
+    assert binding.gemm_device_status(clear=True) == 0
+
+
+def run(A_bits, B_bits, layout, dtype, options=None, D=None):
+    A = to_device(A_bits, dtype)
+    B = to_device(B_bits, dtype)
+    fn = binding.gemm_abt if layout == "abt" else binding.gemm_ab
+    out = fn(A, B, D, options=options)
+    torch.cuda.synchronize()
+    return out
+
+
+def parity(M, N, K, layout, dtype, dist="uniform", seed=0, options=None, lda=None, ldb=None):
+    A, B = inputs.operands(M, N, K, layout, dtype, dist, seed, lda=lda, ldb=ldb)
+    got = from_device(run(A, B, layout, dtype, options))
+    ref, ref64 = oracle.gemm(A, B, layout=layout, dtype=dtype, want_f64=True)
+    return check_close(got, ref, dtype, f"{M}x{N}x{K} {layout} {dtype} {options}", ref64)
+
+
+# ---- exact small-integer cases first: any layout/descriptor slip shows here --
+
+def small_int_operands(M, N, K, layout, dtype, seed):
+    rng = np.random.default_rng(seed)
+    lim = 2
+    Ai = rng.integers(-lim, lim + 1, size=(M, K)).astype(np.float32)
+    Bi = rng.integers(-lim, lim + 1, size=(N, K) if layout == "abt" else (K, N)).astype(np.float32)
+    if dtype == "f16":
+        enc = lambda x: x.astype(np.float16).view(np.uint16)
+    else:
+        enc = inputs.f32_to_bf16_bits
+    return np.ascontiguousarray(enc(Ai)), np.ascontiguousarray(enc(Bi))
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VID)
+@pytest.mark.parametrize("layout", ["abt", "ab"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_exact_small_integers(variant, layout, dtype):
+    # |D| <= 4 * 64 = 256: exact in FP32 and in both output types.
+    M, N, K = 256, 256, 64
+    A, B = small_int_operands(M, N, K, layout, dtype, seed=1)
+    got = from_device(run(A, B, layout, dtype, variant))
+    ref = oracle.gemm(A, B, layout=layout, dtype=dtype)
+    assert np.array_equal(got, ref)
+
+
+def test_identity_single_tile():
+    # D = A . I^T = A on one 128 x 128 x 128 tile.
+    M = N = K = 128
+    A = inputs.matrix(5, 0, M, K, "f16", "uniform")
+    eye = np.eye(K, dtype=np.float16).view(np.uint16)
+    got = from_device(run(A, eye, "abt", "f16"))
+    assert np.array_equal(got, A)
+
+
+# ---- the five workloads ---------------------------------------------------------
+
+def config_case(cfg):
+    return inputs.operands(cfg.M, cfg.N, cfg.K, cfg.layout, cfg.dtype, cfg.dist, cfg.seed)
+
+
+@pytest.mark.parametrize("cfg", configs.CONFIGS[:2], ids=lambda c: c.name)
+def test_small_configs_full(cfg):
+    A, B = config_case(cfg)
+    got = from_device(run(A, B, cfg.layout, cfg.dtype))
+    ref, ref64 = oracle.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, want_f64=True)
+    check_close(got, ref, cfg.dtype, cfg.name, ref64)
+
+
+@pytest.mark.parametrize("cfg", [configs.CONFIGS[4], configs.CONFIGS[2]], ids=lambda c: c.name)
+def test_large_configs_full(cfg):
+    A, B = config_case(cfg)
+    got = from_device(run(A, B, cfg.layout, cfg.dtype))
+    ref, ref64 = oracle.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, want_f64=True)
+    check_close(got, ref, cfg.dtype, cfg.name, ref64)
+
+
+def test_rect_bf16_ab_sampled_tiles():
+    cfg = configs.CONFIGS[3]
+    A, B = config_case(cfg)
+    got = from_device(run(A, B, cfg.layout, cfg.dtype))
+    plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, binding.GEMM_BF16, binding.LAYOUT_AB)
+    bm, bn = plan["block_m"], plan["block_n"]
+    group = min(16, -(-cfg.M // bm))
+    tiles = sample_tiles(cfg.M, cfg.N, cfg.K, bm, bn, group, plan["num_clusters"], plan["stages"],
+                         lambda t: binding.gemm_tile_origin(cfg.M, cfg.N, bm, bn, group, t))
+    assert len(tiles) >= plan["num_clusters"]
+    for (m0, n0) in tiles:
+        m1, n1 = min(m0 + bm, cfg.M), min(n0 + bn, cfg.N)
+        ref, ref64 = oracle.gemm(A, B, layout="ab", dtype="bf16", rows=(m0, m1), cols=(n0, n1),
+                                 want_f64=True)
+        check_close(got[m0:m1, n0:n1], ref, "bf16", f"tile ({m0},{n0})", ref64)
+    # every output must have been written (no NaN/garbage outside the sample):
+    # D = A.B with |entries| bounded by the operand norms
+    vals = decode(got, "bf16")
+    assert np.isfinite(vals).all() and np.abs(vals).max() < 1.0
+
+
+# ---- shapes, strides and edge cases, every variant ---------------------------
+
+SHAPES = [
+    (128, 128, 64),     # one tile, one k-block
+    (256, 256, 1024),   # 16 k-blocks: several ring wraps
+    (300, 200, 200),    # ragged M, N and K
+    (129, 520, 136),    # one row past a tile; K not a multiple of 64
+    (1, 8, 8),          # smallest legal sizes
+    (64, 96, 24),       # K < 64 (zero-filled tail of the only k-block)
+    (520, 264, 4000),   # K tail of 32 after 62 full blocks
+    (1000, 1000, 512),  # many tiles per cluster with few clusters capped below
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VID)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout,dtype", [("abt", "f16"), ("ab", "bf16"), ("abt", "bf16"),
+                                          ("ab", "f16")])
+def test_shapes(variant, shape, layout, dtype):
+    M, N, K = shape
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=M + N + K,
+           options=variant)
+
+
+@pytest.mark.parametrize("max_clusters", [1, 3, 7])
+def test_few_clusters_many_tiles(max_clusters):
+    # Each cluster walks many tiles: the ring position and both TMEM
+    # accumulators are reused across tiles many times.
+    opts = {"cta_group": 2, "block_n": 256, "raster_group": 2, "max_clusters": max_clusters}
+    parity(1024, 1280, 320, "abt", "f16", seed=max_clusters, options=opts)
+
+
+def test_long_k():
+    parity(256, 512, 32768, "abt", "f16", seed=3)
+
+
+@pytest.mark.parametrize("layout", ["abt", "ab"])
+def test_strided_operands_and_guarded_output(layout):
+    # Row strides above the row length; the padding holds NaN (any read of it
+    # poisons the result).  D is a view inside a larger buffer filled with a
+    # sentinel, which must survive outside D.
+    M, N, K = 300, 200, 136
+    A, B = inputs.operands(M, N, K, layout, "f16", "uniform", 9, lda=K + 24,
+                           ldb=(K + 8) if layout == "abt" else (N + 56))
+    sentinel = 0x5A5A
+    ldd = N + 40
+    buf = torch.full((M + 3, ldd), sentinel, dtype=torch.int16, device="cuda")
+    D = buf.view(torch.float16)[1:M + 1, 8:8 + N]
+    run(A, B, layout, "f16", D=D)
+    host = buf.cpu().numpy().view(np.uint16)
+    inside = np.zeros_like(host, dtype=bool)
+    inside[1:M + 1, 8:8 + N] = True
+    assert (host[~inside] == sentinel).all()
+    ref = oracle.gemm(A, B, layout=layout, dtype="f16")
+    check_close(host[1:M + 1, 8:8 + N], ref, "f16", "strided")
+
+
+def test_k_zero_writes_zeros():
+    buf = torch.full((40, 56), 7.0, dtype=torch.float16, device="cuda")
+    D = buf[:, :48]
+    A = torch.empty((40, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((48, 0), dtype=torch.float16, device="cuda")
+    binding.gemm_abt(A, B, D)
+    torch.cuda.synchronize()
+    assert (buf[:, :48] == 0).all() and (buf[:, 48:] == 7.0).all()
+
+
+def test_empty_output_is_a_no_op():
+    A = torch.ones((0, 64), dtype=torch.float16, device="cuda")
+    B = torch.ones((32, 64), dtype=torch.float16, device="cuda")
+    D = binding.gemm_abt(A, B)
+    assert D.shape == (0, 32)
+
+
+def test_argument_errors_on_device_buffers():
+    A = torch.zeros((128, 72), dtype=torch.float16, device="cuda")
+    B = torch.zeros((128, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A[:, 1:65], B)  # base pointer off by 2 bytes
+    assert e.value.status == -4
+    buf = torch.zeros(256 * 128, dtype=torch.float16, device="cuda")
+    A2 = buf[:128 * 64].view(128, 64)
+    D2 = buf[64 * 64:64 * 64 + 128 * 128].view(128, 128)  # overlaps A2
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A2, B, D2)
+    assert e.value.status == -5
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A[:, :64].float(), B.float())
+    assert e.value.status == -2
+
+
+def test_deterministic_and_stream_ordered():
+    A, B = inputs.operands(512, 768, 1024, "abt", "f16", "uniform", 11)
+    dA, dB = to_device(A, "f16"), to_device(B, "f16")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d1 = binding.gemm_abt(dA, dB)
+        d2 = binding.gemm_abt(dA, dB)
+    s.synchronize()
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    assert binding.gemm_device_status(clear=True) == 0
+    binding.gemm_selftest_wait_timeout(20_000_000)  # 20 ms
+    assert binding.gemm_device_status(clear=True) == 0x501
+    assert binding.gemm_device_status(clear=True) == 0
+    parity(256, 256, 256, "abt", "f16", seed=5)

@@ -17,16 +17,18 @@ MUTANTS = {
     "sign": ("acc += a * b;", "acc -= a * b;"),
     "dropped_last_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
     "dropped_first_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
-    "b_transposed_in_abt": ("oracle_to_double(B[j * ldb + k], dtype)", "oracle_to_double(B[k * ldb + j], dtype)"),
-    "b_transposed_in_ab": ("oracle_to_double(B[k * ldb + j], dtype)", "oracle_to_double(B[j * ldb + k], dtype)"),
-    "a_wrong_stride": ("A[i * lda + k]", "A[i * K + k]"),
+    "b_transposed_in_abt": ("? dec[B[j * ldb + k]]", "? dec[B[k * ldb + j]]"),
+    "b_transposed_in_ab": (": dec[B[k * ldb + j]]", ": dec[B[j * ldb + k]]"),
+    "a_wrong_stride": ("dec[A[i * lda + k]]", "dec[A[i * K + k]]"),
     "accumulate_binary32": ("double acc = 0.0;", "float acc = 0.0f;"),
     "round_toward_zero": ("double q = nearbyint(ldexp(a, fbits - e));", "double q = trunc(ldexp(a, fbits - e));"),
     "ties_away": ("double q = nearbyint(ldexp(a, fbits - e));", "double q = round(ldexp(a, fbits - e));"),
     "f16_bias": ("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
     "subnormal_scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     "no_overflow_to_inf": ("if (field >= emax_field) return sign | inf;", "if (field > emax_field) return sign | inf;"),
-    "b_k_reversed": ("oracle_to_double(B[j * ldb + k], dtype)", "oracle_to_double(B[j * ldb + (K - 1 - k)], dtype)"),
+    "b_k_reversed": ("? dec[B[j * ldb + k]]", "? dec[B[j * ldb + (K - 1 - k)]]"),
+    "dtype_table_swapped": ("g_decode[dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_F16]",
+                            "g_decode[dtype == ORACLE_BF16 ? ORACLE_F16 : ORACLE_BF16]"),
     "bf16_read_as_f16": ("return dtype == ORACLE_BF16 ? bf16_bits_to_double(bits) : f16_bits_to_double(bits);",
                          "return f16_bits_to_double(bits);"),
 }
