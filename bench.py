@@ -157,7 +157,73 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons),
+                "source": "nvidia-smi -lms 200 during the timed region"}
+
+
+class NvmlSampler:
+    """Polls the SM clock, clock-event reasons and power of one GPU through
+    NVML (libnvidia-ml, the library nvidia-smi reads) every ~2 ms on a thread,
+    so that even a timed region of a few milliseconds is sampled."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise OSError("nvmlDeviceGetHandleByUUID failed")
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _read(self):
+        ct = self.ct
+        mhz, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz))  # NVML_CLOCK_SM
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ct.byref(mx))
+        self.nvml.nvmlDeviceGetPowerUsage(self.dev, ct.byref(mw))
+        self.reasons_fn(self.dev, ct.byref(rs))
+        return mhz.value, mx.value, mw.value / 1000.0, rs.value
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            self.samples.append(self._read())
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self):
+        self.stop_evt.set()
+        self.thread.join()
+        self.samples.append(self._read())
+        sm = [s[0] for s in self.samples]
+        reasons = set()
+        for s in self.samples:
+            for bit, name in self.REASONS.items():
+                if s[3] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": max(s[1] for s in self.samples), "samples": len(sm),
+                "power_w_max": max(s[2] for s in self.samples), "reasons": sorted(reasons),
+                "source": "NVML polled every ~2 ms during the timed region"}
+
+
+def clock_sampler(uuid: str):
+    try:
+        return NvmlSampler(uuid)
+    except (OSError, AttributeError):
+        return ClockSampler(uuid)
 
 
 def make_inputs(cfg):
@@ -262,7 +328,7 @@ def run_ours(args, cfg):
         raise RuntimeError("device status word set during warm-up")
 
     props = torch.cuda.get_device_properties(dev)
-    sampler = None if args.no_clocks else ClockSampler(f"GPU-{props.uuid}")
+    sampler = None if args.no_clocks else clock_sampler(f"GPU-{props.uuid}")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
