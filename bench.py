@@ -62,6 +62,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks of the default process group."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (slowest_ms / 1e3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -347,16 +364,13 @@ def run_ours(args, cfg):
     barrier()
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per_launch_ms) / len(per_launch_ms)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     status = binding.gemm_device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status word {status:#x} after the timed region")
 
     flops = 2.0 * cfg.M * cfg.N * cfg.K
-    value = world * flops / (ms / 1e3) / 1e12
+    value = job_throughput(flops, world, ms)
     achieved = flops / (ms / 1e3) / 1e12
 
     # ---- end to end through the public API, host buffers -------------------------
@@ -384,11 +398,8 @@ def run_ours(args, cfg):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        e2e = {"value": job_throughput(flops, world, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "steps": n_e2e,
                "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                "d2h_bytes_per_step": int(cfg.M * cfg.N * 2),

@@ -1,0 +1,83 @@
+"""bench.py host logic without a GPU: the multi-rank reduction (gloo, 2 ranks),
+the reference arm's rank handling, and the ncu traffic lookup."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = [0.5, 0.8][rank]
+    slowest = bench.max_over_ranks(local_ms, world, "cpu")
+    value = bench.job_throughput(2.0 * 4096 ** 3, world, slowest)
+    out.put((rank, slowest, value))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_job_throughput():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, slowest, value in res:
+        assert slowest == 0.8  # the slower rank's time
+        assert value == pytest.approx(2 * 2.0 * 4096 ** 3 / 0.8e-3 / 1e12)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--config",
+                        "kloop_256x256x1024_f16_abt"], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
+    assert line["metric"] == bench.METRIC and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_lookup_matches_only_current_kernel(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash()
+    assert len(h) == 12
+    pdir = tmp_path / "profiles"
+    pdir.mkdir()
+    (pdir / "x.md").write_text(
+        f"bench-traffic: workload=w1 kernel={h} bytes_per_launch=123\n"
+        f"bench-traffic: workload=w1 kernel=000000000000 bytes_per_launch=999\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("w1", h) == 123
+    assert bench.recorded_traffic("w2", h) is None
+    assert bench.recorded_traffic("w1", "ffffffffffff") is None
