@@ -26,11 +26,13 @@ STATUS_NAMES = {
     -7: "GEMM_ERR_DEVICE",
     -8: "GEMM_ERR_OPTION",
     -9: "GEMM_ERR_TIMEOUT",
+    -10: "GEMM_ERR_WORKSPACE",
 }
 
 # Every symbol include/gemm.h declares.
-EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_status_string", "gemm_plan",
-           "gemm_tile_origin", "gemm_device_status", "gemm_selftest_wait_timeout")
+EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_workspace_size",
+           "gemm_status_string", "gemm_plan", "gemm_tile_origin", "gemm_device_status",
+           "gemm_selftest_wait_timeout")
 
 
 class GemmError(RuntimeError):
@@ -43,7 +45,8 @@ class GemmError(RuntimeError):
 class GemmOptions(ctypes.Structure):
     """gemm_options_t."""
     _fields_ = [("cta_group", ctypes.c_int), ("block_n", ctypes.c_int),
-                ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int)]
+                ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
+                ("tail_split", ctypes.c_int)]
 
 
 _lib = None
@@ -72,11 +75,17 @@ def load(path: str | None = None):
     lib.gemm_run.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
                              ctypes.POINTER(GemmOptions), vp]
     lib.gemm_run.restype = c_int
+    lib.gemm_run_workspace.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                       ctypes.POINTER(GemmOptions), vp, ctypes.c_size_t, vp]
+    lib.gemm_run_workspace.restype = c_int
+    lib.gemm_workspace_size.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions),
+                                        ctypes.POINTER(ctypes.c_size_t)]
+    lib.gemm_workspace_size.restype = c_int
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(c_int)
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions), ip, ip,
-                              ip, ip, ip, ctypes.POINTER(i64)]
+                              ip, ip, ip, ctypes.POINTER(i64), ip]
     lib.gemm_plan.restype = c_int
     lib.gemm_tile_origin.argtypes = [i64, i64, c_int, c_int, c_int, i64, ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -133,11 +142,33 @@ def _stream_handle(stream, device) -> int:
     return int(s.cuda_stream)
 
 
-def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=None):
+# Workspaces for the split tail, one per (device, stream): calls on one stream
+# run in order, so they may share one; calls on different streams must not.
+_workspaces = {}
+
+
+def _workspace(device, stream_handle: int, nbytes: int):
+    import torch
+
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        # zeroed once when (re)allocated, as gemm_run_workspace requires
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=None,
+             workspace="auto"):
     """D = A.B^T (layout 0, B is N x K) or A.B (layout 1, B is K x N) on torch tensors.
 
     Allocates D with torch when not given.  Enqueues on `stream` (default: the
     current stream of A's device) and returns D without synchronising.
+    `workspace`: "auto" (a zero-initialised device buffer kept per device and
+    stream, sized by gemm_workspace_size), None (no workspace: the plain
+    persistent schedule), or a caller-owned uint8 CUDA tensor.
     """
     import torch
 
@@ -154,27 +185,58 @@ def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=Non
         D = torch.empty((M, N), dtype=A.dtype, device=A.device)
     elif D.dtype != A.dtype or tuple(D.shape) != (M, N):
         raise GemmError(-3, "D has the wrong dtype or shape")
-    st = load().gemm_run(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _ld(A), _ld(B),
-                         _ld(D), _dtype_code(A), int(layout), _options(options),
-                         _stream_handle(stream, A.device))
+    lib = load()
+    sh = _stream_handle(stream, A.device)
+    opts = _options(options)
+    dt = _dtype_code(A)
+    ws_ptr, ws_bytes = None, 0
+    if isinstance(workspace, str) and workspace == "auto":
+        need = ctypes.c_size_t()
+        st = lib.gemm_workspace_size(M, N, K, dt, int(layout), opts, ctypes.byref(need))
+        if st != 0:
+            raise GemmError(st, "gemm_workspace_size")
+        if need.value:
+            ws = _workspace(A.device, sh, need.value)
+            ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
+    elif workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.gemm_run_workspace(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _ld(A),
+                                _ld(B), _ld(D), dt, int(layout), opts, ws_ptr, ws_bytes, sh)
     if st != 0:
-        raise GemmError(st, "gemm_run")
+        raise GemmError(st, "gemm_run_workspace")
     return D
 
 
-def gemm_abt(A, B, D=None, *, options=None, stream=None):
+def gemm_abt(A, B, D=None, *, options=None, stream=None, workspace="auto"):
     """D[M, N] = A[M, K] . B[N, K]^T (FP16/BF16, FP32 accumulation)."""
-    return gemm_run(A, B, D, layout=LAYOUT_ABT, options=options, stream=stream)
+    return gemm_run(A, B, D, layout=LAYOUT_ABT, options=options, stream=stream,
+                    workspace=workspace)
 
 
-def gemm_ab(A, B, D=None, *, options=None, stream=None):
+def gemm_ab(A, B, D=None, *, options=None, stream=None, workspace="auto"):
     """D[M, N] = A[M, K] . B[K, N] (FP16/BF16, FP32 accumulation)."""
-    return gemm_run(A, B, D, layout=LAYOUT_AB, options=options, stream=stream)
+    return gemm_run(A, B, D, layout=LAYOUT_AB, options=options, stream=stream,
+                    workspace=workspace)
+
+
+def gemm_workspace_size(M: int, N: int, K: int, dtype: int = GEMM_F16,
+                        layout: int = LAYOUT_ABT, options=None) -> int:
+    """Bytes of workspace the split tail needs on the current device (0 = none)."""
+    need = ctypes.c_size_t()
+    st = load().gemm_workspace_size(M, N, K, dtype, layout, _options(options),
+                                    ctypes.byref(need))
+    if st != 0:
+        raise GemmError(st, "gemm_workspace_size")
+    return need.value
 
 
 def gemm_run_ptr(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: int, ldd: int,
-                 dtype: int, layout: int = LAYOUT_ABT, options=None, stream: int = 0) -> int:
+                 dtype: int, layout: int = LAYOUT_ABT, options=None, stream: int = 0,
+                 workspace: int = 0, workspace_bytes: int = 0) -> int:
     """The raw C call on integer addresses; returns the status code."""
+    if workspace:
+        return load().gemm_run_workspace(A, B, D, M, N, K, lda, ldb, ldd, dtype, layout,
+                                         _options(options), workspace, workspace_bytes, stream)
     return load().gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, layout, _options(options),
                            stream)
 
@@ -184,13 +246,16 @@ def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOU
     """The tile shape and persistent grid a call would use on the current device."""
     vals = [ctypes.c_int() for _ in range(5)]
     tiles = ctypes.c_int64()
+    split = ctypes.c_int()
     st = load().gemm_plan(M, N, K, dtype, layout, _options(options),
-                          *[ctypes.byref(v) for v in vals], ctypes.byref(tiles))
+                          *[ctypes.byref(v) for v in vals], ctypes.byref(tiles),
+                          ctypes.byref(split))
     if st != 0:
         raise GemmError(st, "gemm_plan")
     keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
     out = {k: v.value for k, v in zip(keys, vals)}
     out["num_tiles"] = tiles.value
+    out["tail_split"] = split.value
     return out
 
 

@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -148,11 +149,59 @@ struct Plan {
     int clusters;
     int64_t tiles;
     int group;
+    int64_t k_blocks;
+    // Split of the last, partial round of tiles along K (1 = none).
+    int64_t whole_units;  // tiles computed whole
+    int split;            // K-ranges per remaining ("tail") tile
+    size_t ws_counter_bytes, ws_partial_bytes;  // workspace the split needs
 };
+
+constexpr int kMaxSplit = 16;
+
+// Workspace layout for a split tail: one 8-byte counter per (tail tile, CTA,
+// epilogue warp), then (256-byte aligned) one FP32 partial of 32 x block_n per
+// (tail tile, CTA, epilogue warp, K-range).
+void size_split(Plan* p) {
+    const int64_t tail = p->tiles - p->whole_units;
+    const int64_t quads = tail * p->cg * kEpilogueWarps;
+    p->ws_counter_bytes = size_t(quads) * 8u;
+    p->ws_partial_bytes = (p->split > 1) ? size_t(quads) * p->split * 32u * p->bn * 4u : 0u;
+    if (p->split <= 1) p->ws_counter_bytes = 0;
+}
+
+size_t workspace_bytes_needed(const Plan& p) {
+    if (p.split <= 1) return 0;
+    return ((p.ws_counter_bytes + 255u) & ~size_t(255)) + p.ws_partial_bytes;
+}
+
+// Decide the split of the tail round.  With C clusters and T tiles the
+// persistent schedule runs floor(T / C) full rounds and a last round of
+// tail = T mod C tiles, leaving C - tail clusters idle.  Splitting each tail tile
+// into s = floor(C / tail) K-ranges (s >= 2) keeps those clusters busy and
+// shortens the last round about s-fold.  `requested`: 0 = automatic, 1 = never,
+// s >= 2 = that split whenever there is a tail.
+void plan_split(Plan* p, int requested, bool have_workspace) {
+    p->whole_units = p->tiles;
+    p->split = 1;
+    const int64_t tail = p->clusters > 0 ? p->tiles % p->clusters : 0;
+    if (have_workspace && tail > 0 && requested != 1) {
+        int64_t s = requested >= 2 ? requested : p->clusters / tail;
+        if (s > kMaxSplit) s = kMaxSplit;
+        if (s > p->k_blocks) s = p->k_blocks;
+        if (s >= 2) {
+            p->split = int(s);
+            p->whole_units = p->tiles - tail;
+        }
+    }
+    size_split(p);
+}
+
+std::atomic<uint32_t> g_epoch{0};
 
 template <class C>
 int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-             int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream) {
+             int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
+             cudaStream_t stream) {
     CUtensorMap ma, mb, md;
     if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, 128))
         return GEMM_ERR_CUDA;
@@ -173,6 +222,16 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
     args.grid.n_tiles = int32_t((N + C::BN - 1) / C::BN);
     args.grid.group = p.group;
+    args.whole_units = p.whole_units;
+    args.split = p.split;
+    args.epoch = g_epoch.fetch_add(1u) + 1u;
+    args.counters = nullptr;
+    args.partials = nullptr;
+    if (p.split > 1) {
+        char* ws = static_cast<char*>(workspace);
+        args.counters = reinterpret_cast<unsigned long long*>(ws);
+        args.partials = reinterpret_cast<float*>(ws + ((p.ws_counter_bytes + 255u) & ~size_t(255)));
+    }
     cudaError_t err;
     launch_variant<C>(ma, mb, md, args, p.clusters, stream, &err);
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -214,9 +273,9 @@ struct QueryFn {
 template <class C>
 struct RunFn {
     static int call(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N,
-                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
                     cudaStream_t stream) {
-        return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, dtype, stream);
+        return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, dtype, workspace, stream);
     }
 };
 
@@ -233,13 +292,14 @@ int check_options(const gemm_options_t* o) {
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_OPTION;
     if (o->block_n != 0 && o->block_n != 128 && o->block_n != 256) return GEMM_ERR_OPTION;
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
+    if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
 // Choose the tile shape and grid.  Needs the current device (for its SM count
 // and cluster occupancy).
-int make_plan(int64_t M, int64_t N, int dtype, int b_layout, const gemm_options_t* o,
-              Plan* p) {
+int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const gemm_options_t* o,
+              bool have_workspace, Plan* p) {
     DeviceInfo di;
     int st = current_device(&di);
     if (st != GEMM_OK) return st;
@@ -263,6 +323,8 @@ int make_plan(int64_t M, int64_t N, int dtype, int b_layout, const gemm_options_
     else if (p->cg == 1 && p->bn == 256) p->stages = Stages<1, 256>::value;
     else if (p->cg == 2) p->stages = Stages<2, 128>::value;
     else p->stages = Stages<1, 128>::value;
+    p->k_blocks = (K + kBlockK - 1) / kBlockK;
+    plan_split(p, o ? o->tail_split : 0, have_workspace);
     return GEMM_OK;
 }
 
@@ -281,9 +343,10 @@ bool overlaps(const void* a, int64_t rows_a, int64_t cols_a, int64_t ld_a, const
 
 using namespace gb300;
 
-extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-                        int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
-                        const gemm_options_t* opts, cudaStream_t stream) {
+extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                  int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                                  int b_layout, const gemm_options_t* opts, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
     int st = check_sizes(M, N, K, dtype, b_layout);
     if (st != GEMM_OK) return st;
     if ((st = check_options(opts)) != GEMM_OK) return st;
@@ -310,10 +373,34 @@ extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GEMM_ERR_WORKSPACE;
     Plan p;
-    if ((st = make_plan(M, N, dtype, b_layout, opts, &p)) != GEMM_OK) return st;
+    if ((st = make_plan(M, N, K, dtype, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
+        return st;
+    if (workspace_bytes < workspace_bytes_needed(p)) return GEMM_ERR_WORKSPACE;
     return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p, A, B, D, M, N, K,
-                           lda, ldb, ldd, dtype, stream);
+                           lda, ldb, ldd, dtype, workspace, stream);
+}
+
+extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+                        const gemm_options_t* opts, cudaStream_t stream) {
+    return gemm_run_workspace(A, B, D, M, N, K, lda, ldb, ldd, dtype, b_layout, opts, nullptr, 0,
+                              stream);
+}
+
+extern "C" int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
+                                   const gemm_options_t* opts, size_t* bytes) {
+    int st = check_sizes(M, N, K, dtype, b_layout);
+    if (st != GEMM_OK) return st;
+    if ((st = check_options(opts)) != GEMM_OK) return st;
+    if (!bytes) return GEMM_ERR_NULL;
+    *bytes = 0;
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    Plan p;
+    if ((st = make_plan(M, N, K, dtype, b_layout, opts, true, &p)) != GEMM_OK) return st;
+    *bytes = workspace_bytes_needed(p);
+    return GEMM_OK;
 }
 
 extern "C" int gemm_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
@@ -328,18 +415,19 @@ extern "C" int gemm_ab(const void* A, const void* B, void* D, int64_t M, int64_t
 
 extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
                          const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
-                         int* stages, int* num_clusters, int64_t* num_tiles) {
+                         int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split) {
     int st = check_sizes(M, N, K, dtype, b_layout);
     if (st != GEMM_OK) return st;
     if ((st = check_options(opts)) != GEMM_OK) return st;
     Plan p;
-    if ((st = make_plan(M, N, dtype, b_layout, opts, &p)) != GEMM_OK) return st;
+    if ((st = make_plan(M, N, K, dtype, b_layout, opts, true, &p)) != GEMM_OK) return st;
     if (cta_group) *cta_group = p.cg;
     if (block_m) *block_m = p.bm;
     if (block_n) *block_n = p.bn;
     if (stages) *stages = p.stages;
     if (num_clusters) *num_clusters = p.clusters;
     if (num_tiles) *num_tiles = p.tiles;
+    if (tail_split) *tail_split = p.split;
     return GEMM_OK;
 }
 
@@ -392,6 +480,7 @@ extern "C" const char* gemm_status_string(int status) {
         case GEMM_ERR_DEVICE: return "current device is not an sm_103 GPU";
         case GEMM_ERR_OPTION: return "unsupported option";
         case GEMM_ERR_TIMEOUT: return "a kernel wait timed out";
+        case GEMM_ERR_WORKSPACE: return "workspace smaller than gemm_workspace_size() or not 256-byte aligned";
         default: return "unknown status";
     }
 }

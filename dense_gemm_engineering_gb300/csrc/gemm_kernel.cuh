@@ -56,7 +56,7 @@ constexpr int kEpilogueWarps = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 // Status word layout: bits 0..7 = reason, bits 8..15 = role.
-enum : uint32_t { kReasonTimeout = 1u };
+enum : uint32_t { kReasonTimeout = 1u, kReasonCounter = 2u };
 enum : uint32_t {
     kRoleProducer = 1u,
     kRoleMma = 2u,
@@ -109,9 +109,49 @@ struct KernelConfig {
 
 struct GemmArgs {
     int32_t M, N, K;
-    int32_t k_blocks;  // ceil(K / 64)
+    int32_t k_blocks;   // ceil(K / 64)
     TileGrid grid;
+    // Work units.  Units [0, whole_units) are whole tiles (unit u = tile u).
+    // The remaining tiles ("tail" tiles, the last partial round of the
+    // persistent schedule) are each split into `split` K-ranges, one unit per
+    // range, so that clusters that would idle in that round share the work.
+    int64_t whole_units;
+    int32_t split;      // K-ranges per tail tile; 1 = no split
+    uint32_t epoch;     // tag of this launch for the tail counters
+    float* partials;    // split > 1: FP32 partial of each (tail tile, range, CTA, warp quarter)
+    unsigned long long* counters;  // split > 1: one per (tail tile, CTA, warp quarter)
 };
+
+struct WorkUnit {
+    int64_t tile;    // task index of the tile in the scheduler order
+    int32_t kb0;     // first k-block
+    int32_t kb1;     // one past the last k-block
+    int32_t range;   // K-range index of a tail tile, -1 for a whole tile
+    int64_t tail;    // index of the tail tile, -1 for a whole tile
+};
+
+__host__ __device__ __forceinline__ int64_t unit_count(const GemmArgs& a) {
+    return a.whole_units + (tile_count(a.grid) - a.whole_units) * a.split;
+}
+
+__host__ __device__ __forceinline__ WorkUnit unit_of(const GemmArgs& a, int64_t u) {
+    WorkUnit w;
+    if (u < a.whole_units) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = a.k_blocks;
+        w.range = -1;
+        w.tail = -1;
+    } else {
+        const int64_t v = u - a.whole_units;
+        w.tail = v / a.split;
+        w.range = int32_t(v - w.tail * a.split);
+        w.tile = a.whole_units + w.tail;
+        w.kb0 = int32_t((int64_t(w.range) * a.k_blocks) / a.split);
+        w.kb1 = int32_t((int64_t(w.range + 1) * a.k_blocks) / a.split);
+    }
+    return w;
+}
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
 // start address >> 4 (bits 0-13), leading-dimension byte offset >> 4 (16-29),
@@ -164,6 +204,24 @@ __device__ __forceinline__ void settle_after_abort() {
     while (ptx::global_timer_ns() - t0 < 1000000ull) __nanosleep(10000);
 }
 
+// Count one finished K-range of a tail tile.  The counter word holds
+// (epoch << 32 | count); a word tagged with another launch's epoch counts as
+// zero, so the workspace never needs clearing between launches.  Returns the
+// number of ranges counted before this one (split - 1 means "this was the
+// last").  No thread ever waits for another here.
+__device__ __forceinline__ uint32_t count_range_done(unsigned long long* word, uint32_t epoch) {
+    unsigned long long old = atomicAdd(word, 0ull);
+    for (int i = 0; i < (1 << 20); ++i) {
+        const uint32_t cnt = (uint32_t(old >> 32) == epoch) ? uint32_t(old) : 0u;
+        const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+        const unsigned long long seen = atomicCAS(word, old, want);
+        if (seen == old) return cnt;
+        old = seen;
+    }
+    atomicCAS(&g_gemm_status, 0u, kReasonCounter);
+    return 0xFFFFFFFFu;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -180,8 +238,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const bool leader = (rank == 0u);
     const int64_t cluster_id = blockIdx.x / C::CG;
     const int64_t num_clusters = gridDim.x / C::CG;
-    const int64_t tiles = tile_count(args.grid);
-    const int kb_count = args.k_blocks;
+    const int64_t units = unit_count(args);
 
     auto full_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * s; };
     auto empty_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * (C::STAGES + s); };
@@ -199,7 +256,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(empty_bar(s), 1);  // one tcgen05.commit per use
         }
         for (uint32_t b = 0; b < 2; ++b) {
-            ptx::mbar_init(acc_full_bar(b), 1);                          // one commit
+            ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
             ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
         }
         *abort_flag = 0u;
@@ -222,12 +279,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             uint32_t s = 0, ph = 0;
             bool ok = true;
-            for (int64_t t = cluster_id; t < tiles && ok; t += num_clusters) {
+            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
+                const WorkUnit w = unit_of(args, u);
                 int32_t mt, nt;
-                tile_of_task(args.grid, t, mt, nt);
+                tile_of_task(args.grid, w.tile, mt, nt);
                 const int32_t a_row = mt * C::BM + int32_t(rank) * 128;
                 const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
-                for (int kb = 0; kb < kb_count; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
                         ok = false;
                         break;
@@ -280,14 +338,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (leader && lane == 0) {
             uint32_t s = 0, ph = 0, ab = 0, aph = 0;
             bool ok = true;
-            for (int64_t t = cluster_id; t < tiles && ok; t += num_clusters) {
+            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
+                const WorkUnit w = unit_of(args, u);
                 if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleMma)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * uint32_t(C::BN);
-                for (int kb = 0; kb < kb_count; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, abort_flag, kRoleMma)) {
                         ok = false;
                         break;
@@ -301,7 +360,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         const uint64_t bd = C::B_MN
                                                 ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
                                                 : sw128_desc(b_addr + 32u * k, 16u, 1024u);
-                        ptx::mma_f16<C::CG>(d_tmem, ad, bd, C::IDESC, uint32_t((kb | k) != 0));
+                        ptx::mma_f16<C::CG>(d_tmem, ad, bd, C::IDESC,
+                                            uint32_t(kb != w.kb0 || k != 0));
                     }
                     ptx::mma_commit<C::CG>(empty_bar(s));  // slot free once these MMAs finish
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
@@ -329,9 +389,59 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t quarter = warp & 3u;  // this warp may read TMEM lanes 32q..32q+31
         const uint32_t buf0 = base + C::OFF_EPI + (warp - 2u) * 2u * C::EPI_BUF_BYTES;
         uint32_t ab = 0, aph = 0, chunk = 0;
-        for (int64_t t = cluster_id; t < tiles; t += num_clusters) {
+
+        // Hand accumulator `b` back to the MMA issuer (all TMEM reads done).
+        auto release_acc = [&](uint32_t b) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (C::CG == 2)
+                    ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(b), 0));
+                else
+                    ptx::mbar_arrive(acc_empty_bar(b));
+            }
+        };
+        // 64 FP32 values of this lane's row -> 16-bit -> swizzled staging -> TMA
+        // store of the warp's 32 x 64 box at (col, row0).
+        auto store_chunk = [&](const float (&v)[64], int32_t col, int32_t row0) {
+            const uint32_t buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
+            __syncwarp();
+            // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
+            // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
+            const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t p0 = ptx::pack2<C::BF16>(v[8 * c + 0], v[8 * c + 1]);
+                const uint32_t p1 = ptx::pack2<C::BF16>(v[8 * c + 2], v[8 * c + 3]);
+                const uint32_t p2 = ptx::pack2<C::BF16>(v[8 * c + 4], v[8 * c + 5]);
+                const uint32_t p3 = ptx::pack2<C::BF16>(v[8 * c + 6], v[8 * c + 7]);
+                ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ (lane & 7u)) << 4), p0, p1, p2, p3);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < args.M && col < args.N) ptx::tma_store_2d(&tmap_d, buf, col, row0);
+                ptx::bulk_commit_group();  // one group per chunk, even if empty
+            }
+            ++chunk;
+        };
+        auto load_acc = [&](uint32_t taddr, float (&v)[64]) {
+            uint32_t lo[32], hi[32];
+            ptx::tmem_ld_32x32b_x32(taddr, lo);
+            ptx::tmem_ld_32x32b_x32(taddr + 32u, hi);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                v[i] = __uint_as_float(lo[i]);
+                v[32 + i] = __uint_as_float(hi[i]);
+            }
+        };
+
+        for (int64_t u = cluster_id; u < units; u += num_clusters) {
+            const WorkUnit w = unit_of(args, u);
             int32_t mt, nt;
-            tile_of_task(args.grid, t, mt, nt);
+            tile_of_task(args.grid, w.tile, mt, nt);
             uint32_t ok = 1u;
             if (lane == 0) ok = wait_bounded(acc_full_bar(ab), aph, abort_flag, kRoleEpilogue);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -343,46 +453,73 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int32_t row0 = mt * C::BM + int32_t(rank) * 128 + int32_t(quarter) * 32;
             const int32_t col0 = nt * C::BN;
             const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * uint32_t(C::BN);
+
+            if (w.range < 0) {
+                // Whole tile: TMEM -> D.
 #pragma unroll 1
-            for (int j = 0; j < C::BN / 64; ++j) {
-                uint32_t lo[32], hi[32];
-                ptx::tmem_ld_32x32b_x32(taddr + 64u * j, lo);
-                ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u, hi);
-                ptx::tmem_wait_ld();
-                if (j == C::BN / 64 - 1) {
-                    // All TMEM reads of this accumulator are done: hand it back.
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (C::CG == 2)
-                            ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(ab), 0));
-                        else
-                            ptx::mbar_arrive(acc_empty_bar(ab));
+                for (int j = 0; j < C::BN / 64; ++j) {
+                    float v[64];
+                    load_acc(taddr + 64u * j, v);
+                    if (j == C::BN / 64 - 1) release_acc(ab);
+                    store_chunk(v, col0 + 64 * j, row0);
+                }
+            } else {
+                // K-range of a tail tile.  Pass 1: write this range's FP32 partial
+                // for the warp's 32 rows to its workspace slot, laid out so that
+                // consecutive lanes touch consecutive 16-byte words.
+                const int64_t slot_stride = 32 * C::BN / 4;  // float4 per slot
+                const int64_t quad = (int64_t(w.tail) * C::CG + rank) * 4 + quarter;
+                float4* const slots = reinterpret_cast<float4*>(args.partials);
+                float4* const mine = slots + (quad * args.split + w.range) * slot_stride;
+#pragma unroll 1
+                for (int j = 0; j < C::BN / 64; ++j) {
+                    float v[64];
+                    load_acc(taddr + 64u * j, v);
+#pragma unroll
+                    for (int g = 0; g < 16; ++g)
+                        mine[(j * 16 + g) * 32 + lane] =
+                            make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                }
+                __threadfence();
+                __syncwarp();
+                uint32_t before = 0;
+                if (lane == 0) before = count_range_done(args.counters + quad, args.epoch);
+                before = __shfl_sync(0xffffffffu, before, 0);
+                if (before != uint32_t(args.split - 1)) {
+                    release_acc(ab);  // another range finishes this block of D
+                } else {
+                    // Pass 2 (the last range to finish): D = sum of all ranges'
+                    // partials in range order, this range's taken from TMEM.
+                    __threadfence();
+                    const float4* const first = slots + quad * args.split * slot_stride;
+#pragma unroll 1
+                    for (int j = 0; j < C::BN / 64; ++j) {
+                        float own[64], acc[64];
+                        load_acc(taddr + 64u * j, own);
+                        if (j == C::BN / 64 - 1) release_acc(ab);
+#pragma unroll 1
+                        for (int r = 0; r < args.split; ++r) {
+                            float part[64];
+                            if (r == w.range) {
+#pragma unroll
+                                for (int i = 0; i < 64; ++i) part[i] = own[i];
+                            } else {
+                                const float4* src = first + r * slot_stride;
+#pragma unroll
+                                for (int g = 0; g < 16; ++g) {
+                                    const float4 q = __ldcg(src + (j * 16 + g) * 32 + lane);
+                                    part[4 * g] = q.x;
+                                    part[4 * g + 1] = q.y;
+                                    part[4 * g + 2] = q.z;
+                                    part[4 * g + 3] = q.w;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) acc[i] = (r == 0) ? part[i] : acc[i] + part[i];
+                        }
+                        store_chunk(acc, col0 + 64 * j, row0);
                     }
                 }
-                const uint32_t buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
-                if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
-                __syncwarp();
-                // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
-                // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-                const uint32_t row_addr = buf + lane * 128u;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t* v = (c < 4) ? &lo[8 * c] : &hi[8 * (c - 4)];
-                    const uint32_t p0 = ptx::pack2<C::BF16>(v[0], v[1]);
-                    const uint32_t p1 = ptx::pack2<C::BF16>(v[2], v[3]);
-                    const uint32_t p2 = ptx::pack2<C::BF16>(v[4], v[5]);
-                    const uint32_t p3 = ptx::pack2<C::BF16>(v[6], v[7]);
-                    ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ (lane & 7u)) << 4), p0, p1, p2, p3);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int32_t col = col0 + 64 * j;
-                    if (row0 < args.M && col < args.N) ptx::tma_store_2d(&tmap_d, buf, col, row0);
-                    ptx::bulk_commit_group();  // one group per chunk, even if empty
-                }
-                ++chunk;
             }
             if (++ab == 2u) { ab = 0; aph ^= 1u; }
         }

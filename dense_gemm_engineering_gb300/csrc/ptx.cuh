@@ -251,8 +251,7 @@ __device__ __forceinline__ void tmem_wait_ld() {
 
 // Two FP32 -> packed 16-bit pair, round to nearest even; `lo` goes to bits 0..15.
 template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits) {
-    const float lo = __uint_as_float(lo_bits), hi = __uint_as_float(hi_bits);
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t d;
     if constexpr (BF16)
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));

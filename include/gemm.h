@@ -24,8 +24,9 @@
  * Violations return an error code; nothing is launched.  There is no slower
  * fallback path.
  *
- * Ownership.  The caller allocates and owns A, B and D.  The library allocates
- * no device memory on any call: tile descriptors travel as kernel parameters.
+ * Ownership.  The caller allocates and owns A, B, D (and the optional
+ * workspace of gemm_run_workspace).  The library allocates no device memory
+ * on any call: tile descriptors travel as kernel parameters.
  * D is written and never read, so it need not be initialised.  D must not
  * overlap A or B (GEMM_ERR_ALIAS).
  *
@@ -45,6 +46,7 @@
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -64,7 +66,8 @@ enum {
     GEMM_ERR_CUDA = -6,    /* a CUDA runtime or driver call failed              */
     GEMM_ERR_DEVICE = -7,  /* the current device is not an sm_103 GPU           */
     GEMM_ERR_OPTION = -8,  /* an unsupported gemm_options_t value               */
-    GEMM_ERR_TIMEOUT = -9  /* a kernel wait gave up (see gemm_device_status)    */
+    GEMM_ERR_TIMEOUT = -9, /* a kernel wait gave up (see gemm_device_status)    */
+    GEMM_ERR_WORKSPACE = -10 /* workspace too small or not 256-byte aligned     */
 };
 
 /* D[M x N] = A[M x K] . B[N x K]^T, all row-major (ld in elements). */
@@ -80,6 +83,7 @@ const char* gemm_status_string(int status);
 
 /*
  * Tuning and test controls.  gemm_abt/gemm_ab are gemm_run with opts = NULL.
+ * An all-zero gemm_options_t means "automatic" for every field.
  *   cta_group     0 = automatic, 1 = one CTA per 128-row tile (tcgen05
  *                 cta_group::1), 2 = a 2-CTA cluster per 256-row tile
  *                 (cta_group::2, the two CTAs' tensor cores act as one).
@@ -89,12 +93,17 @@ const char* gemm_status_string(int status);
  *                 group, N-major inside a group, so consecutive tiles share B).
  *   max_clusters  0 = as many co-resident clusters as fit, else an upper bound
  *                 on the persistent grid (in clusters).
+ *   tail_split    only with a workspace (gemm_run_workspace): 0 = automatic,
+ *                 1 = never, s in [2, 16] = split every tile of the last,
+ *                 partial round of the persistent schedule into s K-ranges
+ *                 (capped by the number of 64-wide k-blocks).
  */
 typedef struct {
     int cta_group;
     int block_n;
     int raster_group;
     int max_clusters;
+    int tail_split;
 } gemm_options_t;
 
 /* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */
@@ -103,14 +112,47 @@ int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
              const gemm_options_t* opts, cudaStream_t stream);
 
 /*
- * Plan of a call, without launching: the tile shape, grid and stage count
- * gemm_run would use for these sizes on the current device.  Any out pointer
- * may be NULL.  Returns the same argument errors as gemm_run (pointers are not
- * checked).
+ * The same GEMM with a caller-owned device workspace, which lets the kernel
+ * shorten the last, partial round of its persistent schedule: with C
+ * co-resident clusters and T tiles, the T mod C tiles of that round are each
+ * split into s K-ranges (s = floor(C / (T mod C)) when automatic) so the
+ * clusters that would idle share the work.  Each range writes an FP32
+ * partial to the workspace; the range that finishes last (found with an
+ * atomic counter, nobody waits) adds the partials in range order and writes D.
+ * Results are deterministic for a given plan.
+ *
+ * workspace        device memory, 256-byte aligned, at least
+ *                  gemm_workspace_size() bytes (0 means no split will happen
+ *                  for these sizes).  Zero it once before its first use;
+ *                  afterwards it may be reused by any number of calls, because
+ *                  every launch tags its counters with a fresh launch number.
+ *                  Calls that share a workspace must not run concurrently
+ *                  (different streams): they would race on it.
+ * workspace = NULL runs the plain persistent schedule (as gemm_run).
+ * Returns GEMM_ERR_WORKSPACE if the workspace is too small or misaligned.
+ */
+int gemm_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+                       const gemm_options_t* opts, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/*
+ * Bytes of workspace gemm_run_workspace needs for these sizes and options on
+ * the current device (written to *bytes; 0 = the call would not split).  At
+ * most (co-resident clusters) x 256 KiB plus a few KiB of counters.
+ */
+int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
+                        const gemm_options_t* opts, size_t* bytes);
+
+/*
+ * Plan of a call, without launching: the tile shape, grid, stage count and
+ * tail split gemm_run_workspace (with a large enough workspace) would use for
+ * these sizes on the current device.  Any out pointer may be NULL.  Returns
+ * the same argument errors as gemm_run (pointers are not checked).
  */
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
               const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
-              int* stages, int* num_clusters, int64_t* num_tiles);
+              int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split);
 
 /*
  * The persistent scheduler's task -> tile map (the same function the kernel
@@ -127,7 +169,8 @@ int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
  * reason here, end all of its loops, release Tensor Memory and return, so the
  * CUDA context stays usable.  The word is bits 0-7 = reason (1 = timeout),
  * bits 8-15 = role that gave up (1 producer, 2 MMA issuer, 3 epilogue,
- * 4 end-of-kernel drain, 5 self-test).  Synchronises the device, then writes the word
+ * 4 end-of-kernel drain, 5 self-test); reason 2 = a split-tail counter could
+ * not be updated.  Synchronises the device, then writes the word
  * to *status (0 = no error since the last clear) and clears it if `clear`.
  * Returns GEMM_OK or GEMM_ERR_CUDA.
  */

@@ -20,10 +20,10 @@ from gpu_util import check_close, decode, from_device, sample_tiles, to_device
 pytestmark = pytest.mark.gpu
 
 VARIANTS = [
-    {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0},
-    {"cta_group": 1, "block_n": 256, "raster_group": 0, "max_clusters": 0},
-    {"cta_group": 2, "block_n": 128, "raster_group": 0, "max_clusters": 0},
-    {"cta_group": 1, "block_n": 128, "raster_group": 0, "max_clusters": 0},
+    {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 1, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 2, "block_n": 128, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 1, "block_n": 128, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
 ]
 VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128"]
 
@@ -163,7 +163,7 @@ def test_shapes(variant, shape, layout, dtype):
 def test_few_clusters_many_tiles(max_clusters):
     # Each cluster walks many tiles: the ring position and both TMEM
     # accumulators are reused across tiles many times.
-    opts = {"cta_group": 2, "block_n": 256, "raster_group": 2, "max_clusters": max_clusters}
+    opts = {"cta_group": 2, "block_n": 256, "raster_group": 2, "max_clusters": max_clusters, "tail_split": 0}
     parity(1024, 1280, 320, "abt", "f16", seed=max_clusters, options=opts)
 
 
@@ -243,3 +243,73 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert binding.gemm_device_status(clear=True) == 0x501
     assert binding.gemm_device_status(clear=True) == 0
     parity(256, 256, 256, "abt", "f16", seed=5)
+
+
+# ---- split tail (last partial round split along K, FP32 partials in a workspace) --
+
+SPLIT_CASES = [
+    # (M, N, K, cta_group, max_clusters, tail_split): tail = tiles mod clusters > 0
+    (512, 512, 1024, 2, 3, 2),      # 4 tiles on 3 clusters: 1 tail tile in 2 ranges
+    (512, 512, 1024, 2, 3, 3),
+    (512, 512, 1000, 2, 3, 16),     # split capped at 16 k-blocks; K tail of 40
+    (768, 768, 512, 2, 4, 8),       # 9 tiles on 4 clusters: 8 ranges, 2 per cluster
+    (300, 700, 640, 2, 2, 5),       # ragged tiles
+    (640, 520, 200, 1, 5, 0),       # cta_group 1, automatic split (k-blocks = 4)
+    (1024, 1024, 2048, 2, 7, 0),    # 16 tiles on 7 clusters: tail 2 -> split 3
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "_".join(map(str, c)))
+@pytest.mark.parametrize("layout,dtype", [("abt", "f16"), ("ab", "bf16")])
+def test_split_tail(case, layout, dtype):
+    M, N, K, cg, clusters, split = case
+    opts = {"cta_group": cg, "block_n": 256, "max_clusters": clusters, "tail_split": split}
+    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1,
+                             opts)
+    assert plan["num_tiles"] % plan["num_clusters"] != 0
+    assert plan["tail_split"] >= 2
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K,
+           options=opts)
+
+
+def test_split_tail_deterministic_and_workspace_reused():
+    M, N, K = 1024, 1024, 2048
+    opts = {"cta_group": 2, "block_n": 256, "max_clusters": 7, "tail_split": 3}
+    A, B = inputs.operands(M, N, K, "abt", "f16", "uniform", 77)
+    dA, dB = to_device(A, "f16"), to_device(B, "f16")
+    need = binding.gemm_workspace_size(M, N, K, 0, 0, opts)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = [binding.gemm_abt(dA, dB, options=opts, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    ref = oracle.gemm(A, B, layout="abt", dtype="f16")
+    check_close(from_device(outs[0]), ref, "f16", "split tail")
+    # without a workspace: the plain schedule, also within tolerance
+    plain = binding.gemm_abt(dA, dB, options=opts, workspace=None)
+    torch.cuda.synchronize()
+    check_close(from_device(plain), ref, "f16", "no workspace")
+
+
+def test_workspace_errors():
+    M, N, K = 1024, 1024, 2048
+    opts = {"cta_group": 2, "block_n": 256, "max_clusters": 7, "tail_split": 3}
+    need = binding.gemm_workspace_size(M, N, K, 0, 0, opts)
+    A = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    B = torch.zeros((N, K), dtype=torch.float16, device="cuda")
+    small = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A, B, options=opts, workspace=small)
+    assert e.value.status == -10
+    big = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A, B, options=opts, workspace=big[8:])  # not 256-byte aligned
+    assert e.value.status == -10
+
+
+def test_headline_plan_splits_tail():
+    # 4096^3 on the full device: 256 tiles; any tail round is split.
+    plan = binding.gemm_plan(4096, 4096, 4096, 0, 0)
+    if plan["num_tiles"] % plan["num_clusters"]:
+        assert plan["tail_split"] >= 2
