@@ -253,8 +253,8 @@ SPLIT_CASES = [
     (512, 512, 1024, 2, 3, 3),
     (512, 512, 1000, 2, 3, 16),     # split capped at 16 k-blocks; K tail of 40
     (768, 768, 512, 2, 4, 8),       # 9 tiles on 4 clusters: 8 ranges, 2 per cluster
-    (300, 700, 640, 2, 2, 5),       # ragged tiles
-    (640, 520, 200, 1, 5, 0),       # cta_group 1, automatic split (k-blocks = 4)
+    (300, 704, 640, 2, 4, 5),       # ragged tiles: 6 tiles on 4 clusters
+    (640, 520, 200, 1, 7, 0),       # cta_group 1: 15 tiles on 7 clusters, auto split capped at 4 k-blocks
     (1024, 1024, 2048, 2, 7, 0),    # 16 tiles on 7 clusters: tail 2 -> split 3
 ]
 
