@@ -31,8 +31,8 @@ STATUS_NAMES = {
 
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_workspace_size",
-           "gemm_status_string", "gemm_plan", "gemm_tile_origin", "gemm_device_status",
-           "gemm_selftest_wait_timeout")
+           "gemm_run_no_alloc", "gemm_status_string", "gemm_plan", "gemm_tile_origin",
+           "gemm_device_status", "gemm_selftest_wait_timeout")
 
 
 class GemmError(RuntimeError):
@@ -81,6 +81,9 @@ def load(path: str | None = None):
     lib.gemm_workspace_size.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions),
                                         ctypes.POINTER(ctypes.c_size_t)]
     lib.gemm_workspace_size.restype = c_int
+    lib.gemm_run_no_alloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                      ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_run_no_alloc.restype = c_int
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(c_int)
@@ -285,3 +288,24 @@ def gemm_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     st = load().gemm_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, torch.device("cuda")))
     if st != 0:
         raise GemmError(st, "gemm_selftest_wait_timeout")
+
+
+def gemm_run_no_alloc(A, B, D, *, layout: int = LAYOUT_ABT, options=None, stream=None):
+    """The GEMM through gemm_run_no_alloc: no allocation anywhere on the path.
+
+    For callers that cannot allocate device memory at call time.  D must be
+    given (the caller owns every buffer); the split tail uses the library's
+    fixed scratch array.  Calls on different streams must not overlap.
+    """
+    if A.device.type != "cuda" or B.device.type != "cuda" or D.device.type != "cuda":
+        raise GemmError(-1, "operands must be CUDA tensors")
+    M, K = A.shape
+    N = B.shape[0] if layout == LAYOUT_ABT else B.shape[1]
+    if tuple(D.shape) != (M, N) or D.dtype != A.dtype or B.dtype != A.dtype:
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    st = load().gemm_run_no_alloc(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _ld(A),
+                                  _ld(B), _ld(D), _dtype_code(A), int(layout), _options(options),
+                                  _stream_handle(stream, A.device))
+    if st != 0:
+        raise GemmError(st, "gemm_run_no_alloc")
+    return D

@@ -145,6 +145,30 @@ int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout
                         const gemm_options_t* opts, size_t* bytes);
 
 /*
+ * gemm_run_workspace for callers that cannot allocate device memory (code
+ * captured into a CUDA graph or running under a fixed memory budget, plugins
+ * whose host framework owns every allocation, loops where an allocation may
+ * block or fail).  The pages describe no counterpart: it is an addition of
+ * this library.
+ *
+ * The split tail's workspace is a fixed 20 MiB scratch array compiled into
+ * the library; every GPU that loads the library holds one until the process
+ * exits.  The caller passes A, B and D as for gemm_run; nothing is allocated
+ * and no allocating routine is called.  A plan that needs more than 20 MiB
+ * (possible only with a large explicit tail_split) returns
+ * GEMM_ERR_WORKSPACE; automatic plans on a 152-SM GB300 always fit.
+ *
+ * The first call on each device looks up the scratch's device address and
+ * zeroes it (a synchronous cudaMemset), so make that first call before any
+ * stream capture.  All calls on a device share the one scratch array, which
+ * keeps the last call's contents: calls that overlap on the GPU (different
+ * streams, concurrent graphs) race on it and must be serialised by the caller.
+ */
+int gemm_run_no_alloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+                      const gemm_options_t* opts, cudaStream_t stream);
+
+/*
  * Plan of a call, without launching: the tile shape, grid, stage count and
  * tail split gemm_run_workspace (with a large enough workspace) would use for
  * these sizes on the current device.  Any out pointer may be NULL.  Returns
