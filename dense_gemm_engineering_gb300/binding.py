@@ -106,14 +106,28 @@ def gemm_status_string(status: int) -> str:
     return load().gemm_status_string(int(status)).decode()
 
 
+_options_cache = {}
+
+
+def _options_key(options):
+    if options is None:
+        return None
+    if isinstance(options, GemmOptions):
+        return tuple(getattr(options, f) for f, _ in GemmOptions._fields_)
+    return tuple(sorted((k, int(v)) for k, v in dict(options).items()))
+
+
 def _options(options) -> ctypes.POINTER(GemmOptions) | None:
     if options is None:
         return None
     if isinstance(options, GemmOptions):
-        o = options
-    else:
-        o = GemmOptions(**{k: int(v) for k, v in dict(options).items()})
-    return ctypes.pointer(o)
+        return ctypes.pointer(options)
+    key = _options_key(options)
+    p = _options_cache.get(key)
+    if p is None:
+        p = ctypes.pointer(GemmOptions(**dict(key)))
+        _options_cache[key] = p
+    return p
 
 
 def _dtype_code(t) -> int:
@@ -148,6 +162,8 @@ def _stream_handle(stream, device) -> int:
 # Workspaces for the split tail, one per (device, stream): calls on one stream
 # run in order, so they may share one; calls on different streams must not.
 _workspaces = {}
+# gemm_workspace_size results per (shape, dtype, layout, options, device).
+_ws_need_cache = {}
 
 
 def _workspace(device, stream_handle: int, nbytes: int):
@@ -194,12 +210,17 @@ def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=Non
     dt = _dtype_code(A)
     ws_ptr, ws_bytes = None, 0
     if isinstance(workspace, str) and workspace == "auto":
-        need = ctypes.c_size_t()
-        st = lib.gemm_workspace_size(M, N, K, dt, int(layout), opts, ctypes.byref(need))
-        if st != 0:
-            raise GemmError(st, "gemm_workspace_size")
-        if need.value:
-            ws = _workspace(A.device, sh, need.value)
+        dev_index = A.device.index if A.device.index is not None else torch.cuda.current_device()
+        key = (M, N, K, dt, int(layout), _options_key(options), dev_index)
+        need = _ws_need_cache.get(key)
+        if need is None:
+            n = ctypes.c_size_t()
+            st = lib.gemm_workspace_size(M, N, K, dt, int(layout), opts, ctypes.byref(n))
+            if st != 0:
+                raise GemmError(st, "gemm_workspace_size")
+            need = _ws_need_cache[key] = n.value
+        if need:
+            ws = _workspace(A.device, sh, need)
             ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
     elif workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()

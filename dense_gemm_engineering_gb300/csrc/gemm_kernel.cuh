@@ -86,7 +86,14 @@ struct KernelConfig {
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * 2u * EPI_BUF_BYTES;
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u;
+    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue warp
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps;
+    // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
+    // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
+    // (32 rows x 64 FP32 columns).
+    static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+    static constexpr uint32_t PIECE_BYTES = 32u * 64u * 4u;
+    static constexpr uint32_t PIECES_PER_WARP = (RING_BYTES / kEpilogueWarps) / PIECE_BYTES;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8u;
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4u;
     static constexpr uint32_t SMEM_USED = OFF_ABORT + 4u;
@@ -246,6 +253,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto acc_empty_bar = [&](uint32_t b) {
         return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
     };
+    auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
 
@@ -259,6 +267,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
             ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
         }
+        for (uint32_t e = 0; e < uint32_t(kEpilogueWarps); ++e) ptx::mbar_init(epi_bar(e), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_a);
@@ -388,7 +397,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // ---- epilogue warps 2..5 ----------------------------------------------
         const uint32_t quarter = warp & 3u;  // this warp may read TMEM lanes 32q..32q+31
         const uint32_t buf0 = base + C::OFF_EPI + (warp - 2u) * 2u * C::EPI_BUF_BYTES;
-        uint32_t ab = 0, aph = 0, chunk = 0;
+        const uint32_t my_epi_bar = epi_bar(warp - 2u);
+        const uint32_t my_ring = base + C::OFF_A + (warp - 2u) * C::PIECES_PER_WARP * C::PIECE_BYTES;
+        uint32_t ab = 0, aph = 0, chunk = 0, eph = 0;
 
         // Hand accumulator `b` back to the MMA issuer (all TMEM reads done).
         auto release_acc = [&](uint32_t b) {
@@ -487,36 +498,113 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 before = __shfl_sync(0xffffffffu, before, 0);
                 if (before != uint32_t(args.split - 1)) {
                     release_acc(ab);  // another range finishes this block of D
+                } else if (u + num_clusters >= units &&
+                           uint32_t(args.split - 1) <= C::PIECES_PER_WARP) {
+                    // Pass 2 (the last range to finish, in this cluster's last
+                    // unit, so the ring is idle): bulk-copy the other ranges'
+                    // pieces of each 64-column chunk into this warp's share of
+                    // the ring, then D = sum of all ranges in range order (this
+                    // range's own piece read from TMEM).
+                    __threadfence();
+                    const uint32_t others = uint32_t(args.split - 1);
+                    const int per_batch_max = int(C::PIECES_PER_WARP / others);
+                    const int per_batch = per_batch_max < C::BN / 64 ? per_batch_max : C::BN / 64;
+                    const float4* const first = slots + quad * args.split * slot_stride;
+                    for (int j0 = 0; j0 < C::BN / 64; j0 += per_batch) {
+                        const int j1 = (j0 + per_batch < C::BN / 64) ? j0 + per_batch : C::BN / 64;
+                        uint32_t ok2 = 1u;
+                        if (lane == 0) {
+                            ptx::fence_proxy_async_global();
+                            ptx::mbar_arrive_expect_tx(my_epi_bar,
+                                                       uint32_t(j1 - j0) * others * C::PIECE_BYTES);
+                            uint32_t piece = 0;
+                            for (int j = j0; j < j1; ++j)
+                                for (int r = 0; r < args.split; ++r) {
+                                    if (r == w.range) continue;
+                                    ptx::bulk_load_g2s(my_ring + piece * C::PIECE_BYTES,
+                                                       first + r * slot_stride + j * 16 * 32,
+                                                       C::PIECE_BYTES, my_epi_bar);
+                                    ++piece;
+                                }
+                            ok2 = wait_bounded(my_epi_bar, eph, abort_flag, kRoleEpilogue);
+                        }
+                        ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+                        if (ok2) {
+                            while (!ptx::mbar_try_wait(my_epi_bar, eph)) {
+                            }
+                        }
+                        eph ^= 1u;
+                        uint32_t piece0 = 0;  // pieces of chunk j start at piece0
+                        for (int j = j0; j < j1; ++j, piece0 += others) {
+                            float acc[64];
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t own[32];  // this range's piece, from TMEM
+                                ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u * h, own);
+                                ptx::tmem_wait_ld();
+                                uint32_t piece = piece0;
+                                for (int r = 0; r < args.split; ++r) {
+                                    if (r == w.range) {
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) {
+                                            const float x = __uint_as_float(own[i]);
+                                            acc[32 * h + i] = (r == 0) ? x : acc[32 * h + i] + x;
+                                        }
+                                        continue;
+                                    }
+                                    const uint32_t pb = my_ring + piece * C::PIECE_BYTES;
+                                    ++piece;
+#pragma unroll
+                                    for (int g = 8 * h; g < 8 * h + 8; ++g) {
+                                        float x, y, z, t;
+                                        ptx::ld_shared_v4(pb + (uint32_t(g) * 32u + lane) * 16u, x, y, z, t);
+                                        acc[4 * g] = (r == 0) ? x : acc[4 * g] + x;
+                                        acc[4 * g + 1] = (r == 0) ? y : acc[4 * g + 1] + y;
+                                        acc[4 * g + 2] = (r == 0) ? z : acc[4 * g + 2] + z;
+                                        acc[4 * g + 3] = (r == 0) ? t : acc[4 * g + 3] + t;
+                                    }
+                                }
+                            }
+                            if (j == C::BN / 64 - 1) release_acc(ab);
+                            store_chunk(acc, col0 + 64 * j, row0);
+                        }
+                    }
                 } else {
-                    // Pass 2 (the last range to finish): D = sum of all ranges'
-                    // partials in range order, this range's taken from TMEM.
+                    // Pass 2 without the ring (a unit that is not this cluster's
+                    // last, or a very deep split): read the other ranges'
+                    // partials straight from L2.
                     __threadfence();
                     const float4* const first = slots + quad * args.split * slot_stride;
 #pragma unroll 1
                     for (int j = 0; j < C::BN / 64; ++j) {
-                        float own[64], acc[64];
-                        load_acc(taddr + 64u * j, own);
-                        if (j == C::BN / 64 - 1) release_acc(ab);
-#pragma unroll 1
-                        for (int r = 0; r < args.split; ++r) {
-                            float part[64];
-                            if (r == w.range) {
+                        float acc[64];
 #pragma unroll
-                                for (int i = 0; i < 64; ++i) part[i] = own[i];
-                            } else {
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t own[32];
+                            ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u * h, own);
+                            ptx::tmem_wait_ld();
+#pragma unroll 1
+                            for (int r = 0; r < args.split; ++r) {
+                                if (r == w.range) {
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) {
+                                        const float x = __uint_as_float(own[i]);
+                                        acc[32 * h + i] = (r == 0) ? x : acc[32 * h + i] + x;
+                                    }
+                                    continue;
+                                }
                                 const float4* src = first + r * slot_stride;
 #pragma unroll
-                                for (int g = 0; g < 16; ++g) {
+                                for (int g = 8 * h; g < 8 * h + 8; ++g) {
                                     const float4 q = __ldcg(src + (j * 16 + g) * 32 + lane);
-                                    part[4 * g] = q.x;
-                                    part[4 * g + 1] = q.y;
-                                    part[4 * g + 2] = q.z;
-                                    part[4 * g + 3] = q.w;
+                                    acc[4 * g] = (r == 0) ? q.x : acc[4 * g] + q.x;
+                                    acc[4 * g + 1] = (r == 0) ? q.y : acc[4 * g + 1] + q.y;
+                                    acc[4 * g + 2] = (r == 0) ? q.z : acc[4 * g + 2] + q.z;
+                                    acc[4 * g + 3] = (r == 0) ? q.w : acc[4 * g + 3] + q.w;
                                 }
                             }
-#pragma unroll
-                            for (int i = 0; i < 64; ++i) acc[i] = (r == 0) ? part[i] : acc[i] + part[i];
                         }
+                        if (j == C::BN / 64 - 1) release_acc(ab);
                         store_chunk(acc, col0 + 64 * j, row0);
                     }
                 }

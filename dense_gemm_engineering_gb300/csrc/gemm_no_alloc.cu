@@ -11,10 +11,10 @@
 //
 // The scratch is a file-scope device array of kNoAllocScratchBytes (20 MiB).
 // Every GPU that loads the library holds its own copy until the process exits.
-// 20 MiB covers the automatic split of any shape on a 152-SM GB300 (76
-// two-CTA clusters: at most one 256 KiB FP32 partial per cluster, plus
-// counters); plans that need more (a large forced tail_split) are rejected
-// with GEMM_ERR_WORKSPACE.
+// 20 MiB covers any split that gives each cluster at most one K-range on a
+// 152-SM GB300 (76 two-CTA clusters: at most one 256 KiB FP32 partial per
+// cluster, plus counters); plans that need more (a deeper tail_split) are
+// rejected with GEMM_ERR_WORKSPACE.
 #include <cuda_runtime.h>
 
 #include <cstdint>

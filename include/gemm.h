@@ -93,10 +93,13 @@ const char* gemm_status_string(int status);
  *                 group, N-major inside a group, so consecutive tiles share B).
  *   max_clusters  0 = as many co-resident clusters as fit, else an upper bound
  *                 on the persistent grid (in clusters).
- *   tail_split    only with a workspace (gemm_run_workspace): 0 = automatic,
- *                 1 = never, s in [2, 16] = split every tile of the last,
- *                 partial round of the persistent schedule into s K-ranges
- *                 (capped by the number of 64-wide k-blocks).
+ *   tail_split    0 or 1 = balanced grid: the persistent schedule's rounds
+ *                 are spread over the fewest clusters that keep the same round
+ *                 count, so no cluster idles in a partial last round.
+ *                 s in [2, 16], only with a workspace (gemm_run_workspace):
+ *                 keep every cluster and split each tile of the last, partial
+ *                 round into s K-ranges (capped by the number of 64-wide
+ *                 k-blocks).
  */
 typedef struct {
     int cta_group;
@@ -113,10 +116,10 @@ int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
 
 /*
  * The same GEMM with a caller-owned device workspace, which lets the kernel
- * shorten the last, partial round of its persistent schedule: with C
- * co-resident clusters and T tiles, the T mod C tiles of that round are each
- * split into s K-ranges (s = floor(C / (T mod C)) when automatic) so the
- * clusters that would idle share the work.  Each range writes an FP32
+ * split the last, partial round of its persistent schedule (requested with
+ * gemm_options_t.tail_split = s >= 2): with C co-resident clusters and T
+ * tiles, the T mod C tiles of that round are each split into s K-ranges so
+ * the clusters that would idle share the work.  Each range writes an FP32
  * partial to the workspace; the range that finishes last (found with an
  * atomic counter, nobody waits) adds the partials in range order and writes D.
  * Results are deterministic for a given plan.
@@ -155,8 +158,9 @@ int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout
  * the library; every GPU that loads the library holds one until the process
  * exits.  The caller passes A, B and D as for gemm_run; nothing is allocated
  * and no allocating routine is called.  A plan that needs more than 20 MiB
- * (possible only with a large explicit tail_split) returns
- * GEMM_ERR_WORKSPACE; automatic plans on a 152-SM GB300 always fit.
+ * (a tail_split s with (T mod C) x s larger than the cluster count C)
+ * returns GEMM_ERR_WORKSPACE; s <= C / (T mod C) always fits on a 152-SM
+ * GB300.
  *
  * The first call on each device looks up the scratch's device address and
  * zeroes it (a synchronous cudaMemset), so make that first call before any

@@ -254,8 +254,8 @@ SPLIT_CASES = [
     (512, 512, 1000, 2, 3, 16),     # split capped at 16 k-blocks; K tail of 40
     (768, 768, 512, 2, 4, 8),       # 9 tiles on 4 clusters: 8 ranges, 2 per cluster
     (300, 704, 640, 2, 4, 5),       # ragged tiles: 6 tiles on 4 clusters
-    (640, 520, 200, 1, 7, 0),       # cta_group 1: 15 tiles on 7 clusters, auto split capped at 4 k-blocks
-    (1024, 1024, 2048, 2, 7, 0),    # 16 tiles on 7 clusters: tail 2 -> split 3
+    (640, 520, 200, 1, 7, 6),       # cta_group 1: 15 tiles on 7 clusters, split capped at 4 k-blocks
+    (1024, 1024, 2048, 2, 7, 3),    # 16 tiles on 7 clusters: tail 2 -> split 3
 ]
 
 
@@ -308,8 +308,14 @@ def test_workspace_errors():
     assert e.value.status == -10
 
 
-def test_headline_plan_splits_tail():
-    # 4096^3 on the full device: 256 tiles; any tail round is split.
-    plan = binding.gemm_plan(4096, 4096, 4096, 0, 0)
-    if plan["num_tiles"] % plan["num_clusters"]:
-        assert plan["tail_split"] >= 2
+def test_default_plan_is_a_balanced_grid():
+    # Automatic plans spread the rounds over the fewest clusters that keep the
+    # round count: 4096^3 has 256 tiles; with 76 co-resident clusters that is
+    # 4 rounds, run on ceil(256 / 4) = 64 clusters.
+    for M, N, K in [(4096, 4096, 4096), (3000, 5000, 4000), (8192, 17408, 5120)]:
+        full = binding.gemm_plan(M, N, K, 0, 0, {"max_clusters": 0, "tail_split": 16})
+        plan = binding.gemm_plan(M, N, K, 0, 0)
+        C = full["num_clusters"]
+        rounds = -(-plan["num_tiles"] // C)
+        assert plan["tail_split"] == 1
+        assert plan["num_clusters"] == -(-plan["num_tiles"] // rounds)

@@ -43,8 +43,8 @@ def _raw_no_alloc(A, B, D, layout, opts):
 CASES = [
     # M, N, K, layout, dtype, options (split tail active: tiles mod clusters > 0)
     (1024, 1024, 2048, 0, "f16", {"cta_group": 2, "max_clusters": 7, "tail_split": 3}),
-    (768, 1280, 1000, 1, "bf16", {"cta_group": 2, "max_clusters": 7, "tail_split": 0}),
-    (4096, 4096, 4096, 0, "f16", {}),
+    (768, 1280, 1000, 1, "bf16", {"cta_group": 2, "max_clusters": 7, "tail_split": 4}),
+    (4096, 4096, 4096, 0, "f16", {"tail_split": 2}),
 ]
 
 
