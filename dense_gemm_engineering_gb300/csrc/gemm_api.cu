@@ -135,11 +135,13 @@ int query_max_clusters(int dev, int sm_count) {
 // Stage counts: as many 128-byte-swizzled K slices as fit next to the
 // 32 KiB epilogue staging in 227 KiB.
 template <int CG, int BN>
-struct Stages;
-template <> struct Stages<2, 256> { static constexpr int value = 6; };  // 32 KiB / stage
-template <> struct Stages<1, 256> { static constexpr int value = 4; };  // 48 KiB / stage
-template <> struct Stages<2, 128> { static constexpr int value = 8; };  // 24 KiB / stage
-template <> struct Stages<1, 128> { static constexpr int value = 6; };  // 32 KiB / stage
+struct Stages {
+    // As many stages (16 KiB of A plus this CTA's share of B) as fit in 227 KiB
+    // next to the 32 KiB epilogue staging and the barriers: 6 for 2-CTA
+    // 256-wide tiles (32 KiB / stage), 4 for 1-CTA 256-wide (48 KiB).
+    static constexpr int value =
+        (227 * 1024 - 32768 - 1024 - 512) / (128 * 64 * 2 + (BN / CG) * 64 * 2);
+};
 
 template <int CG, int BN, bool B_MN, bool BF16>
 using Cfg = KernelConfig<CG, BN, Stages<CG, BN>::value, B_MN, BF16>;
@@ -192,7 +194,7 @@ void plan_split(Plan* p, int requested, bool have_workspace) {
     p->whole_units = p->tiles;
     p->split = 1;
     const int64_t tail = p->clusters > 0 ? p->tiles % p->clusters : 0;
-    if (have_workspace && tail > 0 && requested >= 2) {
+    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0) {
         int64_t s = requested;
         if (s > kMaxSplit) s = kMaxSplit;
         if (s > p->k_blocks) s = p->k_blocks;
@@ -227,6 +229,8 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     if (!encode_2d(&md, D, dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
         return GEMM_ERR_CUDA;
     GemmArgs args;
+    args.d = static_cast<uint16_t*>(D);
+    args.ldd = ldd;
     args.M = int32_t(M);
     args.N = int32_t(N);
     args.K = int32_t(K);
@@ -258,10 +262,17 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, Ts&&... ts) {
 #define GB300_CASES(CG_, BN_) \
     GB300_CASE(CG_, BN_, false, false) GB300_CASE(CG_, BN_, false, true) \
     GB300_CASE(CG_, BN_, true, false) GB300_CASE(CG_, BN_, true, true)
+#define GB300_KMAJOR_CASES(CG_, BN_) \
+    GB300_CASE(CG_, BN_, false, false) GB300_CASE(CG_, BN_, false, true)
     GB300_CASES(2, 256)
     GB300_CASES(1, 256)
     GB300_CASES(2, 128)
     GB300_CASES(1, 128)
+    GB300_KMAJOR_CASES(2, 224)
+    GB300_KMAJOR_CASES(2, 192)
+    GB300_KMAJOR_CASES(1, 224)
+    GB300_KMAJOR_CASES(1, 192)
+#undef GB300_KMAJOR_CASES
 #undef GB300_CASES
 #undef GB300_CASE
     return GEMM_ERR_OPTION;
@@ -302,10 +313,52 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int dtype, int b_layout) {
 int check_options(const gemm_options_t* o) {
     if (!o) return GEMM_OK;
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_OPTION;
-    if (o->block_n != 0 && o->block_n != 128 && o->block_n != 256) return GEMM_ERR_OPTION;
+    if (o->block_n != 0 && o->block_n != 128 && o->block_n != 192 && o->block_n != 224 &&
+        o->block_n != 256)
+        return GEMM_ERR_OPTION;
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
     if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
     return GEMM_OK;
+}
+
+int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
+    int n = 0;
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, dev, sm_count, &n) != GEMM_OK)
+        return 0;
+    return n;
+}
+
+// Tile width N for the automatic plan.  Every round of the persistent schedule
+// costs one tile time, and a tile's time grows with its width divided by the
+// MMA efficiency of that width (narrower tiles move more operand bytes per
+// FLOP).  Pick the width with the least rounds x width / efficiency; ties go
+// to the wider tile.  The efficiencies are deliberately low: the kernel is
+// power-limited on GB300, so a narrower tile that only trims idle time in the
+// last round does not pay (4096^3: 224-wide tiles fill 4 rounds exactly yet run
+// no faster than 256-wide tiles on a balanced grid); a narrower width is taken
+// only when it removes whole rounds.
+int choose_block_n(int64_t M, int64_t N, int bm, int b_layout, int cg, int dtype, int dev,
+                   int sm_count) {
+    struct Cand {
+        int bn;
+        double eff;
+    };
+    static const Cand kCands[] = {{256, 1.0}, {224, 0.84}, {192, 0.72}};
+    int best = 256;
+    double best_cost = 0;
+    for (const Cand& c : kCands) {
+        if (b_layout == 1 && (c.bn % 128) != 0) continue;
+        const int C = max_clusters_for(cg, c.bn, b_layout, dtype, dev, sm_count);
+        if (C <= 0) continue;
+        const int64_t tiles = ((M + bm - 1) / bm) * ((N + c.bn - 1) / c.bn);
+        const int64_t rounds = (tiles + C - 1) / C;
+        const double cost = double(rounds) * c.bn / c.eff;
+        if (best_cost == 0 || cost < best_cost * (1 - 1e-9)) {
+            best = c.bn;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 // Choose the tile shape and grid.  Needs the current device (for its SM count
@@ -318,8 +371,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     int dev = 0;
     cudaGetDevice(&dev);
     p->cg = (o && o->cta_group) ? o->cta_group : (M <= 128 ? 1 : 2);
-    p->bn = (o && o->block_n) ? o->block_n : 256;
     p->bm = 128 * p->cg;
+    if (o && o->block_n) {
+        p->bn = o->block_n;
+        // 192 / 224 are K-major only: an MN-major B tile is loaded in 64-column atoms.
+        if (b_layout == 1 && (p->bn % 128) != 0) return GEMM_ERR_OPTION;
+    } else {
+        p->bn = choose_block_n(M, N, p->bm, b_layout, p->cg, dtype, dev, di.sm_count);
+    }
     p->group = (o && o->raster_group) ? o->raster_group : 16;
     const int64_t m_tiles = (M + p->bm - 1) / p->bm;
     const int64_t n_tiles = (N + p->bn - 1) / p->bn;
@@ -331,10 +390,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
     p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
-    if (p->cg == 2 && p->bn == 256) p->stages = Stages<2, 256>::value;
-    else if (p->cg == 1 && p->bn == 256) p->stages = Stages<1, 256>::value;
-    else if (p->cg == 2) p->stages = Stages<2, 128>::value;
-    else p->stages = Stages<1, 128>::value;
+    p->stages = (227 * 1024 - 32768 - 1024 - 512) / (128 * 64 * 2 + (p->bn / p->cg) * 64 * 2);
     p->k_blocks = (K + kBlockK - 1) / kBlockK;
     plan_split(p, o ? o->tail_split : 0, have_workspace);
     return GEMM_OK;

@@ -78,7 +78,14 @@ struct KernelConfig {
     static constexpr uint32_t A_BYTES = 128u * kBlockK * 2u;            // 16 KiB
     static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * kBlockK * 2u;
     static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES);
-    static constexpr uint32_t TMEM_COLS = 2u * BN;                     // 2 accumulators
+    // Two accumulators of BN FP32 columns at a power-of-two stride (the TMEM
+    // allocation is a power of two of at least 32 columns).
+    static constexpr uint32_t ACC_STRIDE = BN <= 128 ? 128u : 256u;
+    static constexpr uint32_t TMEM_COLS = 2u * ACC_STRIDE;
+    // Epilogue chunks: BN / 64 full 64-column chunks, plus one 32-column chunk
+    // when BN is an odd multiple of 32.
+    static constexpr int FULL_CHUNKS = BN / 64;
+    static constexpr bool HALF_CHUNK = (BN % 64) != 0;
     static constexpr uint32_t EPI_BUF_BYTES = 32u * 128u;              // 32 rows x 64 cols
     static constexpr uint32_t MN_ATOM_BYTES = 64u * 128u;              // MN-major: 64 K x 64 N
 
@@ -107,7 +114,8 @@ struct KernelConfig {
                                       (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
-    static_assert(BN == 128 || BN == 256, "tile N is 128 or 256");
+    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile N is a multiple of 32 in [128, 256]");
+    static_assert((BN / CG) % 16 == 0, "each CTA's share of B is whole 16-row SW128 groups");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
@@ -117,6 +125,8 @@ struct KernelConfig {
 struct GemmArgs {
     int32_t M, N, K;
     int32_t k_blocks;   // ceil(K / 64)
+    uint16_t* d;        // D, for the direct stores of a 32-column tail chunk
+    int64_t ldd;        // row stride of D in elements
     TileGrid grid;
     // Work units.  Units [0, whole_units) are whole tiles (unit u = tile u).
     // The remaining tiles ("tail" tiles, the last partial round of the
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + ab * uint32_t(C::BN);
+                const uint32_t d_tmem = tmem_base + ab * C::ACC_STRIDE;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, abort_flag, kRoleMma)) {
                         ok = false;
@@ -437,6 +447,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             ++chunk;
         };
+        // 32 FP32 values (bit patterns) of row `row` -> 16-bit -> D[row][col..col+31],
+        // masked at the edges of D.
+        auto store_half_chunk = [&](const uint32_t (&r)[32], int32_t col, int32_t row) {
+            if (row >= args.M || col >= args.N) return;
+            uint16_t* dst = args.d + int64_t(row) * args.ldd + col;
+            if (col + 32 <= args.N) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 q = make_uint4(
+                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1])),
+                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3])),
+                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5])),
+                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7])));
+                    reinterpret_cast<uint4*>(dst)[c] = q;
+                }
+            } else {
+                const int32_t n = args.N - col;
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const uint32_t p = ptx::pack2<C::BF16>(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                    if (c < n) dst[c] = uint16_t(p & 0xFFFFu);
+                    if (c + 1 < n) dst[c + 1] = uint16_t(p >> 16);
+                }
+            }
+        };
         auto load_acc = [&](uint32_t taddr, float (&v)[64]) {
             uint32_t lo[32], hi[32];
             ptx::tmem_ld_32x32b_x32(taddr, lo);
@@ -463,16 +498,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
             const int32_t row0 = mt * C::BM + int32_t(rank) * 128 + int32_t(quarter) * 32;
             const int32_t col0 = nt * C::BN;
-            const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * uint32_t(C::BN);
+            const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::ACC_STRIDE;
 
             if (w.range < 0) {
                 // Whole tile: TMEM -> D.
 #pragma unroll 1
-                for (int j = 0; j < C::BN / 64; ++j) {
+                for (int j = 0; j < C::FULL_CHUNKS; ++j) {
                     float v[64];
                     load_acc(taddr + 64u * j, v);
-                    if (j == C::BN / 64 - 1) release_acc(ab);
+                    if (j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release_acc(ab);
                     store_chunk(v, col0 + 64 * j, row0);
+                }
+                if constexpr (C::HALF_CHUNK) {
+                    // Last 32 columns: this lane's row, 64 bytes, stored directly.
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + 64u * C::FULL_CHUNKS, r);
+                    ptx::tmem_wait_ld();
+                    release_acc(ab);
+                    store_half_chunk(r, col0 + 64 * C::FULL_CHUNKS, row0 + int32_t(lane));
                 }
             } else {
                 // K-range of a tail tile.  Pass 1: write this range's FP32 partial

@@ -24,8 +24,16 @@ VARIANTS = [
     {"cta_group": 1, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 2, "block_n": 128, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 1, "block_n": 128, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 2, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 2, "block_n": 192, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 1, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
 ]
-VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128"]
+VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224"]
+
+
+def k_major_only(variant, layout):
+    """Widths 192 and 224 exist for K-major B (A.Bt) only."""
+    return layout == "ab" and variant["block_n"] % 128 != 0
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -76,8 +84,13 @@ def small_int_operands(M, N, K, layout, dtype, seed):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_exact_small_integers(variant, layout, dtype):
     # |D| <= 4 * 64 = 256: exact in FP32 and in both output types.
-    M, N, K = 256, 256, 64
+    M, N, K = 256, 448, 64
     A, B = small_int_operands(M, N, K, layout, dtype, seed=1)
+    if k_major_only(variant, layout):
+        with pytest.raises(binding.GemmError) as e:
+            run(A, B, layout, dtype, variant)
+        assert e.value.status == -8
+        return
     got = from_device(run(A, B, layout, dtype, variant))
     ref = oracle.gemm(A, B, layout=layout, dtype=dtype)
     assert np.array_equal(got, ref)
@@ -146,6 +159,7 @@ SHAPES = [
     (64, 96, 24),       # K < 64 (zero-filled tail of the only k-block)
     (520, 264, 4000),   # K tail of 32 after 62 full blocks
     (1000, 1000, 512),  # many tiles per cluster with few clusters capped below
+    (520, 456, 320),    # 224-wide tiles: the second tile's last 32-column chunk is partial
 ]
 
 
@@ -155,6 +169,8 @@ SHAPES = [
                                           ("ab", "f16")])
 def test_shapes(variant, shape, layout, dtype):
     M, N, K = shape
+    if k_major_only(variant, layout):
+        pytest.skip("K-major B only")
     parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=M + N + K,
            options=variant)
 
@@ -310,12 +326,20 @@ def test_workspace_errors():
 
 def test_default_plan_is_a_balanced_grid():
     # Automatic plans spread the rounds over the fewest clusters that keep the
-    # round count: 4096^3 has 256 tiles; with 76 co-resident clusters that is
-    # 4 rounds, run on ceil(256 / 4) = 64 clusters.
+    # round count: e.g. 4096^3 with 256-wide tiles has 256 tiles; with 76
+    # co-resident clusters that is 4 rounds, run on ceil(256 / 4) = 64 clusters.
     for M, N, K in [(4096, 4096, 4096), (3000, 5000, 4000), (8192, 17408, 5120)]:
-        full = binding.gemm_plan(M, N, K, 0, 0, {"max_clusters": 0, "tail_split": 16})
         plan = binding.gemm_plan(M, N, K, 0, 0)
+        full = binding.gemm_plan(M, N, K, 0, 0, {"block_n": plan["block_n"], "tail_split": 16})
         C = full["num_clusters"]
         rounds = -(-plan["num_tiles"] // C)
         assert plan["tail_split"] == 1
         assert plan["num_clusters"] == -(-plan["num_tiles"] // rounds)
+
+
+def test_automatic_width_prefers_256_unless_rounds_drop():
+    # 4096 x 4096 on the full device: 224-wide tiles (304 tiles) take as many
+    # rounds as 256-wide tiles (256 tiles) on 76 clusters, so the automatic
+    # plan keeps 256.  The MN-major A.B layout always uses a multiple of 128.
+    assert binding.gemm_plan(4096, 4096, 4096, 0, 0)["block_n"] == 256
+    assert binding.gemm_plan(8192, 17408, 5120, 1, 1)["block_n"] in (128, 256)
