@@ -423,20 +423,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         };
         // 64 FP32 values of this lane's row -> 16-bit -> swizzled staging -> TMA
-        // store of the warp's 32 x 64 box at (col, row0).
-        auto store_chunk = [&](const float (&v)[64], int32_t col, int32_t row0) {
-            const uint32_t buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
-            if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
+        // store of the warp's 32 x 64 box at (col, row0).  Staging alternates
+        // between the warp's two buffers, or (in a cluster's last unit, when the
+        // ring is idle) takes a fresh 4 KiB slice of the ring per chunk, which
+        // never waits for an earlier store.
+        auto store_chunk = [&](const uint32_t (&bits)[64], int32_t col, int32_t row0,
+                               int32_t ring_slot = -1) {
+            uint32_t buf;
+            if (ring_slot >= 0) {
+                buf = my_ring + uint32_t(ring_slot) * C::EPI_BUF_BYTES;
+            } else {
+                buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
+                if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
+            }
             __syncwarp();
             // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
             // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
             const uint32_t row_addr = buf + lane * 128u;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint32_t p0 = ptx::pack2<C::BF16>(v[8 * c + 0], v[8 * c + 1]);
-                const uint32_t p1 = ptx::pack2<C::BF16>(v[8 * c + 2], v[8 * c + 3]);
-                const uint32_t p2 = ptx::pack2<C::BF16>(v[8 * c + 4], v[8 * c + 5]);
-                const uint32_t p3 = ptx::pack2<C::BF16>(v[8 * c + 6], v[8 * c + 7]);
+                auto f = [&](int i) { return __uint_as_float(bits[8 * c + i]); };
+                const uint32_t p0 = ptx::pack2<C::BF16>(f(0), f(1));
+                const uint32_t p1 = ptx::pack2<C::BF16>(f(2), f(3));
+                const uint32_t p2 = ptx::pack2<C::BF16>(f(4), f(5));
+                const uint32_t p3 = ptx::pack2<C::BF16>(f(6), f(7));
                 ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ (lane & 7u)) << 4), p0, p1, p2, p3);
             }
             ptx::fence_proxy_async_smem();
@@ -502,12 +512,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
             if (w.range < 0) {
                 // Whole tile: TMEM -> D.
+                const bool last_unit = (u + num_clusters >= units);
 #pragma unroll 1
                 for (int j = 0; j < C::FULL_CHUNKS; ++j) {
-                    float v[64];
-                    load_acc(taddr + 64u * j, v);
+                    uint32_t bits[64];
+                    ptx::tmem_ld_32x32b_x32(taddr + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&bits[0]));
+                    ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u,
+                                            *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
+                    ptx::tmem_wait_ld();
                     if (j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release_acc(ab);
-                    store_chunk(v, col0 + 64 * j, row0);
+                    store_chunk(bits, col0 + 64 * j, row0, last_unit ? j : -1);
                 }
                 if constexpr (C::HALF_CHUNK) {
                     // Last 32 columns: this lane's row, 64 bytes, stored directly.
@@ -609,7 +623,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 }
                             }
                             if (j == C::BN / 64 - 1) release_acc(ab);
-                            store_chunk(acc, col0 + 64 * j, row0);
+                            store_chunk(reinterpret_cast<const uint32_t(&)[64]>(acc), col0 + 64 * j, row0);
                         }
                     }
                 } else {
@@ -648,7 +662,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             }
                         }
                         if (j == C::BN / 64 - 1) release_acc(ab);
-                        store_chunk(acc, col0 + 64 * j, row0);
+                        store_chunk(reinterpret_cast<const uint32_t(&)[64]>(acc), col0 + 64 * j, row0);
                     }
                 }
             }
