@@ -344,6 +344,7 @@ int choose_block_n(int64_t M, int64_t N, int bm, int b_layout, int cg, int dtype
         double eff;
     };
     static const Cand kCands[] = {{256, 1.0}, {224, 0.84}, {192, 0.72}};
+    if (M <= 0 || N <= 0) return 256;
     int best = 256;
     double best_cost = 0;
     for (const Cand& c : kCands) {

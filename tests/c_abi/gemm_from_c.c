@@ -1,0 +1,100 @@
+/*
+ * gemm_from_c.c -- drives the GEMM library through its C ABI from plain C.
+ *
+ * Usage: gemm_from_c <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin
+ * Reads A (M x K) and B (N x K for abt, K x N for ab) as raw 16-bit patterns,
+ * runs gemm_abt / gemm_ab on cudaMalloc'd buffers on a created stream, writes
+ * D (M x N) to D.bin, and checks that a few invalid calls return the
+ * documented status codes.  Exit status 0 on success.
+ */
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime_api.h>
+
+#include "gemm.h"
+
+static void* read_file(const char* path, size_t bytes) {
+    FILE* f = fopen(path, "rb");
+    if (!f) return NULL;
+    void* p = malloc(bytes ? bytes : 1);
+    size_t got = fread(p, 1, bytes, f);
+    fclose(f);
+    if (got != bytes) {
+        free(p);
+        return NULL;
+    }
+    return p;
+}
+
+#define CHECK_CUDA(x)                                                       \
+    do {                                                                    \
+        cudaError_t e_ = (x);                                               \
+        if (e_ != cudaSuccess) {                                            \
+            fprintf(stderr, "%s failed: %s\n", #x, cudaGetErrorString(e_)); \
+            return 2;                                                       \
+        }                                                                   \
+    } while (0)
+
+int main(int argc, char** argv) {
+    if (argc != 9) {
+        fprintf(stderr, "usage: %s <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin\n", argv[0]);
+        return 2;
+    }
+    const int ab = strcmp(argv[1], "ab") == 0;
+    const int dtype = strcmp(argv[2], "bf16") == 0 ? GEMM_BF16 : GEMM_F16;
+    const int64_t M = atoll(argv[3]), N = atoll(argv[4]), K = atoll(argv[5]);
+    const size_t a_bytes = (size_t)(M * K) * 2, b_bytes = (size_t)(N * K) * 2,
+                 d_bytes = (size_t)(M * N) * 2;
+    void* hA = read_file(argv[6], a_bytes);
+    void* hB = read_file(argv[7], b_bytes);
+    if (!hA || !hB) {
+        fprintf(stderr, "cannot read inputs\n");
+        return 2;
+    }
+    void *dA, *dB, *dD;
+    cudaStream_t s;
+    CHECK_CUDA(cudaMalloc(&dA, a_bytes));
+    CHECK_CUDA(cudaMalloc(&dB, b_bytes));
+    CHECK_CUDA(cudaMalloc(&dD, d_bytes));
+    CHECK_CUDA(cudaStreamCreate(&s));
+    CHECK_CUDA(cudaMemcpy(dA, hA, a_bytes, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dB, hB, b_bytes, cudaMemcpyHostToDevice));
+
+    int st = ab ? gemm_ab(dA, dB, dD, M, N, K, K, N, N, dtype, s)
+                : gemm_abt(dA, dB, dD, M, N, K, K, K, N, dtype, s);
+    if (st != GEMM_OK) {
+        fprintf(stderr, "gemm: %s\n", gemm_status_string(st));
+        return 1;
+    }
+    CHECK_CUDA(cudaStreamSynchronize(s));
+    uint32_t word = 1;
+    if (gemm_device_status(&word, 1) != GEMM_OK || word != 0) {
+        fprintf(stderr, "device status %u\n", word);
+        return 1;
+    }
+    void* hD = malloc(d_bytes ? d_bytes : 1);
+    CHECK_CUDA(cudaMemcpy(hD, dD, d_bytes, cudaMemcpyDeviceToHost));
+    FILE* f = fopen(argv[8], "wb");
+    if (!f || fwrite(hD, 1, d_bytes, f) != d_bytes) return 2;
+    fclose(f);
+
+    /* documented errors */
+    if (gemm_abt(dA, dB, dD, M, N, K, K, K, N, 7, s) != GEMM_ERR_DTYPE) return 3;
+    if (gemm_abt(NULL, dB, dD, M, N, K, K, K, N, dtype, s) != GEMM_ERR_NULL) return 3;
+    if (gemm_abt((char*)dA + 2, dB, dD, M, N, K, K, K, N, dtype, s) != GEMM_ERR_ALIGN) return 3;
+    if (gemm_abt(dA, dB, dA, M, N, K, K, K, N, dtype, s) != GEMM_ERR_ALIAS) return 3;
+    if (gemm_status_string(GEMM_ERR_SHAPE)[0] == '\0') return 3;
+
+    cudaFree(dA);
+    cudaFree(dB);
+    cudaFree(dD);
+    cudaStreamDestroy(s);
+    free(hA);
+    free(hB);
+    free(hD);
+    printf("ok\n");
+    return 0;
+}

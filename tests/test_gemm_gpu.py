@@ -343,3 +343,34 @@ def test_automatic_width_prefers_256_unless_rounds_drop():
     # plan keeps 256.  The MN-major A.B layout always uses a multiple of 128.
     assert binding.gemm_plan(4096, 4096, 4096, 0, 0)["block_n"] == 256
     assert binding.gemm_plan(8192, 17408, 5120, 1, 1)["block_n"] in (128, 256)
+
+
+# ---- seeded random cases: shapes, strides, layouts, dtypes and plan options --
+
+def _fuzz_cases(n=48, seed=2026):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        layout = "abt" if rng.random() < 0.6 else "ab"
+        dtype = "f16" if rng.random() < 0.5 else "bf16"
+        M = int(rng.integers(1, 700))
+        N = int(rng.integers(1, 90)) * 8
+        K = int(rng.integers(1, 100)) * 8
+        cg = int(rng.choice([0, 1, 2]))
+        widths = [0, 128, 256] + ([192, 224] if layout == "abt" else [])
+        bn = int(rng.choice(widths))
+        opts = {"cta_group": cg, "block_n": bn, "raster_group": int(rng.choice([0, 1, 3])),
+                "max_clusters": int(rng.choice([0, 1, 2, 5])),
+                "tail_split": int(rng.choice([0, 0, 2, 3]))}
+        pad = [int(rng.choice([0, 8, 24])) for _ in range(2)]
+        cases.append((i, layout, dtype, M, N, K, opts, pad))
+    return cases
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"fuzz{c[0]}")
+def test_random_cases(case):
+    _, layout, dtype, M, N, K, opts, pad = case
+    lda = K + pad[0]
+    ldb = (K if layout == "abt" else N) + pad[1]
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=M * 7 + N,
+           options=opts, lda=lda, ldb=ldb)
