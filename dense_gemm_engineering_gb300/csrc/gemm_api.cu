@@ -134,20 +134,24 @@ int query_max_clusters(int dev, int sm_count) {
 
 // Stage counts: as many 128-byte-swizzled K slices as fit next to the
 // 32 KiB epilogue staging in 227 KiB.
-template <int CG, int BN>
+constexpr int stages_for(int cg, int bn, int cons) {
+    return (227 * 1024 - 32768 - 1024 - 512) / (128 * cons * 64 * 2 + (bn / cg) * 64 * 2);
+}
+template <int CG, int BN, int CONS = 1>
 struct Stages {
-    // As many stages (16 KiB of A plus this CTA's share of B) as fit in 227 KiB
-    // next to the 32 KiB epilogue staging and the barriers: 6 for 2-CTA
-    // 256-wide tiles (32 KiB / stage), 4 for 1-CTA 256-wide (48 KiB).
-    static constexpr int value =
-        (227 * 1024 - 32768 - 1024 - 512) / (128 * 64 * 2 + (BN / CG) * 64 * 2);
+    // As many stages (16 KiB of A per consumer plus this CTA's share of B) as
+    // fit in 227 KiB next to the 32 KiB epilogue staging and the barriers: 6
+    // for 2-CTA 256-wide tiles (32 KiB / stage), 4 for 1-CTA 256-wide or for
+    // two consumers (48 KiB).
+    static constexpr int value = stages_for(CG, BN, CONS);
 };
 
-template <int CG, int BN, bool B_MN, bool BF16>
-using Cfg = KernelConfig<CG, BN, Stages<CG, BN>::value, B_MN, BF16>;
+template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS>;
 
 struct Plan {
     int cg, bm, bn, stages;
+    int cons;  // MMA consumers per CTA
     int clusters;
     int64_t tiles;
     int group;
@@ -194,7 +198,7 @@ void plan_split(Plan* p, int requested, bool have_workspace) {
     p->whole_units = p->tiles;
     p->split = 1;
     const int64_t tail = p->clusters > 0 ? p->tiles % p->clusters : 0;
-    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0) {
+    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0 && p->cons == 1) {
         int64_t s = requested;
         if (s > kMaxSplit) s = kMaxSplit;
         if (s > p->k_blocks) s = p->k_blocks;
@@ -217,7 +221,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
              int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
              cudaStream_t stream) {
     CUtensorMap ma, mb, md;
-    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, 128))
+    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, C::A_ROWS))
         return GEMM_ERR_CUDA;
     if constexpr (!C::B_MN) {
         if (!encode_2d(&mb, B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, C::B_ROWS))
@@ -255,10 +259,13 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
 
 // Dispatch on (cta_group, block_n, layout, dtype) to one template instance.
 template <template <class> class Fn, class... Ts>
-int dispatch(int cg, int bn, bool b_mn, bool bf16, Ts&&... ts) {
+int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, Ts&&... ts) {
 #define GB300_CASE(CG_, BN_, MN_, BF_)                                                   \
-    if (cg == CG_ && bn == BN_ && b_mn == MN_ && bf16 == BF_)                            \
+    if (cons == 1 && cg == CG_ && bn == BN_ && b_mn == MN_ && bf16 == BF_)               \
         return Fn<Cfg<CG_, BN_, MN_, BF_>>::call(std::forward<Ts>(ts)...);
+#define GB300_CASE2(MN_, BF_)                                                            \
+    if (cons == 2 && cg == 2 && bn == 256 && b_mn == MN_ && bf16 == BF_)                 \
+        return Fn<Cfg<2, 256, MN_, BF_, 2>>::call(std::forward<Ts>(ts)...);
 #define GB300_CASES(CG_, BN_) \
     GB300_CASE(CG_, BN_, false, false) GB300_CASE(CG_, BN_, false, true) \
     GB300_CASE(CG_, BN_, true, false) GB300_CASE(CG_, BN_, true, true)
@@ -272,6 +279,11 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, Ts&&... ts) {
     GB300_KMAJOR_CASES(2, 192)
     GB300_KMAJOR_CASES(1, 224)
     GB300_KMAJOR_CASES(1, 192)
+    GB300_CASE2(false, false)
+    GB300_CASE2(false, true)
+    GB300_CASE2(true, false)
+    GB300_CASE2(true, true)
+#undef GB300_CASE2
 #undef GB300_KMAJOR_CASES
 #undef GB300_CASES
 #undef GB300_CASE
@@ -318,12 +330,14 @@ int check_options(const gemm_options_t* o) {
         return GEMM_ERR_OPTION;
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
     if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
+    if (o->consumers < 0 || o->consumers > 2) return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
 int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
     int n = 0;
-    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, dev, sm_count, &n) != GEMM_OK)
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, dev, sm_count, &n) !=
+        GEMM_OK)
         return 0;
     return n;
 }
@@ -372,8 +386,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     int dev = 0;
     cudaGetDevice(&dev);
     p->cg = (o && o->cta_group) ? o->cta_group : (M <= 128 ? 1 : 2);
-    p->bm = 128 * p->cg;
-    if (o && o->block_n) {
+    p->cons = (o && o->consumers) ? o->consumers : 1;
+    p->bm = 128 * p->cg * p->cons;
+    if (p->cons == 2) {
+        // Two consumers: 2-CTA clusters, 256-wide tiles only.
+        if (p->cg != 2 || (o && o->block_n && o->block_n != 256)) return GEMM_ERR_OPTION;
+        p->bn = 256;
+    } else if (o && o->block_n) {
         p->bn = o->block_n;
         // 192 / 224 are K-major only: an MN-major B tile is loaded in 64-column atoms.
         if (b_layout == 1 && (p->bn % 128) != 0) return GEMM_ERR_OPTION;
@@ -386,12 +405,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     p->tiles = m_tiles * n_tiles;
     if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
     int max_clusters = 0;
-    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, dev, di.sm_count,
-                           &max_clusters);
+    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, dev,
+                           di.sm_count, &max_clusters);
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
     p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
-    p->stages = (227 * 1024 - 32768 - 1024 - 512) / (128 * 64 * 2 + (p->bn / p->cg) * 64 * 2);
+    p->stages = stages_for(p->cg, p->bn, p->cons);
     p->k_blocks = (K + kBlockK - 1) / kBlockK;
     plan_split(p, o ? o->tail_split : 0, have_workspace);
     return GEMM_OK;
@@ -447,7 +466,7 @@ extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t
     if ((st = make_plan(M, N, K, dtype, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
         return st;
     if (workspace_bytes < workspace_bytes_needed(p)) return GEMM_ERR_WORKSPACE;
-    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p, A, B, D, M, N, K,
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p.cons, p, A, B, D, M, N, K,
                            lda, ldb, ldd, dtype, workspace, stream);
 }
 

@@ -65,23 +65,32 @@ enum : uint32_t {
     kRoleSelfTest = 5u
 };
 
-template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_>
+template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1>
 struct KernelConfig {
     static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
-    static constexpr int BM = 128 * CG;       // tile rows (MMA M)
+    // MMA consumers per CTA: 1, or 2 ("TIRx GEMM on Blackwell", V9: two MMAs on
+    // different A rows share each staged B tile; each CTA holds 256 A rows).
+    static constexpr int CONS = CONS_;
+    static constexpr int A_ROWS = 128 * CONS;  // A rows each CTA loads per tile
+    static constexpr int BM = A_ROWS * CG;     // tile rows
     static constexpr int BN = BN_;            // tile columns (MMA N)
     static constexpr int STAGES = STAGES_;    // SMEM ring depth
     static constexpr bool B_MN = B_MN_;       // B stored K x N (D = A.B)
     static constexpr bool BF16 = BF16_;
     static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
 
-    static constexpr uint32_t A_BYTES = 128u * kBlockK * 2u;            // 16 KiB
+    static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * kBlockK * 2u;  // 16 KiB per consumer
     static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * kBlockK * 2u;
     static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES);
     // Two accumulators of BN FP32 columns at a power-of-two stride (the TMEM
     // allocation is a power of two of at least 32 columns).
     static constexpr uint32_t ACC_STRIDE = BN <= 128 ? 128u : 256u;
-    static constexpr uint32_t TMEM_COLS = 2u * ACC_STRIDE;
+    // Accumulator slots: with one consumer, two slots (the epilogue of tile i
+    // overlaps the MMAs of tile i+1); with two consumers their two
+    // accumulators fill TMEM, so one slot.
+    static constexpr uint32_t NUM_ACC = CONS == 1 ? 2u : 1u;
+    static constexpr uint32_t SLOT_COLS = uint32_t(CONS) * ACC_STRIDE;
+    static constexpr uint32_t TMEM_COLS = NUM_ACC * SLOT_COLS;
     // Epilogue chunks: BN / 64 full 64-column chunks, plus one 32-column chunk
     // when BN is an odd multiple of 32.
     static constexpr int FULL_CHUNKS = BN / 64;
@@ -109,14 +118,25 @@ struct KernelConfig {
     // tcgen05 instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1),
     // A/B = F16 (0) or BF16 (1) at bits 7-9 / 10-12, A K-major (bit 15 = 0),
     // B major at bit 16, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+    // MMA shape (the same whatever the number of consumers): M = 128 rows per
+    // CTA of the group, N = BN.
+    static constexpr int MMA_M = 128 * CG;
     static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 0u) << 7) |
                                       ((BF16 ? 1u : 0u) << 10) | ((B_MN ? 1u : 0u) << 16) |
-                                      (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+                                      (uint32_t(BN >> 3) << 17) | (uint32_t(MMA_M >> 4) << 24);
+    static_assert(MMA_M == 128 || MMA_M == 256, "tcgen05 kind::f16 M is 128 (1 CTA) or 256 (2 CTAs)");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 kind::f16 N is a multiple of 16, <= 256");
+    static_assert(((IDESC >> 24) & 0x1Fu) == uint32_t(MMA_M >> 4) && ((IDESC >> 17) & 0x3Fu) == uint32_t(BN >> 3),
+                  "instruction descriptor fields in range");
 
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile N is a multiple of 32 in [128, 256]");
     static_assert((BN / CG) % 16 == 0, "each CTA's share of B is whole 16-row SW128 groups");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
+    static_assert(CONS == 1 || CONS == 2, "one or two MMA consumers");
+    static_assert(CONS * (FULL_CHUNKS + (HALF_CHUNK ? 1 : 0)) * EPI_BUF_BYTES <=
+                      PIECES_PER_WARP * PIECE_BYTES,
+                  "the last unit's epilogue chunks fit in each warp's share of the ring");
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
     static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
@@ -302,7 +322,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const WorkUnit w = unit_of(args, u);
                 int32_t mt, nt;
                 tile_of_task(args.grid, w.tile, mt, nt);
-                const int32_t a_row = mt * C::BM + int32_t(rank) * 128;
+                const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
                 const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
@@ -364,7 +384,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + ab * C::ACC_STRIDE;
+                const uint32_t d_tmem = tmem_base + ab * C::SLOT_COLS;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(full_bar(s), ph, abort_flag, kRoleMma)) {
                         ok = false;
@@ -375,29 +395,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t b_addr = base + C::OFF_B + s * C::B_BYTES;
 #pragma unroll
                     for (int k = 0; k < kBlockK / 16; ++k) {
-                        const uint64_t ad = sw128_desc(a_addr + 32u * k, 16u, 1024u);
                         const uint64_t bd = C::B_MN
                                                 ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
                                                 : sw128_desc(b_addr + 32u * k, 16u, 1024u);
-                        ptx::mma_f16<C::CG>(d_tmem, ad, bd, C::IDESC,
-                                            uint32_t(kb != w.kb0 || k != 0));
+#pragma unroll
+                        for (int h = 0; h < C::CONS; ++h) {
+                            // consumer h: A rows 128h..128h+127 of this stage (16 KiB each)
+                            const uint64_t ad = sw128_desc(a_addr + 16384u * h + 32u * k, 16u, 1024u);
+                            ptx::mma_f16<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd, C::IDESC,
+                                                uint32_t(kb != w.kb0 || k != 0));
+                        }
                     }
                     ptx::mma_commit<C::CG>(empty_bar(s));  // slot free once these MMAs finish
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 ptx::mma_commit<C::CG>(acc_full_bar(ab));  // accumulator ready
-                if (++ab == 2u) { ab = 0; aph ^= 1u; }
+                if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
             }
             if (ok) {
-                // Drain: both accumulators released by every epilogue warp of the
-                // cluster (the peer's arrivals target this CTA's barriers).
-                for (int i = 0; i < 2; ++i) {
+                // Drain: every accumulator slot released by every epilogue warp of
+                // the cluster (the peer's arrivals target this CTA's barriers).
+                for (uint32_t i = 0; i < C::NUM_ACC; ++i) {
                     if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
                         ok = false;
                         break;
                     }
-                    if (++ab == 2u) { ab = 0; aph ^= 1u; }
+                    if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
                 }
             }
             if (!ok) settle_after_abort();
@@ -506,30 +530,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }  // completed already: gives every lane its own acquire
             ptx::tc_fence_after();
 
-            const int32_t row0 = mt * C::BM + int32_t(rank) * 128 + int32_t(quarter) * 32;
+            const int32_t row0 = mt * C::BM + int32_t(rank) * C::A_ROWS + int32_t(quarter) * 32;
             const int32_t col0 = nt * C::BN;
-            const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::ACC_STRIDE;
+            const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::SLOT_COLS;
 
             if (w.range < 0) {
-                // Whole tile: TMEM -> D.
+                // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
+                // the CTA's A rows 128h..128h+127).
                 const bool last_unit = (u + num_clusters >= units);
 #pragma unroll 1
-                for (int j = 0; j < C::FULL_CHUNKS; ++j) {
-                    uint32_t bits[64];
-                    ptx::tmem_ld_32x32b_x32(taddr + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&bits[0]));
-                    ptx::tmem_ld_32x32b_x32(taddr + 64u * j + 32u,
-                                            *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
-                    ptx::tmem_wait_ld();
-                    if (j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release_acc(ab);
-                    store_chunk(bits, col0 + 64 * j, row0, last_unit ? j : -1);
-                }
-                if constexpr (C::HALF_CHUNK) {
-                    // Last 32 columns: this lane's row, 64 bytes, stored directly.
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + 64u * C::FULL_CHUNKS, r);
-                    ptx::tmem_wait_ld();
-                    release_acc(ab);
-                    store_half_chunk(r, col0 + 64 * C::FULL_CHUNKS, row0 + int32_t(lane));
+                for (int h = 0; h < C::CONS; ++h) {
+                    const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
+                    const int32_t rh = row0 + 128 * h;
+                    const bool last_h = (h == C::CONS - 1);
+#pragma unroll 1
+                    for (int j = 0; j < C::FULL_CHUNKS; ++j) {
+                        uint32_t bits[64];
+                        ptx::tmem_ld_32x32b_x32(th + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&bits[0]));
+                        ptx::tmem_ld_32x32b_x32(th + 64u * j + 32u,
+                                                *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
+                        ptx::tmem_wait_ld();
+                        if (last_h && j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release_acc(ab);
+                        store_chunk(bits, col0 + 64 * j, rh, last_unit ? h * C::FULL_CHUNKS + j : -1);
+                    }
+                    if constexpr (C::HALF_CHUNK) {
+                        // Last 32 columns: this lane's row, 64 bytes, stored directly.
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(th + 64u * C::FULL_CHUNKS, r);
+                        ptx::tmem_wait_ld();
+                        if (last_h) release_acc(ab);
+                        store_half_chunk(r, col0 + 64 * C::FULL_CHUNKS, rh + int32_t(lane));
+                    }
                 }
             } else {
                 // K-range of a tail tile.  Pass 1: write this range's FP32 partial
@@ -666,7 +697,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
             }
-            if (++ab == 2u) { ab = 0; aph ^= 1u; }
+            if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
         }
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();

@@ -100,6 +100,14 @@ const char* gemm_status_string(int status);
  *                 keep every cluster and split each tile of the last, partial
  *                 round into s K-ranges (capped by the number of 64-wide
  *                 k-blocks).
+ *   consumers     0 or 1 = one MMA accumulator per CTA and tile, two TMEM
+ *                 accumulator slots so the epilogue of one tile overlaps the
+ *                 next tile's MMAs.  2 = two accumulators per CTA that share
+ *                 each staged B tile ("TIRx GEMM on Blackwell", V9): each CTA
+ *                 holds 256 rows of A, a tile is 512 x 256 (cta_group 2 and
+ *                 block_n 256 only), operand traffic per FLOP drops by a
+ *                 quarter, and the two accumulators fill TMEM, so a tile's
+ *                 epilogue no longer overlaps the next tile's MMAs.
  */
 typedef struct {
     int cta_group;
@@ -107,6 +115,7 @@ typedef struct {
     int raster_group;
     int max_clusters;
     int tail_split;
+    int consumers;
 } gemm_options_t;
 
 /* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */

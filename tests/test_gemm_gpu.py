@@ -27,8 +27,11 @@ VARIANTS = [
     {"cta_group": 2, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 2, "block_n": 192, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 1, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
+    {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0,
+     "consumers": 2},
 ]
-VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224"]
+VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224",
+       "cg2_n256_2cons"]
 
 
 def k_major_only(variant, layout):
@@ -362,6 +365,8 @@ def _fuzz_cases(n=48, seed=2026):
         opts = {"cta_group": cg, "block_n": bn, "raster_group": int(rng.choice([0, 1, 3])),
                 "max_clusters": int(rng.choice([0, 1, 2, 5])),
                 "tail_split": int(rng.choice([0, 0, 2, 3]))}
+        if cg == 2 and bn in (0, 256) and rng.random() < 0.4:
+            opts["consumers"] = 2
         pad = [int(rng.choice([0, 8, 24])) for _ in range(2)]
         cases.append((i, layout, dtype, M, N, K, opts, pad))
     return cases
@@ -374,3 +379,20 @@ def test_random_cases(case):
     ldb = (K if layout == "abt" else N) + pad[1]
     parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=M * 7 + N,
            options=opts, lda=lda, ldb=ldb)
+
+
+def test_two_consumers_many_tiles_per_cluster():
+    # 512 x 256 tiles, few clusters: the single TMEM slot is reused by every
+    # tile of a cluster, so each tile's MMAs wait for the previous epilogue.
+    for layout, dtype in (("abt", "f16"), ("ab", "bf16")):
+        opts = {"cta_group": 2, "consumers": 2, "max_clusters": 3}
+        parity(1300, 1104, 640, layout, dtype, seed=13, options=opts)
+
+
+def test_two_consumer_option_limits():
+    A = torch.zeros((512, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
+    for bad in ({"consumers": 2, "cta_group": 1}, {"consumers": 2, "block_n": 128}):
+        with pytest.raises(binding.GemmError) as e:
+            binding.gemm_abt(A, B, options=bad)
+        assert e.value.status == -8
