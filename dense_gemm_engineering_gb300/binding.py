@@ -46,7 +46,8 @@ class GemmOptions(ctypes.Structure):
     """gemm_options_t."""
     _fields_ = [("cta_group", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
-                ("tail_split", ctypes.c_int), ("consumers", ctypes.c_int)]
+                ("tail_split", ctypes.c_int), ("consumers", ctypes.c_int),
+                ("multicast", ctypes.c_int)]
 
 
 _lib = None

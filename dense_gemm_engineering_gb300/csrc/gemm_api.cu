@@ -94,13 +94,13 @@ template <class C>
 void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                     const GemmArgs& args, int clusters, cudaStream_t stream, cudaError_t* err) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(clusters * C::CG), 1, 1);
+    cfg.gridDim = dim3(unsigned(clusters * C::CLUSTER), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.x = C::CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -116,12 +116,12 @@ int query_max_clusters(int dev, int sm_count) {
         cudaSuccess)
         return -1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(C::CG * (sm_count / C::CG)), 1, 1);
+    cfg.gridDim = dim3(unsigned(C::CLUSTER * (sm_count / C::CLUSTER)), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C::CG;
+    attr[0].val.clusterDim.x = C::CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -146,12 +146,13 @@ struct Stages {
     static constexpr int value = stages_for(CG, BN, CONS);
 };
 
-template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1>
-using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS>;
+template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC>;
 
 struct Plan {
     int cg, bm, bn, stages;
     int cons;  // MMA consumers per CTA
+    int mc;    // CTA pairs per cluster sharing A by multicast
     int clusters;
     int64_t tiles;
     int group;
@@ -198,7 +199,8 @@ void plan_split(Plan* p, int requested, bool have_workspace) {
     p->whole_units = p->tiles;
     p->split = 1;
     const int64_t tail = p->clusters > 0 ? p->tiles % p->clusters : 0;
-    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0 && p->cons == 1) {
+    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0 && p->cons == 1 &&
+        p->mc == 1) {
         int64_t s = requested;
         if (s > kMaxSplit) s = kMaxSplit;
         if (s > p->k_blocks) s = p->k_blocks;
@@ -221,7 +223,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
              int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
              cudaStream_t stream) {
     CUtensorMap ma, mb, md;
-    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, C::A_ROWS))
+    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, C::A_BOX_ROWS))
         return GEMM_ERR_CUDA;
     if constexpr (!C::B_MN) {
         if (!encode_2d(&mb, B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, C::B_ROWS))
@@ -240,7 +242,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     args.K = int32_t(K);
     args.k_blocks = int32_t((K + kBlockK - 1) / kBlockK);
     args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
-    args.grid.n_tiles = int32_t((N + C::BN - 1) / C::BN);
+    args.grid.n_tiles = int32_t((N + C::BN_CLUSTER - 1) / C::BN_CLUSTER);
     args.grid.group = p.group;
     args.whole_units = p.whole_units;
     args.split = p.split;
@@ -259,7 +261,16 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
 
 // Dispatch on (cta_group, block_n, layout, dtype) to one template instance.
 template <template <class> class Fn, class... Ts>
-int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, Ts&&... ts) {
+int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, Ts&&... ts) {
+#define GB300_CASEMC(MN_, BF_)                                                           \
+    if (mc == 2 && cons == 1 && cg == 2 && bn == 256 && b_mn == MN_ && bf16 == BF_)      \
+        return Fn<Cfg<2, 256, MN_, BF_, 1, 2>>::call(std::forward<Ts>(ts)...);
+    GB300_CASEMC(false, false)
+    GB300_CASEMC(false, true)
+    GB300_CASEMC(true, false)
+    GB300_CASEMC(true, true)
+#undef GB300_CASEMC
+    if (mc != 1) return GEMM_ERR_OPTION;
 #define GB300_CASE(CG_, BN_, MN_, BF_)                                                   \
     if (cons == 1 && cg == CG_ && bn == BN_ && b_mn == MN_ && bf16 == BF_)               \
         return Fn<Cfg<CG_, BN_, MN_, BF_>>::call(std::forward<Ts>(ts)...);
@@ -331,12 +342,13 @@ int check_options(const gemm_options_t* o) {
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
     if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
     if (o->consumers < 0 || o->consumers > 2) return GEMM_ERR_OPTION;
+    if (o->multicast < 0 || o->multicast > 2) return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
 int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
     int n = 0;
-    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, dev, sm_count, &n) !=
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, 1, dev, sm_count, &n) !=
         GEMM_OK)
         return 0;
     return n;
@@ -385,12 +397,17 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     if (st != GEMM_OK) return st;
     int dev = 0;
     cudaGetDevice(&dev);
-    p->cg = (o && o->cta_group) ? o->cta_group : (M <= 128 ? 1 : 2);
+    p->mc = (o && o->multicast) ? o->multicast : 1;
+    p->cg = (o && o->cta_group) ? o->cta_group : ((M <= 128 && p->mc == 1) ? 1 : 2);
     p->cons = (o && o->consumers) ? o->consumers : 1;
+    if (p->mc == 2 && (p->cg != 2 || p->cons != 1 || (o && o->block_n && o->block_n != 256)))
+        return GEMM_ERR_OPTION;
     p->bm = 128 * p->cg * p->cons;
     if (p->cons == 2) {
         // Two consumers: 2-CTA clusters, 256-wide tiles only.
         if (p->cg != 2 || (o && o->block_n && o->block_n != 256)) return GEMM_ERR_OPTION;
+        p->bn = 256;
+    } else if (p->mc == 2) {
         p->bn = 256;
     } else if (o && o->block_n) {
         p->bn = o->block_n;
@@ -401,11 +418,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     }
     p->group = (o && o->raster_group) ? o->raster_group : 16;
     const int64_t m_tiles = (M + p->bm - 1) / p->bm;
-    const int64_t n_tiles = (N + p->bn - 1) / p->bn;
+    const int64_t n_tiles = (N + p->bn * p->mc - 1) / (p->bn * p->mc);
     p->tiles = m_tiles * n_tiles;
     if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
     int max_clusters = 0;
-    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, dev,
+    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, p->mc, dev,
                            di.sm_count, &max_clusters);
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
@@ -466,7 +483,7 @@ extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t
     if ((st = make_plan(M, N, K, dtype, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
         return st;
     if (workspace_bytes < workspace_bytes_needed(p)) return GEMM_ERR_WORKSPACE;
-    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p.cons, p, A, B, D, M, N, K,
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p.cons, p.mc, p, A, B, D, M, N, K,
                            lda, ldb, ldd, dtype, workspace, stream);
 }
 

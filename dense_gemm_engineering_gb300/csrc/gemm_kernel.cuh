@@ -65,9 +65,14 @@ enum : uint32_t {
     kRoleSelfTest = 5u
 };
 
-template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1>
+template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1>
 struct KernelConfig {
     static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
+    // CTA pairs per cluster: 1, or 2 side by side along N that share A — each
+    // CTA loads half of its A rows and multicasts them to its counterpart in
+    // the other pair, so A's L2 -> SMEM traffic halves.
+    static constexpr int MC = MC_;
+    static constexpr int CLUSTER = CG * MC;   // CTAs per cluster
     // MMA consumers per CTA: 1, or 2 ("TIRx GEMM on Blackwell", V9: two MMAs on
     // different A rows share each staged B tile; each CTA holds 256 A rows).
     static constexpr int CONS = CONS_;
@@ -134,6 +139,9 @@ struct KernelConfig {
     static_assert((BN / CG) % 16 == 0, "each CTA's share of B is whole 16-row SW128 groups");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(CONS == 1 || CONS == 2, "one or two MMA consumers");
+    static_assert(MC == 1 || (MC == 2 && CG == 2 && CONS == 1), "A multicast pairs 2-CTA, 1-consumer tiles");
+    static constexpr int A_BOX_ROWS = A_ROWS / MC;  // A rows per TMA issue
+    static constexpr int BN_CLUSTER = BN * MC;      // columns of a cluster's tile
     static_assert(CONS * (FULL_CHUNKS + (HALF_CHUNK ? 1 : 0)) * EPI_BUF_BYTES <=
                       PIECES_PER_WARP * PIECE_BYTES,
                   "the last unit's epilogue chunks fit in each warp's share of the ring");
@@ -271,10 +279,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
     const uint32_t lane = threadIdx.x % 32u;
-    const uint32_t rank = (C::CG == 2) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t crank = (C::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t rank = crank & uint32_t(C::CG - 1);         // CTA within its pair
+    const uint32_t pair = crank / uint32_t(C::CG);             // pair within the cluster
+    const uint32_t pair_leader = crank & ~uint32_t(C::CG - 1);  // cluster rank of the pair's leader
     const bool leader = (rank == 0u);
-    const int64_t cluster_id = blockIdx.x / C::CG;
-    const int64_t num_clusters = gridDim.x / C::CG;
+    const int64_t cluster_id = blockIdx.x / C::CLUSTER;
+    const int64_t num_clusters = gridDim.x / C::CLUSTER;
     const int64_t units = unit_count(args);
 
     auto full_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * s; };
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
             ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
-            ptx::mbar_init(empty_bar(s), 1);  // one tcgen05.commit per use
+            ptx::mbar_init(empty_bar(s), uint32_t(C::MC));  // one tcgen05.commit per pair
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
@@ -309,7 +320,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         ptx::tmem_relinquish<C::CG>();
     }
     ptx::tc_fence_before();
-    if constexpr (C::CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if constexpr (C::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
 
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 int32_t mt, nt;
                 tile_of_task(args.grid, w.tile, mt, nt);
                 const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
-                const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
+                const int32_t b_row = nt * C::BN_CLUSTER + int32_t(pair) * C::BN + int32_t(rank) * C::B_ROWS;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
                         ok = false;
@@ -344,8 +355,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                  b_row + 64 * c, k0);
                         }
                     } else {
-                        const uint32_t fb = ptx::map_to_rank(full_bar(s), 0);
-                        ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
+                        const uint32_t fb = ptx::map_to_rank(full_bar(s), pair_leader);
+                        if constexpr (C::MC == 1) {
+                            ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
+                        } else {
+                            // this pair's share of the A rows, to the same CTA rank of every pair
+                            uint16_t mask = 0;
+#pragma unroll
+                            for (int q = 0; q < C::MC; ++q) mask |= uint16_t(1u << (q * C::CG + rank));
+                            ptx::tma_load_2d_pair_multicast(a_dst + pair * (C::A_BOX_ROWS * 128u), &tmap_a,
+                                                            fb, k0, a_row + int32_t(pair) * C::A_BOX_ROWS,
+                                                            mask);
+                        }
                         if constexpr (!C::B_MN) {
                             ptx::tma_load_2d_pair(b_dst, &tmap_b, fb, k0, b_row);
                         } else {
@@ -406,11 +427,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                 uint32_t(kb != w.kb0 || k != 0));
                         }
                     }
-                    ptx::mma_commit<C::CG>(empty_bar(s));  // slot free once these MMAs finish
+                    // slot free (in every CTA that received data for it) once these MMAs finish
+                    ptx::mma_commit<C::CG>(empty_bar(s), uint16_t((1u << C::CLUSTER) - 1u));
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit<C::CG>(acc_full_bar(ab));  // accumulator ready
+                ptx::mma_commit<C::CG>(acc_full_bar(ab), uint16_t(0x3u << pair_leader));  // accumulator ready
                 if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
             }
             if (ok) {
@@ -441,7 +463,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if constexpr (C::CG == 2)
-                    ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(b), 0));
+                    ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(b), pair_leader));
                 else
                     ptx::mbar_arrive(acc_empty_bar(b));
             }
@@ -531,7 +553,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_fence_after();
 
             const int32_t row0 = mt * C::BM + int32_t(rank) * C::A_ROWS + int32_t(quarter) * 32;
-            const int32_t col0 = nt * C::BN;
+            const int32_t col0 = nt * C::BN_CLUSTER + int32_t(pair) * C::BN;
             const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::SLOT_COLS;
 
             if (w.range < 0) {
@@ -705,7 +727,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     // ---- teardown ---------------------------------------------------------
     ptx::tc_fence_before();
-    if constexpr (C::CG == 2) ptx::cluster_sync(); else __syncthreads();
+    if constexpr (C::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);

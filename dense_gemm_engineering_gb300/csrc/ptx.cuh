@@ -122,6 +122,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Same, multicast: the tile lands at the same offset in the shared memory of
+// every CTA in `cta_mask`, and each destination's completion is signalled on
+// the barrier at `cluster_bar`'s offset in that destination's pair leader.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
+                                                           uint32_t cluster_bar, int32_t x,
+                                                           int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
 // 2-D tile store from shared memory; out-of-bounds elements are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y) {
@@ -237,9 +250,9 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 
 // Arrive (once) on `bar` when all previously issued MMAs of this thread have
 // completed.  For a CTA pair the arrive goes to the barrier at the same offset
-// in both CTAs.
+// in every CTA of `cta_mask` (the pair itself by default).
 template <int CG>
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t cta_mask = 0x3) {
     if constexpr (CG == 1)
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                          bar)
@@ -248,7 +261,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         asm volatile(
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
             " [%0], %1;" ::"r"(bar),
-            "h"(static_cast<uint16_t>(0x3))
+            "h"(cta_mask)
             : "memory");
 }
 

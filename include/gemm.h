@@ -108,6 +108,11 @@ const char* gemm_status_string(int status);
  *                 block_n 256 only), operand traffic per FLOP drops by a
  *                 quarter, and the two accumulators fill TMEM, so a tile's
  *                 epilogue no longer overlaps the next tile's MMAs.
+ *   multicast     0 or 1 = one CTA pair per cluster.  2 = clusters of two
+ *                 pairs side by side along N (a 256 x 512 cluster tile,
+ *                 cta_group 2, block_n 256, one consumer) that share A: each
+ *                 CTA loads half of its 128 A rows and multicasts them to the
+ *                 same rank of the other pair, halving A's L2 -> SMEM traffic.
  */
 typedef struct {
     int cta_group;
@@ -116,6 +121,7 @@ typedef struct {
     int max_clusters;
     int tail_split;
     int consumers;
+    int multicast;
 } gemm_options_t;
 
 /* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */
