@@ -242,6 +242,14 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// wait_bounded for a whole converged warp: every lane waits (and acquires), and
+// all lanes return the same result.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t* abort_flag, uint32_t role) {
+    const bool ok = wait_bounded(bar, parity, abort_flag, role);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // After an abort: give in-flight asynchronous copies and MMAs (which complete
 // in microseconds) time to land before shared memory and TMEM are released.
 __device__ __forceinline__ void settle_after_abort() {
@@ -324,22 +332,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
 
+    // The producer and the MMA issuer run warp-converged and let one elected
+    // lane issue: every value the loop computes is then warp-uniform, and a
+    // tcgen05.mma / TMA issue from a converged warp costs the issuing thread
+    // far less than from a single-lane branch.  With the loop confined to one
+    // lane, the issuer needed ~535 cycles per k-block (4 MMAs, a barrier wait
+    // and a commit) -- more than the 512 tensor cycles of a 256-wide k-block.
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------
-        if (lane == 0) {
-            uint32_t s = 0, ph = 0;
-            bool ok = true;
-            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
-                const WorkUnit w = unit_of(args, u);
-                int32_t mt, nt;
-                tile_of_task(args.grid, w.tile, mt, nt);
-                const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
-                const int32_t b_row = nt * C::BN_CLUSTER + int32_t(pair) * C::BN + int32_t(rank) * C::B_ROWS;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
-                        ok = false;
-                        break;
-                    }
+        uint32_t s = 0, ph = 0;
+        bool ok = true;
+        for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
+            const WorkUnit w = unit_of(args, u);
+            int32_t mt, nt;
+            tile_of_task(args.grid, w.tile, mt, nt);
+            const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
+            const int32_t b_row = nt * C::BN_CLUSTER + int32_t(pair) * C::BN + int32_t(rank) * C::B_ROWS;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
+                    ok = false;
+                    break;
+                }
+                if (ptx::elect_one_sync()) {
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_TX);
                     const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
                     const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
@@ -376,70 +390,76 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                       b_row + 64 * c, k0);
                         }
                     }
-                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
+                __syncwarp();
+                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
             }
-            if (ok) {
-                // Drain: every slot must have been released by the MMA, so no
-                // tcgen05.commit arrives on this CTA's barriers after it exits.
-                for (int i = 0; i < C::STAGES; ++i) {
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kRoleDrain)) {
-                        ok = false;
-                        break;
-                    }
-                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
-                }
-            }
-            if (!ok) settle_after_abort();
         }
+        if (ok) {
+            // Drain: every slot must have been released by the MMA, so no
+            // tcgen05.commit arrives on this CTA's barriers after it exits.
+            for (int i = 0; i < C::STAGES; ++i) {
+                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleDrain)) {
+                    ok = false;
+                    break;
+                }
+                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+            }
+        }
+        if (!ok) settle_after_abort();
         __syncwarp();
     } else if (warp == 1) {
-        // ---- MMA issuer (leader CTA, one thread) ---------------------------
-        if (leader && lane == 0) {
+        // ---- MMA issuer (leader CTA) ------------------------------------------
+        if (leader) {
             uint32_t s = 0, ph = 0, ab = 0, aph = 0;
             bool ok = true;
             for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
                 const WorkUnit w = unit_of(args, u);
-                if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleMma)) {
+                if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleMma)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * C::SLOT_COLS;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, kRoleMma)) {
+                    if (!wait_bounded_warp(full_bar(s), ph, abort_flag, kRoleMma)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint32_t a_addr = base + C::OFF_A + s * C::A_BYTES;
                     const uint32_t b_addr = base + C::OFF_B + s * C::B_BYTES;
+                    if (ptx::elect_one_sync()) {
 #pragma unroll
-                    for (int k = 0; k < kBlockK / 16; ++k) {
-                        const uint64_t bd = C::B_MN
-                                                ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
-                                                : sw128_desc(b_addr + 32u * k, 16u, 1024u);
+                        for (int k = 0; k < kBlockK / 16; ++k) {
+                            const uint64_t bd = C::B_MN
+                                                    ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
+                                                    : sw128_desc(b_addr + 32u * k, 16u, 1024u);
 #pragma unroll
-                        for (int h = 0; h < C::CONS; ++h) {
-                            // consumer h: A rows 128h..128h+127 of this stage (16 KiB each)
-                            const uint64_t ad = sw128_desc(a_addr + 16384u * h + 32u * k, 16u, 1024u);
-                            ptx::mma_f16<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd, C::IDESC,
-                                                uint32_t(kb != w.kb0 || k != 0));
+                            for (int h = 0; h < C::CONS; ++h) {
+                                // consumer h: A rows 128h..128h+127 of this stage (16 KiB each)
+                                const uint64_t ad = sw128_desc(a_addr + 16384u * h + 32u * k, 16u, 1024u);
+                                ptx::mma_f16<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd, C::IDESC,
+                                                    uint32_t(kb != w.kb0 || k != 0));
+                            }
                         }
+                        // slot free (in every CTA that received data for it) once these MMAs finish
+                        ptx::mma_commit<C::CG>(empty_bar(s), uint16_t((1u << C::CLUSTER) - 1u));
                     }
-                    // slot free (in every CTA that received data for it) once these MMAs finish
-                    ptx::mma_commit<C::CG>(empty_bar(s), uint16_t((1u << C::CLUSTER) - 1u));
+                    __syncwarp();
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit<C::CG>(acc_full_bar(ab), uint16_t(0x3u << pair_leader));  // accumulator ready
+                if (ptx::elect_one_sync())
+                    ptx::mma_commit<C::CG>(acc_full_bar(ab), uint16_t(0x3u << pair_leader));  // accumulator ready
+                __syncwarp();
                 if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
             }
             if (ok) {
                 // Drain: every accumulator slot released by every epilogue warp of
                 // the cluster (the peer's arrivals target this CTA's barriers).
                 for (uint32_t i = 0; i < C::NUM_ACC; ++i) {
-                    if (!wait_bounded(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
+                    if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
                         ok = false;
                         break;
                     }

@@ -29,6 +29,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// True on exactly one lane of the (converged) calling warp.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n"
+        ".reg .b32 rx;\n"
+        ".reg .pred px;\n"
+        "elect.sync rx|px, %1;\n"
+        "@px mov.s32 %0, 1;\n"
+        "}\n"
+        : "+r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // ---- cluster --------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
