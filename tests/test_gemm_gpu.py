@@ -331,8 +331,9 @@ def test_workspace_errors():
 
 def test_default_plan_is_a_balanced_grid():
     # Automatic plans spread the rounds over the fewest clusters that keep the
-    # round count: e.g. 4096^3 with 256-wide tiles has 256 tiles; with 76
-    # co-resident clusters that is 4 rounds, run on ceil(256 / 4) = 64 clusters.
+    # round count: e.g. 3000 x 5000 with 224-wide tiles has 12 x 23 = 276 tiles;
+    # with 76 co-resident clusters that is 4 rounds, run on ceil(276 / 4) = 69
+    # clusters.
     for M, N, K in [(4096, 4096, 4096), (3000, 5000, 4000), (8192, 17408, 5120)]:
         plan = binding.gemm_plan(M, N, K, 0, 0)
         full = binding.gemm_plan(M, N, K, 0, 0, {"block_n": plan["block_n"], "tail_split": 16})
@@ -342,11 +343,15 @@ def test_default_plan_is_a_balanced_grid():
         assert plan["num_clusters"] == -(-plan["num_tiles"] // rounds)
 
 
-def test_automatic_width_prefers_256_unless_rounds_drop():
-    # 4096 x 4096 on the full device: 224-wide tiles (304 tiles) take as many
-    # rounds as 256-wide tiles (256 tiles) on 76 clusters, so the automatic
-    # plan keeps 256.  The MN-major A.B layout always uses a multiple of 128.
-    assert binding.gemm_plan(4096, 4096, 4096, 0, 0)["block_n"] == 256
+def test_automatic_width_minimises_rounds_times_width():
+    # 76 two-CTA clusters.  4096 x 4096: 256-wide tiles take 4 rounds of 256
+    # columns, 224-wide tiles 4 rounds of 224, so 224 wins.  8192 x 8192: 14
+    # rounds x 256 against 16 x 224, a tie that the larger tile takes.
+    # 2048 x 2048: 64 tiles of 256 fit one round, 224 would need two.  The
+    # MN-major A.B layout always uses a multiple of 128.
+    assert binding.gemm_plan(4096, 4096, 4096, 0, 0)["block_n"] == 224
+    assert binding.gemm_plan(8192, 8192, 8192, 1, 0)["block_n"] == 256
+    assert binding.gemm_plan(2048, 2048, 8192, 0, 0)["block_n"] == 256
     assert binding.gemm_plan(8192, 17408, 5120, 1, 1)["block_n"] in (128, 256)
 
 

@@ -67,9 +67,10 @@ def test_no_alloc_matches_workspace_path_twice(case):
 
 
 def test_no_alloc_rejects_plans_beyond_its_scratch():
-    # 4096^3 on 76 clusters leaves 28 tail tiles; a forced 16-way split would
-    # need 28 x 16 x 256 KiB = 112 MiB of scratch, beyond the fixed 20 MiB.
-    opts = {"cta_group": 2, "tail_split": 16}
+    # 4096^3 in 256-wide tiles on 76 clusters leaves 28 tail tiles; a forced
+    # 16-way split would need 28 x 16 x 256 KiB = 112 MiB of scratch, beyond the
+    # fixed 20 MiB.
+    opts = {"cta_group": 2, "block_n": 256, "tail_split": 16}
     need = binding.gemm_workspace_size(4096, 4096, 4096, 0, 0, opts)
     if need <= 20 << 20:
         pytest.skip("this GPU's plan fits in the scratch")
