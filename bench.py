@@ -89,15 +89,42 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed, so that
+    the hash below changes with the code only.  String and character literals
+    are kept verbatim."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: ncu traffic figures are valid only for this hash."""
+    """Hash of the CUDA sources' code (comments and layout ignored): ncu traffic
+    figures are valid only for this hash."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_engineering_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "gemm.h"), "rb") as f:
-        h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + strip_c_comments(f.read()).encode())
+    with open(os.path.join(ROOT, "include", "gemm.h"), encoding="utf-8") as f:
+        h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -332,12 +332,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
 
-    // The producer and the MMA issuer run warp-converged and let one elected
-    // lane issue: every value the loop computes is then warp-uniform, and a
-    // tcgen05.mma / TMA issue from a converged warp costs the issuing thread
-    // far less than from a single-lane branch.  With the loop confined to one
-    // lane, the issuer needed ~535 cycles per k-block (4 MMAs, a barrier wait
-    // and a commit) -- more than the 512 tensor cycles of a 256-wide k-block.
+    // The producer and the MMA issuer are warp roles whose loops run on the whole
+    // warp, with one elected lane issuing each TMA copy, MMA and commit ("TIRx: A
+    // Unified Tile Primitive ML Compiler", Figure 3: elect_sync() picks the issuing
+    // thread; "TIRx GEMM on Blackwell": one elected thread submits a tcgen05 MMA).
+    // Every value the loop computes is then warp-uniform.  With the loop confined
+    // to one lane instead, the issuer needed ~535 cycles per k-block (4 MMAs, a
+    // barrier wait and a commit): more than the 512 tensor cycles of a 256-wide
+    // k-block.
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------
         uint32_t s = 0, ph = 0;

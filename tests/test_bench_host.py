@@ -81,3 +81,12 @@ def test_traffic_lookup_matches_only_current_kernel(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w1", h) == 123
     assert bench.recorded_traffic("w2", h) is None
     assert bench.recorded_traffic("w1", "ffffffffffff") is None
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    code = 'int f(int x) { return x + 1; } // add one\n/* block */ const char* s = "// not a comment";'
+    same = 'int  f(int x) {\n  return x + 1;\n}\nconst char* s = "// not a comment"; // note'
+    other = 'int f(int x) { return x + 2; }\nconst char* s = "// not a comment";'
+    assert bench.strip_c_comments(code) == bench.strip_c_comments(same)
+    assert bench.strip_c_comments(code) != bench.strip_c_comments(other)
+    assert '"// not a comment"' in bench.strip_c_comments(code)
