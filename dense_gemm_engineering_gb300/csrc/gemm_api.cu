@@ -422,6 +422,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     const int64_t m_tiles = (M + p->bm - 1) / p->bm;
     const int64_t n_tiles = (N + p->bn * p->mc - 1) / (p->bn * p->mc);
     p->tiles = m_tiles * n_tiles;
+    if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
     if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
     int max_clusters = 0;
     st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, p->mc, dev,
@@ -547,7 +548,7 @@ extern "C" int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, 
     g.m_tiles = int32_t((M + block_m - 1) / block_m);
     g.n_tiles = int32_t((N + block_n - 1) / block_n);
     g.group = group;
-    if (task < 0 || task >= tile_count(g)) return GEMM_ERR_SHAPE;
+    if (tile_count(g) >= kMaxTiles || task < 0 || task >= tile_count(g)) return GEMM_ERR_SHAPE;
     int32_t mt, nt;
     tile_of_task(g, task, mt, nt);
     if (m0) *m0 = int64_t(mt) * block_m;

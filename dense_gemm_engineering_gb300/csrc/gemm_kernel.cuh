@@ -188,12 +188,14 @@ __host__ __device__ __forceinline__ WorkUnit unit_of(const GemmArgs& a, int64_t 
         w.range = -1;
         w.tail = -1;
     } else {
-        const int64_t v = u - a.whole_units;
-        w.tail = v / a.split;
-        w.range = int32_t(v - w.tail * a.split);
-        w.tile = a.whole_units + w.tail;
-        w.kb0 = int32_t((int64_t(w.range) * a.k_blocks) / a.split);
-        w.kb1 = int32_t((int64_t(w.range + 1) * a.k_blocks) / a.split);
+        // 32-bit arithmetic (unit counts are below 2^31; see kMaxTiles)
+        const uint32_t v = uint32_t(u - a.whole_units), split = uint32_t(a.split);
+        const uint32_t tail = v / split;
+        w.tail = tail;
+        w.range = int32_t(v - tail * split);
+        w.tile = a.whole_units + tail;
+        w.kb0 = int32_t((uint32_t(w.range) * uint32_t(a.k_blocks)) / split);
+        w.kb1 = int32_t((uint32_t(w.range + 1) * uint32_t(a.k_blocks)) / split);
     }
     return w;
 }

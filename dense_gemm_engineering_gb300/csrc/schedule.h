@@ -33,16 +33,24 @@ GB300_HD int64_t tile_count(const TileGrid& g) {
     return static_cast<int64_t>(g.m_tiles) * g.n_tiles;
 }
 
-// Task -> (m tile, n tile).  Requires 0 <= task < tile_count(g).
+// Largest tile count the scheduler handles: its index arithmetic is 32-bit (a
+// 64-bit division is a long software routine on the GPU, and the producer's
+// first TMA issue waits on this map).  Far beyond any output that fits in memory.
+constexpr int64_t kMaxTiles = int64_t(1) << 31;
+
+// Task -> (m tile, n tile).  Requires 0 <= task < tile_count(g) < kMaxTiles.
 GB300_HD void tile_of_task(const TileGrid& g, int64_t task, int32_t& mt, int32_t& nt) {
-    const int64_t per_group = static_cast<int64_t>(g.group) * g.n_tiles;
-    const int64_t grp = task / per_group;
-    const int64_t first_m = grp * g.group;
-    const int64_t rows_in_group =
-        (g.m_tiles - first_m) < g.group ? (g.m_tiles - first_m) : g.group;
-    const int64_t r = task - grp * per_group;
-    nt = static_cast<int32_t>(r / rows_in_group);
-    mt = static_cast<int32_t>(first_m + r % rows_in_group);
+    const uint32_t t = static_cast<uint32_t>(task);
+    const uint32_t group = static_cast<uint32_t>(g.group);
+    const uint32_t per_group = group * static_cast<uint32_t>(g.n_tiles);  // <= tile count
+    const uint32_t grp = t / per_group;
+    const uint32_t first_m = grp * group;
+    const uint32_t left = static_cast<uint32_t>(g.m_tiles) - first_m;
+    const uint32_t rows_in_group = left < group ? left : group;
+    const uint32_t r = t - grp * per_group;
+    const uint32_t q = r / rows_in_group;
+    nt = static_cast<int32_t>(q);
+    mt = static_cast<int32_t>(first_m + (r - q * rows_in_group));
 }
 
 }  // namespace gb300

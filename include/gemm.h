@@ -201,7 +201,9 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
  * The persistent scheduler's task -> tile map (the same function the kernel
  * runs), for host-side checks.  Tiles of block_m x block_n cover the M x N
  * output; `group` M tiles form a raster group.  Writes the tile's first row
- * and column.  Returns GEMM_ERR_SHAPE if task is outside [0, tiles).
+ * and column.  Returns GEMM_ERR_SHAPE if task is outside [0, tiles) or if
+ * there are 2^31 tiles or more (the scheduler's index arithmetic is 32-bit;
+ * gemm_run rejects such sizes with the same error).
  */
 int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
                      int64_t task, int64_t* m0, int64_t* n0);

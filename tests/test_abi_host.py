@@ -151,3 +151,20 @@ def test_smem_carve_up_is_disjoint():
         for (s0, e0), (s1, e1) in zip(spans, spans[1:]):
             assert e0 == s1 and s0 < e0
         assert spans[-1][1] + (2 * stages + 4) * 8 + 8 + 1024 <= 232448
+
+
+def test_tile_map_limits_and_large_grids(lib):
+    # The scheduler's index arithmetic is 32-bit: 2^31 tiles or more is a shape
+    # error; just below the limit the map still covers the far corner.
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_tile_origin(1 << 30, 1 << 30, 128, 128, 16, 0)  # 2^46 tiles
+    assert e.value.status == -3
+    M, N, bm, bn, group = 46340 * 128, 46340 * 128, 128, 128, 16  # 2,147,395,600 tiles < 2^31
+    tiles = (M // bm) * (N // bn)
+    assert tiles < 2**31
+    assert binding.gemm_tile_origin(M, N, bm, bn, group, tiles - 1) == (M - bm, N - bn)
+    # the first task of the last (full) group and the last task of the grid
+    per_group = group * (N // bn)
+    last_group_first = (tiles // per_group - 1) * per_group
+    m0, n0 = binding.gemm_tile_origin(M, N, bm, bn, group, last_group_first)
+    assert n0 == 0 and m0 == ((M // bm) // group - 1) * group * bm
