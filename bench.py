@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-context", action="store_true",
+                   help="skip the context figures (cuBLAS, warm L2, single-core oracle)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample")
     return p.parse_args(argv)
@@ -296,6 +298,53 @@ def oracle_sample(cfg, A, B, target_s: float):
                       f"{dt:.1f} s"}, rows, dt
 
 
+def oracle_single_core(cfg, A, B, rows: int = 64):
+    """The oracle on one host core over the first `rows` rows of D, with the
+    time of the whole of D extrapolated from it (a context figure)."""
+    import oracle
+
+    orc = oracle.get()
+    threads = orc.num_threads()
+    rows = min(rows, cfg.M)
+    orc.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, rows))
+        dt = time.perf_counter() - t0
+    finally:
+        orc.set_num_threads(threads)
+    flops = 2.0 * rows * cfg.N * cfg.K
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows} of D, {dt:.2f} s",
+            "extrapolated_full_s": dt * cfg.M / rows}
+
+
+def time_launches(fn, count, dev, flush=None):
+    """Mean device time (ms) of `count` launches of fn, CUDA events around each
+    launch on the current stream, optional L2 flush before each."""
+    import torch
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        if flush is not None:
+            flush.zero_()
+        fn()
+    torch.cuda.synchronize(dev)
+    evs = []
+    for _ in range(count):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    t = [a.elapsed_time(b) for a, b in evs]
+    return sum(t) / len(t)
+
+
 def run_reference(args, cfg):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -510,6 +559,29 @@ def run_ours(args, cfg):
     if world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = oracle_sample(cfg, A, B, args.cpu_seconds)
 
+    # ---- context figures, measured after the timed region ------------------------
+    context = None
+    if not args.no_context:
+        n_ctx = max(5, min(args.steps, 20))
+        if cfg.layout == "abt":
+            mm = lambda: torch.mm(dA, dB.t())  # noqa: E731
+        else:
+            mm = lambda: torch.mm(dA, dB)  # noqa: E731
+        t_mm = time_launches(mm, n_ctx, dev, flush)
+        t_warm = time_launches(lambda: gemm(dA, dB, dD), n_ctx, dev)
+        context = {
+            "torch_mm": {"value": flops / (t_mm / 1e3) / 1e12, "unit": UNIT, "ms_per_step": t_mm,
+                         "what": "torch.mm (cuBLAS) on the same device tensors, L2 flushed "
+                                 "before each launch, CUDA events"},
+            "ours_warm_l2": {"value": flops / (t_warm / 1e3) / 1e12, "unit": UNIT,
+                             "ms_per_step": t_warm,
+                             "what": "this GEMM back to back, inputs left in L2"},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            context["cpu_single_core"] = oracle_single_core(cfg, A, B)
+        if binding.gemm_device_status(clear=True) != 0:
+            raise RuntimeError("device status word set during the context runs")
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -534,6 +606,7 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "per_launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
                           "max": max(per_launch_ms)},
+        "context": context,
     }
     if clocks and clocks.get("sm_mhz"):
         line["tensor_peak_nominal"]["frac_at_run_clock"] = (

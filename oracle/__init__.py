@@ -79,11 +79,17 @@ class Oracle:
         lib.oracle_from_double.restype = ctypes.c_uint16
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         self._lib = lib
         self.path = so_path
 
     def num_threads(self) -> int:
         return int(self._lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads for later calls (the OpenMP runtime's setting; n >= 1)."""
+        self._lib.oracle_set_num_threads(int(n))
 
     def to_double(self, bits, dtype) -> np.ndarray:
         """Exact binary64 value of each 16-bit pattern."""

@@ -169,3 +169,13 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Set the number of threads later calls use (n >= 1; ignored without OpenMP).
+ * Used only to time the oracle on one core. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -90,3 +90,16 @@ def test_source_hash_ignores_comments_but_not_code():
     assert bench.strip_c_comments(code) == bench.strip_c_comments(same)
     assert bench.strip_c_comments(code) != bench.strip_c_comments(other)
     assert '"// not a comment"' in bench.strip_c_comments(code)
+
+
+def test_single_core_oracle_context_restores_threads():
+    import oracle
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.CONFIGS[0]  # 128 x 128 x 64
+    A, B = bench.make_inputs(cfg)
+    before = oracle.get().num_threads()
+    ctx = bench.oracle_single_core(cfg, A, B, rows=16)
+    assert oracle.get().num_threads() == before
+    assert ctx["cores"] == 1 and ctx["value"] > 0
+    assert ctx["extrapolated_full_s"] > 0 and "rows 0..16" in ctx["sample"]
