@@ -20,7 +20,9 @@ Distributions (element i of a row-major matrix, i = row * cols + col):
     normal  N(0, s^2): Box-Muller on draws 2i and 2i+1:
                        u1 = ((d_2i >> 11) + 1) * 2^-53,  u2 = (d_2i+1 >> 11) * 2^-53
                        v  = fp32(s * sqrt(-2 ln u1) * cos(2 pi u2))
-Then v is rounded once (nearest, ties to even) to binary16 or bfloat16.
+Then v is rounded once (nearest, ties to even) to binary16 or bfloat16, or to
+the 8-bit E4M3 / E5M2 formats (OCP 8-bit floating point; magnitudes beyond the
+largest finite value saturate to it, which the drawn values never reach).
 
 Stream 0 draws A, stream 1 draws B.  Padding columns (row stride > cols) are
 filled with a quiet NaN so that any read of padding poisons the result.
@@ -37,7 +39,41 @@ _C1 = np.uint64(0xBF58476D1CE4E5B9)
 _C2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
-NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F, "e5m2": 0x7E}
+FP8 = ("e4m3", "e5m2")
+
+
+def _fp8_positive_table(fmt: str):
+    """(values, codes) of the finite non-negative codes of an FP8 format, in
+    increasing order (the codes are monotonic in value)."""
+    if fmt == "e4m3":  # 1.4.3, bias 7, no infinities, 0x7F is NaN
+        codes = np.arange(0x7F)
+        e, f = codes >> 3, codes & 7
+        vals = np.where(e == 0, f * 2.0 ** -9, (8 + f) * np.exp2(e - 10.0))
+    elif fmt == "e5m2":  # 1.5.2, bias 15, 0x7C is inf
+        codes = np.arange(0x7C)
+        e, f = codes >> 2, codes & 3
+        vals = np.where(e == 0, f * 2.0 ** -16, (4 + f) * np.exp2(e - 17.0))
+    else:
+        raise ValueError(f"unknown FP8 format {fmt!r}")
+    return vals.astype(np.float64), codes.astype(np.uint8)
+
+
+_FP8_TABLES = {f: _fp8_positive_table(f) for f in FP8}
+
+
+def f32_to_fp8_bits(x: np.ndarray, fmt: str) -> np.ndarray:
+    """binary32 -> FP8 pattern, nearest with ties to the even code; finite
+    magnitudes above the largest finite value saturate to it."""
+    vals, codes = _FP8_TABLES[fmt]
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.minimum(np.abs(x), vals[-1])
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((codes[hi] & 1) == 0))
+    c = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    return c | np.where(np.signbit(x), np.uint8(0x80), np.uint8(0)).astype(np.uint8)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -78,6 +114,8 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 def _to_bits(v32: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype in FP8:
+        return f32_to_fp8_bits(v32, dtype)
     if dtype == "f16":
         return v32.astype(np.float16).view(np.uint16)
     if dtype == "bf16":
@@ -103,12 +141,13 @@ def values_f32(seed: int, stream: int, start: int, count: int, dist: str,
 
 def bits(seed: int, stream: int, count: int, dtype: str, dist: str,
          sigma: float = 0.02) -> np.ndarray:
-    """First `count` elements of a stream as 16-bit patterns (uint16).
+    """First `count` elements of a stream as storage patterns (uint16, or
+    uint8 for the FP8 formats).
 
     Chunks are independent (the generator is counter-based), so they are drawn
     on a thread pool; the result does not depend on the chunking.
     """
-    out = np.empty(count, dtype=np.uint16)
+    out = np.empty(count, dtype=np.uint8 if dtype in FP8 else np.uint16)
 
     def fill(s):
         n = min(_CHUNK, count - s)
@@ -137,14 +176,17 @@ def matrix(seed: int, stream: int, rows: int, cols: int, dtype: str, dist: str,
     flat = bits(seed, stream, rows * cols, dtype, dist, sigma)
     if ld == cols:
         return flat.reshape(rows, cols)
-    buf = np.full((rows, ld), NAN_BITS[dtype], dtype=np.uint16)
+    buf = np.full((rows, ld), NAN_BITS[dtype], dtype=flat.dtype)
     buf[:, :cols] = flat.reshape(rows, cols)
     return buf[:, :cols]
 
 
 def operands(M: int, N: int, K: int, layout: str, dtype: str, dist: str, seed: int,
              lda: int | None = None, ldb: int | None = None):
-    """(A, B) for D = A.Bt (layout 'abt', B is N x K) or D = A.B ('ab', B is K x N)."""
+    """(A, B) for D = A.Bt (layout 'abt', B is N x K) or D = A.B ('ab', B is K x N).
+    FP8 operands ('e4m3', 'e5m2') exist for the A.Bt layout only."""
+    if dtype in FP8 and layout != "abt":
+        raise ValueError("FP8 operands are K-major: layout 'abt' only")
     A = matrix(seed, 0, M, K, dtype, dist, lda)
     if layout == "abt":
         B = matrix(seed, 1, N, K, dtype, dist, ldb)

@@ -81,6 +81,13 @@ class Oracle:
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         lib.oracle_set_num_threads.restype = None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_fp8_to_double.argtypes = [ctypes.c_uint8, ctypes.c_int]
+        lib.oracle_fp8_to_double.restype = ctypes.c_double
+        lib.oracle_gemm_fp8.argtypes = [u8p, u8p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_double, i64, i64, i64, i64,
+                                        u16p, f64p, i64]
+        lib.oracle_gemm_fp8.restype = None
         self._lib = lib
         self.path = so_path
 
@@ -157,6 +164,68 @@ class Oracle:
         return (out16, out64) if want_f64 else out16
 
 
+def _fp8(fmt) -> int:
+    if fmt in ("e4m3", 0):
+        return 0
+    if fmt in ("e5m2", 1):
+        return 1
+    raise ValueError(f"unknown FP8 format {fmt!r}")
+
+
+def _fp8_methods():
+    def fp8_to_double(self, bits, fmt) -> np.ndarray:
+        """Exact binary64 value of each FP8 pattern (E4M3 or E5M2)."""
+        f = _fp8(fmt)
+        b = np.asarray(bits, dtype=np.uint8)
+        return np.array([self._lib.oracle_fp8_to_double(int(v), f) for v in b.ravel()],
+                        dtype=np.float64).reshape(b.shape)
+
+    def gemm_fp8(self, A, B, *, fmt="e4m3", out_dtype="bf16", alpha=1.0, rows=None, cols=None,
+                 want_f64: bool = False):
+        """Oracle FP8 GEMM: D = round(alpha * A . Bt), A (M, K) and B (N, K) uint8
+        FP8 patterns (K-major, unit inner stride), D as 16-bit patterns of
+        ``out_dtype``.  ``alpha`` is used at its binary32 value, as the GPU does."""
+        f = _fp8(fmt)
+        d = _dt(out_dtype)
+        A = np.asarray(A)
+        B = np.asarray(B)
+        if A.dtype != np.uint8 or B.dtype != np.uint8:
+            raise TypeError("oracle.gemm_fp8 takes uint8 FP8 patterns")
+        if A.ndim != 2 or B.ndim != 2:
+            raise ValueError("operands must be 2-D")
+        if A.size and A.strides[1] != 1:
+            A = np.ascontiguousarray(A)
+        if B.size and B.strides[1] != 1:
+            B = np.ascontiguousarray(B)
+        M, K = A.shape
+        N, Kb = B.shape
+        if Kb != K:
+            raise ValueError(f"K mismatch: {K} vs {Kb}")
+        i0, i1 = rows if rows is not None else (0, M)
+        j0, j1 = cols if cols is not None else (0, N)
+        if not (0 <= i0 <= i1 <= M and 0 <= j0 <= j1 <= N):
+            raise ValueError("rows/cols out of range")
+        lda = A.strides[0] if A.shape[0] > 1 else max(A.shape[1], 1)
+        ldb = B.strides[0] if B.shape[0] > 1 else max(B.shape[1], 1)
+        out16 = np.zeros((i1 - i0, j1 - j0), dtype=np.uint16)
+        out64 = np.zeros((i1 - i0, j1 - j0), dtype=np.float64) if want_f64 else None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        a32 = float(np.float32(alpha))
+        if out16.size:
+            self._lib.oracle_gemm_fp8(A.ctypes.data_as(u8p) if A.size else None,
+                                      B.ctypes.data_as(u8p) if B.size else None,
+                                      M, N, K, lda, ldb, f, d, a32, i0, i1, j0, j1,
+                                      out16.ctypes.data_as(u16p),
+                                      out64.ctypes.data_as(f64p) if want_f64 else None, j1 - j0)
+        return (out16, out64) if want_f64 else out16
+
+    return fp8_to_double, gemm_fp8
+
+
+Oracle.fp8_to_double, Oracle.gemm_fp8 = _fp8_methods()
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -183,3 +252,11 @@ def from_double(x, dtype):
 
 def num_threads() -> int:
     return get().num_threads()
+
+
+def gemm_fp8(A, B, **kw):
+    return get().gemm_fp8(A, B, **kw)
+
+
+def fp8_to_double(bits, fmt):
+    return get().fp8_to_double(bits, fmt)

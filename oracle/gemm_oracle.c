@@ -29,6 +29,9 @@
  * definition (the upper half of an IEEE binary32: 1 sign, 8 exponent bits with
  * bias 127, 7 fraction bits).
  *
+ * The FP8 variant (oracle_gemm_fp8, below) follows the same rule from exact
+ * E4M3 / E5M2 inputs, with one FP32 scale applied to the sum.
+ *
  * Parity pins (tests/test_oracle.py): hand-computed products, identity and
  * permutation operands, the transpose invariant (A.Bt)t == B.At, closed forms
  * for all-ones operands, exact small-integer products, agreement of the two
@@ -157,6 +160,64 @@ void oracle_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int
             int64_t o = (i - i0) * ldo + (j - j0);
             if (out_f64) out_f64[o] = acc;
             if (out16) out16[o] = oracle_from_double(acc, dtype);
+        }
+    }
+}
+
+/* ---- FP8 inputs ------------------------------------------------------------
+ *
+ * The 8-bit formats, written from the OCP 8-bit floating point specification
+ * ("OFP8"), the encodings the tcgen05 kind::f8f6f4 MMA consumes:
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; subnormals at
+ *         exponent field 0 (f/8 * 2^-6); NO infinities; S.1111.111 is NaN, so
+ *         exponent field 15 with fraction 0..6 is an ordinary normal number
+ *         (largest finite 1.75 * 2^8 = 448).
+ *   E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits, IEEE 754 style:
+ *         subnormals f/4 * 2^-14, exponent field 31 is inf (f = 0) or NaN.
+ */
+#define ORACLE_E4M3 0
+#define ORACLE_E5M2 1
+
+double oracle_fp8_to_double(uint8_t b, int fmt) {
+    const int sign = (b >> 7) & 1;
+    double v;
+    if (fmt == ORACLE_E4M3) {
+        const int e = (b >> 3) & 0xf, f = b & 7;
+        if (e == 15 && f == 7) return NAN;
+        v = (e == 0) ? ldexp((double)f, -9) : ldexp((double)(8 + f), e - 10);
+    } else {
+        const int e = (b >> 2) & 0x1f, f = b & 3;
+        if (e == 31) return f ? NAN : (sign ? -INFINITY : INFINITY);
+        v = (e == 0) ? ldexp((double)f, -16) : ldexp((double)(4 + f), e - 17);
+    }
+    return sign ? -v : v;
+}
+
+/* D[i,j] = round_RNE( alpha * sum_{k<K} A[i,k] * B[j,k] ), A (M x K) and B
+ * (N x K) both K-major ("Choosing schedules and instructions for a backend",
+ * the instruction table: fp8e4m3 operands are K-major only).  The products of
+ * two 8-bit values are exact in binary64 and the sum runs over k in order;
+ * alpha (one scale for the whole product: "TIRx: A Unified Tile Primitive ML
+ * Compiler", kernel performance, "scale factors that adjust their numerical
+ * range", with one group spanning each tensor) multiplies the sum once, and
+ * the result is rounded once to the 16-bit output type. */
+void oracle_gemm_fp8(const uint8_t* A, const uint8_t* B, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int in_fmt, int out_dtype, double alpha,
+                     int64_t i0, int64_t i1, int64_t j0, int64_t j1,
+                     uint16_t* out16, double* out_f64, int64_t ldo) {
+    (void)M;
+    (void)N;
+    double dec[256];
+    for (int c = 0; c < 256; ++c) dec[c] = oracle_fp8_to_double((uint8_t)c, in_fmt);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = i0; i < i1; ++i) {
+        for (int64_t j = j0; j < j1; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += dec[A[i * lda + k]] * dec[B[j * ldb + k]];
+            const double d = alpha * acc;
+            int64_t o = (i - i0) * ldo + (j - j0);
+            if (out_f64) out_f64[o] = d;
+            if (out16) out16[o] = oracle_from_double(d, out_dtype);
         }
     }
 }

@@ -205,6 +205,87 @@ def pin_bf16_rounding_matches_torch_on_binary32_values(orc):
     assert np.array_equal(got, ref)
 
 
+# ---- FP8 (E4M3 / E5M2) inputs -------------------------------------------------
+
+def fp8_torch_values(codes, fmt):
+    """FP8 patterns -> float64 through torch's own float8 types (not the oracle)."""
+    t = torch.from_numpy(np.asarray(codes, dtype=np.uint8).copy())
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return t.view(dt).to(torch.float64).numpy()
+
+
+def pin_fp8_decode_matches_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt in ("e4m3", "e5m2"):
+        got = orc.fp8_to_double(codes, fmt)
+        ref = fp8_torch_values(codes, fmt)
+        assert np.array_equal(np.isnan(got), np.isnan(ref)), fmt
+        ok = ~np.isnan(ref)
+        assert np.array_equal(got[ok], ref[ok]), fmt
+
+
+def pin_fp8_decode_hand_values(orc):
+    # OCP 8-bit floating point: E4M3 bias 7 (no infinities, S.1111.111 = NaN),
+    # E5M2 bias 15 (IEEE style); values worked out by hand.
+    e4m3 = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5,
+            0x38: 1.0, 0x3F: 1.875, 0x40: 2.0, 0x48: 4.0, 0x77: 240.0, 0x7E: 448.0,
+            0xB8: -1.0, 0xFE: -448.0}
+    e5m2 = {0x00: 0.0, 0x01: 2.0 ** -16, 0x03: 3 * 2.0 ** -16, 0x04: 2.0 ** -14,
+            0x3C: 1.0, 0x3D: 1.25, 0x40: 2.0, 0x7B: 57344.0, 0xBC: -1.0}
+    for fmt, table in (("e4m3", e4m3), ("e5m2", e5m2)):
+        codes = np.array(list(table), dtype=np.uint8)
+        assert np.array_equal(orc.fp8_to_double(codes, fmt), np.array(list(table.values()))), fmt
+    assert np.isnan(orc.fp8_to_double(np.array([0x7F, 0xFF], np.uint8), "e4m3")).all()
+    assert np.isinf(orc.fp8_to_double(np.array([0x7C], np.uint8), "e5m2")).all()
+    assert np.isnan(orc.fp8_to_double(np.array([0x7D, 0x7E, 0x7F], np.uint8), "e5m2")).all()
+
+
+def pin_fp8_hand_product(orc):
+    # A = [1, 2, -0.5], B rows [4, 0.25, 2] and [1, 1, 1]:  D = [3.5, 2.5]
+    A = np.array([[0x38, 0x40, 0xB0]], dtype=np.uint8)
+    B = np.array([[0x48, 0x28, 0x40], [0x38, 0x38, 0x38]], dtype=np.uint8)
+    _, d64 = orc.gemm_fp8(A, B, fmt="e4m3", out_dtype="f16", want_f64=True)
+    assert np.array_equal(d64, [[3.5, 2.5]])
+    d16 = orc.gemm_fp8(A, B, fmt="e4m3", out_dtype="bf16", alpha=2.0)
+    assert np.array_equal(dec(d16, "bf16"), [[7.0, 5.0]])
+
+
+def pin_fp8_gemm_matches_16bit_path(orc):
+    # Every E4M3 and E5M2 value is exact in binary16, so the FP8 GEMM must equal
+    # the 16-bit GEMM of the same values (converted here by torch and numpy).
+    for fmt in ("e4m3", "e5m2"):
+        A, B = inputs.operands(19, 23, 77, "abt", fmt, "uniform", 5)
+        A16 = fp8_torch_values(A, fmt).astype(np.float16).view(np.uint16)
+        B16 = fp8_torch_values(B, fmt).astype(np.float16).view(np.uint16)
+        got, g64 = orc.gemm_fp8(A, B, fmt=fmt, out_dtype="f16", want_f64=True)
+        ref, r64 = orc.gemm(A16, B16, layout="abt", dtype="f16", want_f64=True)
+        assert np.array_equal(g64, r64) and np.array_equal(got, ref), fmt
+
+
+def pin_fp8_against_torch_float64(orc):
+    for fmt in ("e4m3", "e5m2"):
+        A, B = inputs.operands(13, 9, 150, "abt", fmt, "normal", 6)
+        a, b = fp8_torch_values(A, fmt), fp8_torch_values(B, fmt)
+        ref = (torch.from_numpy(a) @ torch.from_numpy(b).T).numpy() * np.float64(np.float32(0.375))
+        _, got = orc.gemm_fp8(A, B, fmt=fmt, out_dtype="bf16", alpha=0.375, want_f64=True)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-300), fmt
+
+
+def pin_fp8_alpha_applied_once(orc):
+    A, B = inputs.operands(7, 11, 64, "abt", "e4m3", "uniform", 8)
+    _, one = orc.gemm_fp8(A, B, fmt="e4m3", out_dtype="bf16", want_f64=True)
+    for alpha in (0.5, 3.0, 0.1):
+        _, got = orc.gemm_fp8(A, B, fmt="e4m3", out_dtype="bf16", alpha=alpha, want_f64=True)
+        assert np.array_equal(got, np.float64(np.float32(alpha)) * one), alpha
+
+
+def pin_fp8_transpose_invariant(orc):
+    A, B = inputs.operands(12, 17, 40, "abt", "e5m2", "uniform", 9)
+    d1 = orc.gemm_fp8(A, B, fmt="e5m2", out_dtype="bf16")
+    d2 = orc.gemm_fp8(B, A, fmt="e5m2", out_dtype="bf16")
+    assert np.array_equal(d1.T, d2)
+
+
 PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 

@@ -31,6 +31,16 @@ MUTANTS = {
                             "g_decode[dtype == ORACLE_BF16 ? ORACLE_F16 : ORACLE_BF16]"),
     "bf16_read_as_f16": ("return dtype == ORACLE_BF16 ? bf16_bits_to_double(bits) : f16_bits_to_double(bits);",
                          "return f16_bits_to_double(bits);"),
+    "fp8_e4m3_bias": ("ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 9)"),
+    "fp8_e4m3_ieee_nan_rule": ("if (e == 15 && f == 7) return NAN;", "if (e == 15) return NAN;"),
+    "fp8_e5m2_subnormal": ("ldexp((double)f, -16)", "ldexp((double)f, -15)"),
+    "fp8_alpha_dropped": ("const double d = alpha * acc;", "const double d = acc;"),
+    "fp8_b_k_reversed": ("acc += dec[A[i * lda + k]] * dec[B[j * ldb + k]];",
+                         "acc += dec[A[i * lda + k]] * dec[B[j * ldb + (K - 1 - k)]];"),
+    "fp8_sign": ("acc += dec[A[i * lda + k]] * dec[B[j * ldb + k]];",
+                 "acc -= dec[A[i * lda + k]] * dec[B[j * ldb + k]];"),
+    "fp8_formats_swapped": ("dec[c] = oracle_fp8_to_double((uint8_t)c, in_fmt);",
+                            "dec[c] = oracle_fp8_to_double((uint8_t)c, 1 - in_fmt);"),
 }
 
 
