@@ -12,7 +12,7 @@ import os
 
 from . import build as _build
 
-GEMM_F16, GEMM_BF16 = 0, 1
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3
 LAYOUT_ABT, LAYOUT_AB = 0, 1
 
 STATUS_NAMES = {
@@ -32,7 +32,8 @@ STATUS_NAMES = {
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_workspace_size",
            "gemm_run_no_alloc", "gemm_status_string", "gemm_plan", "gemm_tile_origin",
-           "gemm_device_status", "gemm_selftest_wait_timeout")
+           "gemm_device_status", "gemm_selftest_wait_timeout", "gemm_fp8_abt", "gemm_fp8_run",
+           "gemm_fp8_run_workspace")
 
 
 class GemmError(RuntimeError):
@@ -85,6 +86,15 @@ def load(path: str | None = None):
     lib.gemm_run_no_alloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
                                       ctypes.POINTER(GemmOptions), vp]
     lib.gemm_run_no_alloc.restype = c_int
+    f32 = ctypes.c_float
+    lib.gemm_fp8_abt.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int, f32, vp]
+    lib.gemm_fp8_abt.restype = c_int
+    lib.gemm_fp8_run.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int, f32,
+                                 ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_fp8_run.restype = c_int
+    lib.gemm_fp8_run_workspace.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                           f32, ctypes.POINTER(GemmOptions), vp, ctypes.c_size_t, vp]
+    lib.gemm_fp8_run_workspace.restype = c_int
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     ip = ctypes.POINTER(c_int)
@@ -141,7 +151,7 @@ def _dtype_code(t) -> int:
     raise GemmError(-2, f"tensor dtype {t.dtype}")
 
 
-def _ld(t) -> int:
+def _ld(t, multiple: int = 8) -> int:
     # Row stride in elements of a row-major 2-D view (inner stride must be 1).
     if t.dim() != 2:
         raise GemmError(-3, "operands must be 2-D")
@@ -150,7 +160,26 @@ def _ld(t) -> int:
     if t.shape[0] > 1:
         return int(t.stride(0))
     # one row (or none): the stride is never used; any legal value will do
-    return max(8, (int(t.shape[1]) + 7) // 8 * 8)
+    m = multiple
+    return max(m, (int(t.shape[1]) + m - 1) // m * m)
+
+
+def _fp8_code(t, fmt) -> int:
+    """GEMM_E4M3 / GEMM_E5M2 for a torch float8 tensor, or for a uint8 tensor of
+    FP8 bit patterns with `fmt` = "e4m3" / "e5m2"."""
+    import torch
+
+    by_dtype = {getattr(torch, "float8_e4m3fn", None): GEMM_E4M3,
+                getattr(torch, "float8_e5m2", None): GEMM_E5M2}
+    if t.dtype in by_dtype and t.dtype is not None:
+        code = by_dtype[t.dtype]
+        if fmt is not None and {"e4m3": GEMM_E4M3, "e5m2": GEMM_E5M2}.get(fmt) != code:
+            raise GemmError(-2, f"fmt {fmt!r} does not match tensor dtype {t.dtype}")
+        return code
+    if t.dtype == torch.uint8 and fmt in ("e4m3", "e5m2"):
+        return GEMM_E4M3 if fmt == "e4m3" else GEMM_E5M2
+    raise GemmError(-2, f"FP8 operands: float8 tensors, or uint8 with fmt='e4m3'/'e5m2' "
+                        f"(got {t.dtype}, fmt={fmt!r})")
 
 
 def _stream_handle(stream, device) -> int:
@@ -229,6 +258,55 @@ def gemm_run(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=Non
                                 _ld(B), _ld(D), dt, int(layout), opts, ws_ptr, ws_bytes, sh)
     if st != 0:
         raise GemmError(st, "gemm_run_workspace")
+    return D
+
+
+def gemm_fp8(A, B, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0, options=None,
+             stream=None, workspace="auto"):
+    """D[M, N] = alpha * A[M, K] . B[N, K]^T with FP8 A and B (both E4M3 or both
+    E5M2: torch float8 tensors, or uint8 bit patterns with `fmt`), FP32
+    accumulation and a 16-bit D (`out_dtype`, default bfloat16)."""
+    import torch
+
+    if A.device.type != "cuda" or B.device.type != "cuda":
+        raise GemmError(-1, "operands must be CUDA tensors")
+    code = _fp8_code(A, fmt)
+    if _fp8_code(B, fmt) != code:
+        raise GemmError(-2, "A and B must share an FP8 format")
+    M, K = A.shape
+    N, Kb = B.shape
+    if Kb != K:
+        raise GemmError(-3, f"K mismatch ({K} vs {Kb})")
+    odt = out_dtype if out_dtype is not None else (D.dtype if D is not None else torch.bfloat16)
+    if D is None:
+        D = torch.empty((M, N), dtype=odt, device=A.device)
+    elif D.dtype != odt or tuple(D.shape) != (M, N):
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    out_code = _dtype_code(D)
+    lib = load()
+    sh = _stream_handle(stream, A.device)
+    opts = _options(options)
+    ws_ptr, ws_bytes = None, 0
+    if isinstance(workspace, str) and workspace == "auto":
+        dev_index = A.device.index if A.device.index is not None else torch.cuda.current_device()
+        key = (M, N, K, code, LAYOUT_ABT, _options_key(options), dev_index)
+        need = _ws_need_cache.get(key)
+        if need is None:
+            n = ctypes.c_size_t()
+            st = lib.gemm_workspace_size(M, N, K, code, LAYOUT_ABT, opts, ctypes.byref(n))
+            if st != 0:
+                raise GemmError(st, "gemm_workspace_size")
+            need = _ws_need_cache[key] = n.value
+        if need:
+            ws = _workspace(A.device, sh, need)
+            ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
+    elif workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.gemm_fp8_run_workspace(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                    _ld(A, 16), _ld(B, 16), _ld(D), code, out_code, float(alpha),
+                                    opts, ws_ptr, ws_bytes, sh)
+    if st != 0:
+        raise GemmError(st, "gemm_fp8_run_workspace")
     return D
 
 

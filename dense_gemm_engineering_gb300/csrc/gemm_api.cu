@@ -42,16 +42,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // Row-major 2-D tensor of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row stride `ld` elements; boxes of box_inner x box_outer,
 // 128-byte swizzle, zero fill outside the tensor.
-bool encode_2d(CUtensorMap* map, const void* ptr, int dtype, uint64_t inner, uint64_t outer,
+// `fmt`: GEMM_F16 / GEMM_BF16 (2-byte elements) or GEMM_E4M3 / GEMM_E5M2
+// (1-byte elements, moved as raw bytes).
+bool encode_2d(CUtensorMap* map, const void* ptr, int fmt, uint64_t inner, uint64_t outer,
                uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    const bool byte = (fmt == GEMM_E4M3 || fmt == GEMM_E5M2);
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {ld * 2u};
+    const cuuint64_t strides[1] = {ld * (byte ? 1u : 2u)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : fmt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     return enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -90,9 +94,26 @@ int current_device(DeviceInfo* out) {
 
 // ---- kernel variants -----------------------------------------------------------
 
+// Opt a variant in to its dynamic shared memory size on the current device
+// (once per device; every launch and occupancy query goes through here).
+template <class C>
+cudaError_t ensure_smem_attribute() {
+    static std::atomic<uint64_t> done{0};  // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load() & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(gemm_tcgen05_kernel<C>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e == cudaSuccess && bit) done.fetch_or(bit);
+    return e;
+}
+
 template <class C>
 void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                     const GemmArgs& args, int clusters, cudaStream_t stream, cudaError_t* err) {
+    if ((*err = ensure_smem_attribute<C>()) != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(clusters * C::CLUSTER), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
@@ -112,9 +133,7 @@ void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
 template <class C>
 int query_max_clusters(int dev, int sm_count) {
     const void* fn = reinterpret_cast<const void*>(gemm_tcgen05_kernel<C>);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-        return -1;
+    if (ensure_smem_attribute<C>() != cudaSuccess) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(C::CLUSTER * (sm_count / C::CLUSTER)), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
@@ -146,8 +165,8 @@ struct Stages {
     static constexpr int value = stages_for(CG, BN, CONS);
 };
 
-template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1>
-using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC>;
+template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1, int F8 = 0>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC, F8>;
 
 struct Plan {
     int cg, bm, bn, stages;
@@ -220,27 +239,28 @@ std::atomic<uint32_t> g_epoch{0};
 
 template <class C>
 int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-             int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
-             cudaStream_t stream) {
+             int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha,
+             void* workspace, cudaStream_t stream) {
     CUtensorMap ma, mb, md;
-    if (!encode_2d(&ma, A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda), kBlockK, C::A_BOX_ROWS))
+    if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_BOX_ROWS))
         return GEMM_ERR_CUDA;
     if constexpr (!C::B_MN) {
-        if (!encode_2d(&mb, B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb), kBlockK, C::B_ROWS))
+        if (!encode_2d(&mb, B, in_fmt, uint64_t(K), uint64_t(N), uint64_t(ldb), C::BK, C::B_ROWS))
             return GEMM_ERR_CUDA;
     } else {
-        if (!encode_2d(&mb, B, dtype, uint64_t(N), uint64_t(K), uint64_t(ldb), 64, kBlockK))
+        if (!encode_2d(&mb, B, in_fmt, uint64_t(N), uint64_t(K), uint64_t(ldb), 64, C::BK))
             return GEMM_ERR_CUDA;
     }
-    if (!encode_2d(&md, D, dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
+    if (!encode_2d(&md, D, out_dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
         return GEMM_ERR_CUDA;
     GemmArgs args;
+    args.alpha = alpha;
     args.d = static_cast<uint16_t*>(D);
     args.ldd = ldd;
     args.M = int32_t(M);
     args.N = int32_t(N);
     args.K = int32_t(K);
-    args.k_blocks = int32_t((K + kBlockK - 1) / kBlockK);
+    args.k_blocks = int32_t((K + C::BK - 1) / C::BK);
     args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
     args.grid.n_tiles = int32_t((N + C::BN_CLUSTER - 1) / C::BN_CLUSTER);
     args.grid.group = p.group;
@@ -259,9 +279,27 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Dispatch on (cta_group, block_n, layout, dtype) to one template instance.
+// Dispatch on (cta_group, block_n, layout, dtype, FP8 input) to one template
+// instance.  `bf16` is the output type (and the input type when f8 == 0).
 template <template <class> class Fn, class... Ts>
-int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, Ts&&... ts) {
+int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, int f8, Ts&&... ts) {
+    if (f8 != 0) {
+        // FP8 inputs: K-major B, one consumer, no multicast; 2-CTA 256 / 224-wide
+        // and 1-CTA 256-wide tiles.
+        if (b_mn || cons != 1 || mc != 1) return GEMM_ERR_OPTION;
+#define GB300_CASE8(CG_, BN_, F8_, BF_)                                                  \
+    if (cg == CG_ && bn == BN_ && f8 == F8_ && bf16 == BF_)                              \
+        return Fn<Cfg<CG_, BN_, false, BF_, 1, 1, F8_>>::call(std::forward<Ts>(ts)...);
+#define GB300_CASES8(CG_, BN_) \
+    GB300_CASE8(CG_, BN_, 1, false) GB300_CASE8(CG_, BN_, 1, true) \
+    GB300_CASE8(CG_, BN_, 2, false) GB300_CASE8(CG_, BN_, 2, true)
+        GB300_CASES8(2, 256)
+        GB300_CASES8(2, 224)
+        GB300_CASES8(1, 256)
+#undef GB300_CASES8
+#undef GB300_CASE8
+        return GEMM_ERR_OPTION;
+    }
 #define GB300_CASEMC(MN_, BF_)                                                           \
     if (mc == 2 && cons == 1 && cg == 2 && bn == 256 && b_mn == MN_ && bf16 == BF_)      \
         return Fn<Cfg<2, 256, MN_, BF_, 1, 2>>::call(std::forward<Ts>(ts)...);
@@ -319,14 +357,21 @@ struct QueryFn {
 template <class C>
 struct RunFn {
     static int call(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N,
-                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype, void* workspace,
-                    cudaStream_t stream) {
-        return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, dtype, workspace, stream);
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype,
+                    float alpha, void* workspace, cudaStream_t stream) {
+        return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace,
+                           stream);
     }
 };
 
+bool is_fp8(int fmt) { return fmt == GEMM_E4M3 || fmt == GEMM_E5M2; }
+int f8_code(int fmt) { return fmt == GEMM_E4M3 ? 1 : fmt == GEMM_E5M2 ? 2 : 0; }
+
+// `dtype` is the input format: GEMM_F16 / GEMM_BF16, or (where FP8 inputs are
+// accepted) GEMM_E4M3 / GEMM_E5M2, which take the K-major A.Bt layout only.
 int check_sizes(int64_t M, int64_t N, int64_t K, int dtype, int b_layout) {
-    if (dtype != GEMM_F16 && dtype != GEMM_BF16) return GEMM_ERR_DTYPE;
+    if (dtype != GEMM_F16 && dtype != GEMM_BF16 && !is_fp8(dtype)) return GEMM_ERR_DTYPE;
+    if (is_fp8(dtype) && b_layout != 0) return GEMM_ERR_OPTION;
     if (b_layout != 0 && b_layout != 1) return GEMM_ERR_OPTION;
     if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return GEMM_ERR_SHAPE;
@@ -348,8 +393,8 @@ int check_options(const gemm_options_t* o) {
 
 int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
     int n = 0;
-    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, 1, dev, sm_count, &n) !=
-        GEMM_OK)
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, 1, f8_code(dtype), dev,
+                          sm_count, &n) != GEMM_OK)
         return 0;
     return n;
 }
@@ -404,6 +449,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     p->cons = (o && o->consumers) ? o->consumers : 1;
     if (p->mc == 2 && (p->cg != 2 || p->cons != 1 || (o && o->block_n && o->block_n != 256)))
         return GEMM_ERR_OPTION;
+    if (is_fp8(dtype) && (p->mc != 1 || p->cons != 1)) return GEMM_ERR_OPTION;
     p->bm = 128 * p->cg * p->cons;
     if (p->cons == 2) {
         // Two consumers: 2-CTA clusters, 256-wide tiles only.
@@ -425,24 +471,25 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
     if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
     int max_clusters = 0;
-    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, p->mc, dev,
-                           di.sm_count, &max_clusters);
+    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, p->mc,
+                           f8_code(dtype), dev, di.sm_count, &max_clusters);
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
     p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
     p->stages = stages_for(p->cg, p->bn, p->cons);
-    p->k_blocks = (K + kBlockK - 1) / kBlockK;
+    const int bk = is_fp8(dtype) ? kBlockK8 : kBlockK;
+    p->k_blocks = (K + bk - 1) / bk;
     plan_split(p, o ? o->tail_split : 0, have_workspace);
     return GEMM_OK;
 }
 
-bool overlaps(const void* a, int64_t rows_a, int64_t cols_a, int64_t ld_a, const void* b,
-              int64_t rows_b, int64_t cols_b, int64_t ld_b) {
+bool overlaps(const void* a, int64_t rows_a, int64_t cols_a, int64_t ld_a, int esize_a,
+              const void* b, int64_t rows_b, int64_t cols_b, int64_t ld_b, int esize_b) {
     if (rows_a == 0 || cols_a == 0 || rows_b == 0 || cols_b == 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
-    const uintptr_t a1 = a0 + uintptr_t(((rows_a - 1) * ld_a + cols_a) * 2);
+    const uintptr_t a1 = a0 + uintptr_t(((rows_a - 1) * ld_a + cols_a) * esize_a);
     const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
-    const uintptr_t b1 = b0 + uintptr_t(((rows_b - 1) * ld_b + cols_b) * 2);
+    const uintptr_t b1 = b0 + uintptr_t(((rows_b - 1) * ld_b + cols_b) * esize_b);
     return a0 < b1 && b0 < a1;
 }
 
@@ -451,24 +498,34 @@ bool overlaps(const void* a, int64_t rows_a, int64_t cols_a, int64_t ld_a, const
 
 using namespace gb300;
 
-extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N,
-                                  int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
-                                  int b_layout, const gemm_options_t* opts, void* workspace,
-                                  size_t workspace_bytes, cudaStream_t stream) {
-    int st = check_sizes(M, N, K, dtype, b_layout);
+namespace gb300 {
+namespace {
+
+// Shared body of the 16-bit and FP8 entry points.  in_fmt: GEMM_F16 /
+// GEMM_BF16 (then out_dtype == in_fmt) or GEMM_E4M3 / GEMM_E5M2 (A.Bt only).
+int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+             int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha, int b_layout,
+             const gemm_options_t* opts, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream) {
+    int st = check_sizes(M, N, K, in_fmt, b_layout);
     if (st != GEMM_OK) return st;
+    if (out_dtype != GEMM_F16 && out_dtype != GEMM_BF16) return GEMM_ERR_DTYPE;
     if ((st = check_options(opts)) != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
+    const int esize = is_fp8(in_fmt) ? 1 : 2;
     const int64_t b_rows = b_layout == 0 ? N : K;
     const int64_t b_cols = b_layout == 0 ? K : N;
     if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
     if (ldd < N || ldd <= 0) return GEMM_ERR_SHAPE;
     if (K > 0 && (lda < K || ldb < b_cols || lda <= 0 || ldb <= 0)) return GEMM_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(D) & 15u) || (ldd & 7)) return GEMM_ERR_ALIGN;
+    // TMA: 16-byte aligned bases and row strides that are multiples of 16 bytes.
+    const int64_t ld_mask = (16 / esize) - 1;
     if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
-                  (lda & 7) || (ldb & 7)))
+                  (lda & ld_mask) || (ldb & ld_mask)))
         return GEMM_ERR_ALIGN;
-    if (K > 0 && (overlaps(D, M, N, ldd, A, M, K, lda) || overlaps(D, M, N, ldd, B, b_rows, b_cols, ldb)))
+    if (K > 0 && (overlaps(D, M, N, ldd, 2, A, M, K, lda, esize) ||
+                  overlaps(D, M, N, ldd, 2, B, b_rows, b_cols, ldb, esize)))
         return GEMM_ERR_ALIAS;
 
     if (K == 0) {
@@ -483,11 +540,48 @@ extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t
 
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GEMM_ERR_WORKSPACE;
     Plan p;
-    if ((st = make_plan(M, N, K, dtype, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
+    if ((st = make_plan(M, N, K, in_fmt, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
         return st;
     if (workspace_bytes < workspace_bytes_needed(p)) return GEMM_ERR_WORKSPACE;
-    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, dtype == GEMM_BF16, p.cons, p.mc, p, A, B, D, M, N, K,
-                           lda, ldb, ldd, dtype, workspace, stream);
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, p.mc,
+                           f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
+                           alpha, workspace, stream);
+}
+
+}  // namespace
+}  // namespace gb300
+
+extern "C" int gemm_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                  int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                                  int b_layout, const gemm_options_t* opts, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    if (is_fp8(dtype)) return GEMM_ERR_DTYPE;  // FP8 inputs: gemm_fp8_run_workspace
+    return run_impl(A, B, D, M, N, K, lda, ldb, ldd, dtype, dtype, 1.0f, b_layout, opts, workspace,
+                    workspace_bytes, stream);
+}
+
+extern "C" int gemm_fp8_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                                      int in_format, int out_dtype, float alpha,
+                                      const gemm_options_t* opts, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    if (!is_fp8(in_format)) return GEMM_ERR_DTYPE;
+    return run_impl(A, B, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha, 0, opts,
+                    workspace, workspace_bytes, stream);
+}
+
+extern "C" int gemm_fp8_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldd, int in_format, int out_dtype,
+                            float alpha, const gemm_options_t* opts, cudaStream_t stream) {
+    return gemm_fp8_run_workspace(A, B, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha,
+                                  opts, nullptr, 0, stream);
+}
+
+extern "C" int gemm_fp8_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldd, int in_format, int out_dtype,
+                            float alpha, cudaStream_t stream) {
+    return gemm_fp8_run(A, B, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha, nullptr,
+                        stream);
 }
 
 extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,

@@ -51,6 +51,7 @@ namespace gb300 {
 static __device__ uint32_t g_gemm_status;
 
 constexpr int kBlockK = 64;         // 64 x 16 bit = one 128-byte swizzle row
+constexpr int kBlockK8 = 128;       // 128 x 8 bit: the same 128-byte row for FP8 inputs
 constexpr int kNumThreads = 192;    // 6 warps: producer, MMA, 4 epilogue
 constexpr int kEpilogueWarps = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -65,7 +66,8 @@ enum : uint32_t {
     kRoleSelfTest = 5u
 };
 
-template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1>
+template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1,
+          int F8_ = 0>
 struct KernelConfig {
     static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
     // CTA pairs per cluster: 1, or 2 side by side along N that share A — each
@@ -81,11 +83,17 @@ struct KernelConfig {
     static constexpr int BN = BN_;            // tile columns (MMA N)
     static constexpr int STAGES = STAGES_;    // SMEM ring depth
     static constexpr bool B_MN = B_MN_;       // B stored K x N (D = A.B)
-    static constexpr bool BF16 = BF16_;
+    static constexpr bool BF16 = BF16_;       // output type (and input type unless F8)
+    // Input type: 0 = the 16-bit output type; 1 = FP8 E4M3, 2 = FP8 E5M2 (OCP
+    // 8-bit floating point), multiplied on tcgen05.mma kind::f8f6f4.
+    static constexpr int F8 = F8_;
+    static constexpr int BK = F8 ? kBlockK8 : kBlockK;  // K elements per ring stage
+    static constexpr int ELEM_BYTES = F8 ? 1 : 2;
+    static constexpr int MMA_K = F8 ? 32 : 16;         // K per MMA: 32 bytes either way
     static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
 
-    static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * kBlockK * 2u;  // 16 KiB per consumer
-    static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * kBlockK * 2u;
+    static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * BK * ELEM_BYTES;  // 16 KiB per consumer
+    static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * BK * ELEM_BYTES;
     static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES);
     // Two accumulators of BN FP32 columns at a power-of-two stride (the TMEM
     // allocation is a power of two of at least 32 columns).
@@ -120,15 +128,21 @@ struct KernelConfig {
     static constexpr uint32_t SMEM_USED = OFF_ABORT + 4u;
     static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024u;  // slack to align the base
 
-    // tcgen05 instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1),
-    // A/B = F16 (0) or BF16 (1) at bits 7-9 / 10-12, A K-major (bit 15 = 0),
-    // B major at bit 16, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-    // MMA shape (the same whatever the number of consumers): M = 128 rows per
-    // CTA of the group, N = BN.
+    // tcgen05 instruction descriptor (one layout for kind::f16 and
+    // kind::f8f6f4): D = F32 (bits 4-5 = 1), the A / B type at bits 7-9 /
+    // 10-12 (kind::f16: F16 = 0, BF16 = 1; kind::f8f6f4: E4M3 = 0, E5M2 = 1),
+    // A K-major (bit 15 = 0), B major at bit 16, N >> 3 at bits 17-22, M >> 4
+    // at bits 24-28.  MMA shape (the same whatever the number of consumers):
+    // M = 128 rows per CTA of the group, N = BN.
     static constexpr int MMA_M = 128 * CG;
-    static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 0u) << 7) |
-                                      ((BF16 ? 1u : 0u) << 10) | ((B_MN ? 1u : 0u) << 16) |
-                                      (uint32_t(BN >> 3) << 17) | (uint32_t(MMA_M >> 4) << 24);
+    static constexpr uint32_t AB_TYPE = F8 ? uint32_t(F8 - 1) : (BF16 ? 1u : 0u);
+    static constexpr uint32_t IDESC = (1u << 4) | (AB_TYPE << 7) | (AB_TYPE << 10) |
+                                      ((B_MN ? 1u : 0u) << 16) | (uint32_t(BN >> 3) << 17) |
+                                      (uint32_t(MMA_M >> 4) << 24);
+    static_assert(F8 == 0 || F8 == 1 || F8 == 2, "FP8 input: none, E4M3 or E5M2");
+    static_assert(!(F8 && B_MN), "FP8 operands are K-major (A.Bt only)");
+    static_assert(BK * ELEM_BYTES == 128 && MMA_K * ELEM_BYTES == 32,
+                  "a stage row is one 128-byte swizzle row; an MMA consumes 32 bytes of it");
     static_assert(MMA_M == 128 || MMA_M == 256, "tcgen05 kind::f16 M is 128 (1 CTA) or 256 (2 CTAs)");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 kind::f16 N is a multiple of 16, <= 256");
     static_assert(((IDESC >> 24) & 0x1Fu) == uint32_t(MMA_M >> 4) && ((IDESC >> 17) & 0x3Fu) == uint32_t(BN >> 3),
@@ -152,7 +166,8 @@ struct KernelConfig {
 
 struct GemmArgs {
     int32_t M, N, K;
-    int32_t k_blocks;   // ceil(K / 64)
+    int32_t k_blocks;   // ceil(K / BK)
+    float alpha;        // FP8 inputs: D = alpha * (A . Bt) (unused for 16-bit inputs)
     uint16_t* d;        // D, for the direct stores of a 32-column tail chunk
     int64_t ldd;        // row stride of D in elements
     TileGrid grid;
@@ -361,7 +376,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_TX);
                     const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
                     const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
-                    const int32_t k0 = kb * kBlockK;
+                    const int32_t k0 = kb * C::BK;
                     if constexpr (C::CG == 1) {
                         ptx::tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, a_row);
                         if constexpr (!C::B_MN) {
@@ -435,7 +450,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t b_addr = base + C::OFF_B + s * C::B_BYTES;
                     if (ptx::elect_one_sync()) {
 #pragma unroll
-                        for (int k = 0; k < kBlockK / 16; ++k) {
+                        for (int k = 0; k < C::BK / C::MMA_K; ++k) {
                             const uint64_t bd = C::B_MN
                                                     ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
                                                     : sw128_desc(b_addr + 32u * k, 16u, 1024u);
@@ -443,8 +458,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             for (int h = 0; h < C::CONS; ++h) {
                                 // consumer h: A rows 128h..128h+127 of this stage (16 KiB each)
                                 const uint64_t ad = sw128_desc(a_addr + 16384u * h + 32u * k, 16u, 1024u);
-                                ptx::mma_f16<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd, C::IDESC,
-                                                    uint32_t(kb != w.kb0 || k != 0));
+                                const uint32_t acc = uint32_t(kb != w.kb0 || k != 0);
+                                if constexpr (C::F8)
+                                    ptx::mma_f8f6f4<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd,
+                                                           C::IDESC, acc);
+                                else
+                                    ptx::mma_f16<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd,
+                                                        C::IDESC, acc);
                             }
                         }
                         // slot free (in every CTA that received data for it) once these MMAs finish
@@ -497,6 +517,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // between the warp's two buffers, or (in a cluster's last unit, when the
         // ring is idle) takes a fresh 4 KiB slice of the ring per chunk, which
         // never waits for an earlier store.
+        // FP8 inputs: D = alpha * (A . Bt), applied to the FP32 sum before the
+        // one rounding to 16 bits.
+        const float alpha = args.alpha;
+        auto scaled = [&](float x) -> float {
+            if constexpr (C::F8) return x * alpha; else return x;
+        };
         auto store_chunk = [&](const uint32_t (&bits)[64], int32_t col, int32_t row0,
                                int32_t ring_slot = -1) {
             uint32_t buf;
@@ -512,7 +538,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint32_t row_addr = buf + lane * 128u;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                auto f = [&](int i) { return __uint_as_float(bits[8 * c + i]); };
+                auto f = [&](int i) { return scaled(__uint_as_float(bits[8 * c + i])); };
                 const uint32_t p0 = ptx::pack2<C::BF16>(f(0), f(1));
                 const uint32_t p1 = ptx::pack2<C::BF16>(f(2), f(3));
                 const uint32_t p2 = ptx::pack2<C::BF16>(f(4), f(5));
@@ -530,23 +556,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // 32 FP32 values (bit patterns) of row `row` -> 16-bit -> D[row][col..col+31],
         // masked at the edges of D.
         auto store_half_chunk = [&](const uint32_t (&r)[32], int32_t col, int32_t row) {
+            auto pk = [&](uint32_t lo, uint32_t hi) {
+                return ptx::pack2<C::BF16>(scaled(__uint_as_float(lo)), scaled(__uint_as_float(hi)));
+            };
             if (row >= args.M || col >= args.N) return;
             uint16_t* dst = args.d + int64_t(row) * args.ldd + col;
             if (col + 32 <= args.N) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 q = make_uint4(
-                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1])),
-                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3])),
-                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5])),
-                        ptx::pack2<C::BF16>(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7])));
+                        pk(r[8 * c + 0], r[8 * c + 1]), pk(r[8 * c + 2], r[8 * c + 3]),
+                        pk(r[8 * c + 4], r[8 * c + 5]), pk(r[8 * c + 6], r[8 * c + 7]));
                     reinterpret_cast<uint4*>(dst)[c] = q;
                 }
             } else {
                 const int32_t n = args.N - col;
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const uint32_t p = ptx::pack2<C::BF16>(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                    const uint32_t p = pk(r[c], r[c + 1]);
                     if (c < n) dst[c] = uint16_t(p & 0xFFFFu);
                     if (c + 1 < n) dst[c + 1] = uint16_t(p >> 16);
                 }

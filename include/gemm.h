@@ -54,14 +54,21 @@
 extern "C" {
 #endif
 
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
+/* Element types.  GEMM_F16 / GEMM_BF16 are the 16-bit input and output types
+ * of gemm_abt / gemm_ab / gemm_run.  GEMM_E4M3 / GEMM_E5M2 are the 8-bit input
+ * formats of the gemm_fp8_* entry points (OCP 8-bit floating point: E4M3 =
+ * 1 sign, 4 exponent bits with bias 7, 3 fraction bits, no infinities, NaN =
+ * S.1111.111; E5M2 = 1 sign, 5 exponent bits with bias 15, 2 fraction bits,
+ * IEEE-style inf/NaN); gemm_plan and gemm_workspace_size accept them as
+ * `dtype` to describe an FP8 call. */
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2, GEMM_E5M2 = 3 } gemm_dtype_t;
 
 enum {
     GEMM_OK = 0,
     GEMM_ERR_NULL = -1,    /* a null pointer with a non-empty extent           */
-    GEMM_ERR_DTYPE = -2,   /* dtype is not GEMM_F16 / GEMM_BF16                 */
+    GEMM_ERR_DTYPE = -2,   /* an element type the entry point does not take     */
     GEMM_ERR_SHAPE = -3,   /* negative or too-large size, or ld < row length   */
-    GEMM_ERR_ALIGN = -4,   /* pointer not 16-B aligned or ld not a multiple of 8 */
+    GEMM_ERR_ALIGN = -4,   /* pointer not 16-B aligned or ld*elem not 16-B multiple */
     GEMM_ERR_ALIAS = -5,   /* D overlaps A or B                                 */
     GEMM_ERR_CUDA = -6,    /* a CUDA runtime or driver call failed              */
     GEMM_ERR_DEVICE = -7,  /* the current device is not an sm_103 GPU           */
@@ -153,6 +160,40 @@ int gemm_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t
                        int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
                        const gemm_options_t* opts, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/*
+ * FP8 GEMM: D[M x N] = alpha * A[M x K] . B[N x K]^T, A and B FP8 (in_format
+ * GEMM_E4M3 or GEMM_E5M2, both operands in the same format), D 16-bit
+ * (out_dtype GEMM_F16 or GEMM_BF16), all row-major with ld in elements.
+ *
+ * The operation is the FP8 GEMM of "TIRx: A Unified Tile Primitive ML
+ * Compiler" (kernel performance: FP8 matrix multiplication with scale
+ * factors that adjust the values' range), here with ONE scale for the whole
+ * product (alpha, e.g. scale_A * scale_B of per-tensor scaling); the operands
+ * are K-major as "Choosing schedules and instructions for a backend"
+ * requires of fp8e4m3 (instruction table).  Products accumulate in FP32 in
+ * tensor memory (tcgen05.mma kind::f8f6f4); alpha multiplies the FP32 sum,
+ * which is then rounded once (nearest even) to out_dtype.
+ *
+ * Arguments and errors as gemm_run, except: A and B are byte arrays, so lda
+ * and ldb must be multiples of 16 (TMA row strides are 16-byte multiples;
+ * GEMM_ERR_ALIGN otherwise); ldd a multiple of 8.  Options: cta_group,
+ * block_n (0, 256, or 224 with 2-CTA tiles), raster_group, max_clusters and
+ * tail_split as for gemm_run; consumers and multicast must be 0 or 1
+ * (GEMM_ERR_OPTION otherwise).  A 16-bit in_format gives GEMM_ERR_DTYPE.
+ * K = 0 writes zeros; M = 0 or N = 0 does nothing.  No library allocation;
+ * gemm_fp8_run_workspace takes a workspace exactly as gemm_run_workspace.
+ */
+int gemm_fp8_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldd, int in_format, int out_dtype,
+                 float alpha, cudaStream_t stream);
+int gemm_fp8_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldd, int in_format, int out_dtype,
+                 float alpha, const gemm_options_t* opts, cudaStream_t stream);
+int gemm_fp8_run_workspace(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int in_format,
+                           int out_dtype, float alpha, const gemm_options_t* opts,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Bytes of workspace gemm_run_workspace needs for these sizes and options on

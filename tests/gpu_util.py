@@ -65,7 +65,7 @@ def check_close(got_bits, ref_bits, dtype, what="", ref_f64=None):
 
 
 def sample_tiles(M, N, K, block_m, block_n, group, num_clusters, stages, tile_origin,
-                 seed=0, extra_random=16):
+                 seed=0, extra_random=16, block_k=64):
     """Seeded sample of whole output tiles that covers every value of
     (cluster, iteration, ring stage at tile start, ring phase at tile start,
     TMEM accumulator buffer) at least once, plus `extra_random` random tiles and
@@ -77,7 +77,7 @@ def sample_tiles(M, N, K, block_m, block_n, group, num_clusters, stages, tile_or
     m_tiles = -(-M // block_m)
     n_tiles = -(-N // block_n)
     tiles = m_tiles * n_tiles
-    kb = -(-K // 64)
+    kb = -(-K // block_k)  # k-blocks per tile (64 for 16-bit, 128 for FP8 inputs)
     feats = []
     for t in range(tiles):
         c, it = t % num_clusters, t // num_clusters

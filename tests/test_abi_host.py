@@ -168,3 +168,40 @@ def test_tile_map_limits_and_large_grids(lib):
     last_group_first = (tiles // per_group - 1) * per_group
     m0, n0 = binding.gemm_tile_origin(M, N, bm, bn, group, last_group_first)
     assert n0 == 0 and m0 == ((M // bm) // group - 1) * group * bm
+
+
+def call8(A=P, B=Q, D=R, M=128, N=128, K=128, lda=128, ldb=128, ldd=128, fmt=2, out=1, alpha=1.0,
+          opts=None):
+    o = binding._options(opts)
+    return binding.load().gemm_fp8_run(A, B, D, M, N, K, lda, ldb, ldd, fmt, out, alpha, o, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=0), -2),            # a 16-bit input type
+    (dict(fmt=1), -2),
+    (dict(fmt=4), -2),
+    (dict(out=2), -2),            # FP8 output is not offered
+    (dict(M=-1), -3),
+    (dict(lda=64), -3),           # lda < K
+    (dict(lda=136), -4),          # byte rows: ld must be a multiple of 16
+    (dict(ldb=152, K=128), -4),
+    (dict(A=P + 8), -4),
+    (dict(ldd=130), -4),
+    (dict(D=P + 64), -5),         # D overlaps A (A is 128 x 128 bytes = 16 KiB)
+    (dict(A=0), -1),
+    (dict(opts={"consumers": 3}), -8),
+])
+def test_fp8_argument_errors(lib, kw, status):
+    assert call8(**kw) == status
+
+
+def test_fp8_types_are_rejected_by_the_16bit_entry_points(lib):
+    assert call(dtype=2) == -2 and call(dtype=3) == -2
+    # an FP8 plan exists for A.Bt only
+    n = binding.ctypes.c_size_t()
+    st = binding.load().gemm_workspace_size(128, 128, 128, 2, 1, None, binding.ctypes.byref(n))
+    assert st == -8
+
+
+def test_fp8_empty_output_is_a_no_op(lib):
+    assert call8(M=0) == 0 and call8(N=0) == 0 and call8(M=0, A=0, B=0, D=0) == 0
