@@ -278,6 +278,60 @@ def make_inputs(cfg):
     return inputs.operands(cfg.M, cfg.N, cfg.K, cfg.layout, cfg.dtype, cfg.dist, cfg.seed)
 
 
+# ---- per-workload types: 16-bit (A, B, D share a type) or FP8 inputs --------------
+
+def metric_for(cfg) -> str:
+    from dense_gemm_engineering_gb300 import configs
+
+    if cfg.name == configs.HEADLINE.name:
+        return METRIC
+    kind = f"{cfg.dtype.upper()}->{cfg.out.upper()}" if cfg.is_fp8 else cfg.dtype.upper()
+    op = "A·Bᵀ" if cfg.layout == "abt" else "A·B"
+    return f"GEMM TFLOP/s ({kind} {op}, {cfg.M}x{cfg.N}x{cfg.K})"
+
+
+def storage_tensor(X):
+    """numpy bit patterns -> CPU torch tensor over the same bytes (int16 / uint8)."""
+    import numpy as np
+    import torch
+
+    return torch.from_numpy(X.view(np.int16) if X.dtype == np.uint16 else X)
+
+
+def torch_dtype(name: str):
+    import torch
+
+    return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
+
+
+def operand(t, cfg):
+    """Device storage tensor -> the view the GEMM entry point takes."""
+    return t if cfg.is_fp8 else t.view(torch_dtype(cfg.dtype))
+
+
+def gemm_for(cfg):
+    from dense_gemm_engineering_gb300 import binding
+
+    if cfg.is_fp8:
+        return lambda a, b, d: binding.gemm_fp8(a, b, d, fmt=cfg.dtype, alpha=cfg.alpha)
+    return binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+
+
+def oracle_rows(orc, cfg, A, B, rows):
+    if cfg.is_fp8:
+        return orc.gemm_fp8(A, B, fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha, rows=rows)
+    return orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=rows)
+
+
+def peak_for(cfg, peaks):
+    """Roofline denominator: the measured bf16 burst, x2 for FP8 inputs (the
+    nominal dense FP8 : BF16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if cfg.is_fp8:
+        return 2.0 * bf16, "bf16 burst (MEASURED_PEAKS.json) x 2, the nominal FP8:BF16 ratio"
+    return bf16, "bf16 burst (MEASURED_PEAKS.json); FP16:BF16 nominal ratio 1:1"
+
+
 def oracle_sample(cfg, A, B, target_s: float):
     """Time the oracle on the first rows of D, sized to about target_s seconds."""
     import oracle
@@ -285,11 +339,11 @@ def oracle_sample(cfg, A, B, target_s: float):
     orc = oracle.get()
     probe_rows = min(cfg.M, 8)
     t0 = time.perf_counter()
-    orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, probe_rows))
+    oracle_rows(orc, cfg, A, B, (0, probe_rows))
     t_probe = max(time.perf_counter() - t0, 1e-6)
     rows = max(probe_rows, min(cfg.M, int(target_s / (t_probe / probe_rows))))
     t0 = time.perf_counter()
-    orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, rows))
+    oracle_rows(orc, cfg, A, B, (0, rows))
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cfg.N * cfg.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
@@ -309,7 +363,7 @@ def oracle_single_core(cfg, A, B, rows: int = 64):
     orc.set_num_threads(1)
     try:
         t0 = time.perf_counter()
-        orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(0, rows))
+        oracle_rows(orc, cfg, A, B, (0, rows))
         dt = time.perf_counter() - t0
     finally:
         orc.set_num_threads(threads)
@@ -360,14 +414,15 @@ def run_reference(args, cfg):
     for i in range(args.warmup + args.steps):
         r0 = (i * step_rows) % max(1, cfg.M - step_rows + 1)
         t0 = time.perf_counter()
-        orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=(r0, r0 + step_rows))
+        oracle_rows(orc, cfg, A, B, (r0, r0 + step_rows))
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
     flops = 2.0 * step_rows * cfg.N * cfg.K
     value = flops / sec / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_for(cfg), "value": value, "unit": UNIT,
+        "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic",
@@ -400,13 +455,12 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
     import torch
 
     flops = 2.0 * cfg.M * cfg.N * cfg.K
-    tdt = torch.float16 if cfg.dtype == "f16" else torch.bfloat16
-    hA = torch.from_numpy(A.view(np.int16)).pin_memory()
-    hB = torch.from_numpy(B.view(np.int16)).pin_memory()
+    hA = storage_tensor(A).pin_memory()
+    hB = storage_tensor(B).pin_memory()
     slots = 2
-    dA = [torch.empty(hA.shape, dtype=torch.int16, device=dev) for _ in range(slots)]
-    dB = [torch.empty(hB.shape, dtype=torch.int16, device=dev) for _ in range(slots)]
-    dD = [torch.empty((cfg.M, cfg.N), dtype=tdt, device=dev) for _ in range(slots)]
+    dA = [torch.empty(hA.shape, dtype=hA.dtype, device=dev) for _ in range(slots)]
+    dB = [torch.empty(hB.shape, dtype=hB.dtype, device=dev) for _ in range(slots)]
+    dD = [torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev) for _ in range(slots)]
     hD = [torch.empty((cfg.M, cfg.N), dtype=torch.int16).pin_memory() for _ in range(slots)]
     comp = torch.cuda.current_stream(dev)
     s_a, s_b, s_d = (torch.cuda.Stream(dev) for _ in range(3))
@@ -434,7 +488,7 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
                 comp.wait_event(ev)
             if i >= slots:
                 comp.wait_event(d2h_done[i - slots])  # D slot k downloaded
-            gemm(dA[k].view(tdt), dB[k].view(tdt), dD[k])
+            gemm(operand(dA[k], cfg), operand(dB[k], cfg), dD[k])
             gemm_done[i].record(comp)
             s_d.wait_event(gemm_done[i])
             with torch.cuda.stream(s_d):
@@ -451,7 +505,7 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
         for _ in range(count):
             dA[0].copy_(hA, non_blocking=True)
             dB[0].copy_(hB, non_blocking=True)
-            gemm(dA[0].view(tdt), dB[0].view(tdt), dD[0])
+            gemm(operand(dA[0], cfg), operand(dB[0], cfg), dD[0])
             hD[0].copy_(dD[0].view(torch.int16), non_blocking=True)
         e1.record(comp)
         torch.cuda.synchronize(dev)
@@ -464,7 +518,7 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
     return {"value": job_throughput(flops, world, ms), "unit": UNIT, "ms_per_step": ms,
             "steps": n, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
             "d2h_bytes_per_step": int(cfg.M * cfg.N * 2),
-            "path": "pinned host A, B -> device (2 copy streams) -> gemm_abt/gemm_ab -> device D "
+            "path": "pinned host A, B -> device (2 copy streams) -> the public GEMM call -> device D "
                     "-> pinned host (copy stream); 2 device slots, step i+1's uploads and step "
                     "i-1's download overlap step i's GEMM",
             "serial_value": job_throughput(flops, world, ms_serial),
@@ -487,12 +541,10 @@ def run_ours(args, cfg):
     binding.load()
 
     A, B = make_inputs(cfg)
-    tdt = torch.float16 if cfg.dtype == "f16" else torch.bfloat16
-    dA16 = torch.from_numpy(A.view(np.int16)).to(dev)
-    dB16 = torch.from_numpy(B.view(np.int16)).to(dev)
-    dA, dB = dA16.view(tdt), dB16.view(tdt)
-    dD = torch.empty((cfg.M, cfg.N), dtype=tdt, device=dev)
-    gemm = binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+    dA = operand(storage_tensor(A).to(dev), cfg)
+    dB = operand(storage_tensor(B).to(dev), cfg)
+    dD = torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev)
+    gemm = gemm_for(cfg)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -542,13 +594,15 @@ def run_ours(args, cfg):
         e2e = end_to_end(A, B, cfg, gemm, dev, args.steps, world)
 
     peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak, peak_basis = peak_for(cfg, peaks)
     src_hash = kernel_source_hash()
     traffic = recorded_traffic(cfg.name, src_hash)
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    nominal = props.multi_processor_count * FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
-    plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, 0 if cfg.dtype == "f16" else 1,
-                             0 if cfg.layout == "abt" else 1)
+    flop_clk = FLOP_PER_CLK_PER_SM * (2 if cfg.is_fp8 else 1)
+    nominal = props.multi_processor_count * flop_clk * sm_max * 1e6 / 1e12
+    dtype_code = {"f16": binding.GEMM_F16, "bf16": binding.GEMM_BF16, "e4m3": binding.GEMM_E4M3,
+                  "e5m2": binding.GEMM_E5M2}[cfg.dtype]
+    plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, dtype_code, 0 if cfg.layout == "abt" else 1)
 
     if rank != 0:
         if world > 1:
@@ -563,16 +617,31 @@ def run_ours(args, cfg):
     context = None
     if not args.no_context:
         n_ctx = max(5, min(args.steps, 20))
-        if cfg.layout == "abt":
+        if cfg.is_fp8:
+            # cuBLASLt's FP8 GEMM through torch (scales of 1, alpha folded in by D's scale)
+            f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
+            a8, b8 = dA.view(f8), dB.view(f8)
+            one = torch.tensor(1.0, device=dev)
+            sa = torch.tensor(float(cfg.alpha), device=dev)
+            mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=one,  # noqa: E731
+                                          out_dtype=torch_dtype(cfg.out))
+            mm_what = "torch._scaled_mm (cuBLASLt FP8)"
+        elif cfg.layout == "abt":
             mm = lambda: torch.mm(dA, dB.t())  # noqa: E731
+            mm_what = "torch.mm (cuBLAS)"
         else:
             mm = lambda: torch.mm(dA, dB)  # noqa: E731
-        t_mm = time_launches(mm, n_ctx, dev, flush)
+            mm_what = "torch.mm (cuBLAS)"
+        try:
+            t_mm = time_launches(mm, n_ctx, dev, flush)
+        except RuntimeError as e:  # e.g. an FP8 format the library does not take
+            t_mm, mm_what = None, f"{mm_what} unavailable: {str(e).splitlines()[0][:120]}"
         t_warm = time_launches(lambda: gemm(dA, dB, dD), n_ctx, dev)
         context = {
-            "torch_mm": {"value": flops / (t_mm / 1e3) / 1e12, "unit": UNIT, "ms_per_step": t_mm,
-                         "what": "torch.mm (cuBLAS) on the same device tensors, L2 flushed "
-                                 "before each launch, CUDA events"},
+            "torch_mm": {"value": flops / (t_mm / 1e3) / 1e12 if t_mm else None, "unit": UNIT,
+                         "ms_per_step": t_mm,
+                         "what": f"{mm_what} on the same device tensors, L2 flushed before each "
+                                 "launch, CUDA events"},
             "ours_warm_l2": {"value": flops / (t_warm / 1e3) / 1e12, "unit": UNIT,
                              "ms_per_step": t_warm,
                              "what": "this GEMM back to back, inputs left in L2"},
@@ -583,7 +652,8 @@ def run_ours(args, cfg):
             raise RuntimeError("device status word set during the context runs")
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(cfg), "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K,
@@ -594,12 +664,11 @@ def run_ours(args, cfg):
                    "wall_s_timed_region": t_wall},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json); FP16:BF16 "
-                                    "nominal ratio 1:1",
+                     "peak_source": f"{peak_src} {peak_basis}",
                      "kernel_source": src_hash},
         "tensor_peak_nominal": {"tflops": nominal, "frac": achieved / nominal,
                                 "basis": f"{props.multi_processor_count} SMs x "
-                                         f"{FLOP_PER_CLK_PER_SM} flop/clk x {sm_max:.0f} MHz"},
+                                         f"{flop_clk} flop/clk x {sm_max:.0f} MHz"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -610,7 +679,7 @@ def run_ours(args, cfg):
     }
     if clocks and clocks.get("sm_mhz"):
         line["tensor_peak_nominal"]["frac_at_run_clock"] = (
-            achieved / (props.multi_processor_count * FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] / 1e6))
+            achieved / (props.multi_processor_count * flop_clk * clocks["sm_mhz"] / 1e6))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -10,6 +10,11 @@ Sources of the shapes:
     backend", section 1 (the TileFoundry H200 workload, B stored K x N).
   * 3000 x 5000 x 4000 A.Bt FP16: a ragged shape, not a multiple of any tile,
     that exercises the out-of-bounds fill on loads and the clipped stores.
+
+FP8 workloads (E4M3 inputs, BF16 output; "TIRx: A Unified Tile Primitive ML
+Compiler", kernel performance: FP8 GEMMs with M = 8192 and model-derived weight
+shapes, which the page does not list): the headline square shape in FP8, and
+M = N = K = 8192.
 """
 from __future__ import annotations
 
@@ -23,9 +28,23 @@ class GemmConfig:
     M: int
     N: int
     K: int
-    dtype: str  # "f16" or "bf16" (inputs and output)
+    dtype: str  # input type: "f16" / "bf16" (also the output), or FP8 "e4m3" / "e5m2"
     dist: str  # "uniform" U[-1,1) or "normal" N(0, 0.02^2)
     seed: int
+    out_dtype: str = ""  # FP8 inputs: the 16-bit output type ("" = dtype)
+    alpha: float = 1.0  # FP8 inputs: D = alpha * A.Bt
+
+    @property
+    def is_fp8(self) -> bool:
+        return self.dtype in ("e4m3", "e5m2")
+
+    @property
+    def out(self) -> str:
+        return self.out_dtype or self.dtype
+
+    @property
+    def elem_bytes(self) -> int:
+        return 1 if self.is_fp8 else 2
 
     @property
     def flops(self) -> int:
@@ -33,12 +52,12 @@ class GemmConfig:
 
     @property
     def min_bytes(self) -> int:
-        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+        return self.elem_bytes * (self.M * self.K + self.N * self.K) + 2 * self.M * self.N
 
     @property
     def rtol(self) -> float:
-        # |got - ref| <= 1e-2 + rtol * |ref|
-        return 1e-3 if self.dtype == "f16" else 8e-3
+        # |got - ref| <= 1e-2 + rtol * |ref|, set by the 16-bit output type
+        return 1e-3 if self.out == "f16" else 8e-3
 
     atol: float = 1e-2
 
@@ -51,7 +70,14 @@ CONFIGS = [
     GemmConfig("ragged_3000x5000x4000_f16_abt", "abt", 3000, 5000, 4000, "f16", "uniform", 4),
 ]
 
-BY_NAME = {c.name: c for c in CONFIGS}
+FP8_CONFIGS = [
+    GemmConfig("fp8_square_4096x4096x4096_e4m3_abt", "abt", 4096, 4096, 4096, "e4m3", "uniform",
+               12, out_dtype="bf16"),
+    GemmConfig("fp8_8192x8192x8192_e4m3_abt", "abt", 8192, 8192, 8192, "e4m3", "normal", 13,
+               out_dtype="bf16"),
+]
+
+BY_NAME = {c.name: c for c in CONFIGS + FP8_CONFIGS}
 
 # The measured workload: FP16 A.Bt at 4096^3.
 HEADLINE = CONFIGS[2]

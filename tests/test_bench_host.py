@@ -65,8 +65,33 @@ def test_reference_arm_line():
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
-    assert line["metric"] == bench.METRIC and line["value"] > 0
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.BY_NAME["kloop_256x256x1024_f16_abt"]
+    assert line["metric"] == bench.metric_for(cfg) and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_metric_names_follow_the_workload():
+    from dense_gemm_engineering_gb300 import configs
+
+    assert bench.metric_for(configs.HEADLINE) == bench.METRIC
+    names = {bench.metric_for(c) for c in configs.CONFIGS + configs.FP8_CONFIGS}
+    assert len(names) == len(configs.CONFIGS) + len(configs.FP8_CONFIGS)
+    fp8 = configs.FP8_CONFIGS[0]
+    assert "E4M3->BF16" in bench.metric_for(fp8)
+    peak, basis = bench.peak_for(fp8, {"bf16_tflops": 1910.0})
+    assert peak == 3820.0 and "x 2" in basis
+
+
+def test_reference_arm_runs_the_fp8_oracle():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--config",
+                        "fp8_square_4096x4096x4096_e4m3_abt"], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and "E4M3" in line["metric"]
 
 
 def test_traffic_lookup_matches_only_current_kernel(tmp_path, monkeypatch):
