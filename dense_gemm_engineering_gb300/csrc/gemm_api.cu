@@ -206,8 +206,8 @@ size_t workspace_bytes_needed(const Plan& p) {
 //  * Balanced grid (default): run the same number of rounds on the fewest
 //    clusters, C' = ceil(T / rounds), so every cluster gets the same tile
 //    count and no cluster idles in a partial round.  The clusters left out
-//    draw no power, which lets the busy ones clock higher (the kernel is
-//    power-limited: measured ~3 % at 4096^3, 256 tiles on 64 instead of 76
+//    draw no power, which lets the busy ones clock higher (the clock is set by
+//    the power limit: measured ~3 % at 4096^3, 256 tiles on 64 instead of 76
 //    clusters).
 //  * Split tail (tail_split = s >= 2, with a workspace): keep all C clusters
 //    and split each tail tile into s K-ranges whose FP32 partials are summed
@@ -403,11 +403,9 @@ int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_co
 // costs one tile time, and a tile's time grows with its width divided by the
 // MMA efficiency of that width (narrower tiles move more operand bytes per
 // FLOP).  Pick the width with the least rounds x width / efficiency; ties go
-// to the wider tile.  The efficiencies are deliberately low: the kernel is
-// power-limited on GB300, so a narrower tile that only trims idle time in the
-// last round does not pay (4096^3: 224-wide tiles fill 4 rounds exactly yet run
-// no faster than 256-wide tiles on a balanced grid); a narrower width is taken
-// only when it removes whole rounds.
+// to the wider tile.  4096^3 on 76 clusters: 256-wide tiles take 4 rounds of
+// 256, 224-wide tiles 4 rounds of 224 (all 304 tiles busy), and the 224-wide
+// plan runs ~7 % faster; at 8192^3 the two tie and 256 wins.
 int choose_block_n(int64_t M, int64_t N, int bm, int b_layout, int cg, int dtype, int dev,
                    int sm_count) {
     struct Cand {

@@ -2,7 +2,8 @@
 //
 // One persistent, warp-specialised kernel computes D = A.B^T (B stored N x K,
 // K-major) or D = A.B (B stored K x N, MN-major) with FP16/BF16 operands, an
-// FP32 accumulator in Tensor Memory and a 16-bit output.
+// FP32 accumulator in Tensor Memory and a 16-bit output; with F8 set it takes
+// FP8 (E4M3 / E5M2) A and B, K-major, and writes round(alpha * A.B^T).
 //
 // Structure, and the passages it follows:
 //   * Operands move GMEM -> SMEM by TMA into a ring of STAGES slots, 128-byte
@@ -17,9 +18,10 @@
 //     acc_empty[b] (accumulator b drained, epilogue -> MMA).  A waiter on a
 //     "free" barrier starts on the opposite parity, so the first pass through
 //     the ring does not block; every reuse flips the phase bit (V2, V7).
-//   * Warp 0: TMA producer (one thread).  Warp 1: allocates TMEM and, in the
-//     cluster's leader CTA, issues tcgen05.mma from one thread.  Warps 2-5:
-//     epilogue warpgroup (V7's writeback warpgroup).
+//   * Warp 0: TMA producer.  Warp 1: allocates TMEM and, in the cluster's
+//     leader CTA, issues tcgen05.mma.  Both loops run on the whole warp and
+//     one elected lane issues each copy / MMA / commit.  Warps 2-5: epilogue
+//     warpgroup (V7's writeback warpgroup).
 //   * Persistent CTAs walk the tile list of schedule.h (V6; TileFoundry
 //     sections 2-3).
 //   * CG == 2: a cluster of two CTAs computes a 256-row tile with
