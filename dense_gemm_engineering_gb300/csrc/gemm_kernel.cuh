@@ -483,8 +483,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             if (ok) {
                 // Drain: every accumulator slot released by every epilogue warp of
-                // the cluster (the peer's arrivals target this CTA's barriers).
-                for (uint32_t i = 0; i < C::NUM_ACC; ++i) {
+                // the cluster (the peer's arrivals target this CTA's barriers),
+                // except the slot of the cluster's last unit, which the epilogue
+                // keeps (its release would be the last arrival of the launch).
+                for (uint32_t i = 0; i + 1 < C::NUM_ACC; ++i) {
                     if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
                         ok = false;
                         break;
@@ -609,10 +611,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int32_t col0 = nt * C::BN_CLUSTER + int32_t(pair) * C::BN;
             const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::SLOT_COLS;
 
+            // In the cluster's last unit the accumulator is not handed back: no
+            // MMA will write it again, the MMA warp's drain does not wait for it,
+            // and the teardown barrier orders these TMEM reads before the
+            // dealloc.  (The hand-back is a cluster-scope release arrive that
+            // costs the last tile's epilogue ~1.3 k cycles on the critical path.)
+            const bool last_unit = (u + num_clusters >= units);
+            auto release = [&](uint32_t b) {
+                if (!last_unit) release_acc(b);
+            };
             if (w.range < 0) {
                 // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
                 // the CTA's A rows 128h..128h+127).
-                const bool last_unit = (u + num_clusters >= units);
 #pragma unroll 1
                 for (int h = 0; h < C::CONS; ++h) {
                     const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
@@ -625,7 +635,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_ld_32x32b_x32(th + 64u * j + 32u,
                                                 *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
                         ptx::tmem_wait_ld();
-                        if (last_h && j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release_acc(ab);
+                        if (last_h && j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release(ab);
                         store_chunk(bits, col0 + 64 * j, rh, last_unit ? h * C::FULL_CHUNKS + j : -1);
                     }
                     if constexpr (C::HALF_CHUNK) {
@@ -633,7 +643,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(th + 64u * C::FULL_CHUNKS, r);
                         ptx::tmem_wait_ld();
-                        if (last_h) release_acc(ab);
+                        if (last_h) release(ab);
                         store_half_chunk(r, col0 + 64 * C::FULL_CHUNKS, rh + int32_t(lane));
                     }
                 }
@@ -660,7 +670,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (lane == 0) before = count_range_done(args.counters + quad, args.epoch);
                 before = __shfl_sync(0xffffffffu, before, 0);
                 if (before != uint32_t(args.split - 1)) {
-                    release_acc(ab);  // another range finishes this block of D
+                    release(ab);  // another range finishes this block of D
                 } else if (u + num_clusters >= units &&
                            uint32_t(args.split - 1) <= C::PIECES_PER_WARP) {
                     // Pass 2 (the last range to finish, in this cluster's last
@@ -728,7 +738,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                     }
                                 }
                             }
-                            if (j == C::BN / 64 - 1) release_acc(ab);
+                            if (j == C::BN / 64 - 1) release(ab);
                             store_chunk(reinterpret_cast<const uint32_t(&)[64]>(acc), col0 + 64 * j, row0);
                         }
                     }
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 }
                             }
                         }
-                        if (j == C::BN / 64 - 1) release_acc(ab);
+                        if (j == C::BN / 64 - 1) release(ab);
                         store_chunk(reinterpret_cast<const uint32_t(&)[64]>(acc), col0 + 64 * j, row0);
                     }
                 }
