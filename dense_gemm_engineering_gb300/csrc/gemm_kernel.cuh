@@ -784,13 +784,29 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
         }
+        // Done with TMEM and with the cluster's shared state: arrive on the
+        // final cluster barrier now, so that its latency and the skew between
+        // the cluster's CTAs overlap the drain of this warp's bulk stores.
+        ptx::tc_fence_before();
+        if constexpr (C::CLUSTER > 1) ptx::cluster_arrive();
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();
     }
 
     // ---- teardown ---------------------------------------------------------
-    ptx::tc_fence_before();
-    if constexpr (C::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
+    // Every CTA of the cluster stays until all are done (the peer reads this
+    // CTA's shared memory and arrives on its barriers); TMEM is freed after
+    // every warp's last TMEM read.
+    if constexpr (C::CLUSTER > 1) {
+        if (warp < 2) {
+            ptx::tc_fence_before();
+            ptx::cluster_arrive();
+        }
+        ptx::cluster_wait();
+    } else {
+        ptx::tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);

@@ -58,6 +58,15 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a warp that is done with the cluster's
+// shared state early but may only leave once every CTA of the cluster is.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The shared::cluster address of `addr` (a shared::cta address of this CTA's
 // layout) inside CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
