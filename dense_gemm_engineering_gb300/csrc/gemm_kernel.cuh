@@ -57,6 +57,9 @@ constexpr int kBlockK8 = 128;       // 128 x 8 bit: the same 128-byte row for FP
 constexpr int kNumThreads = 192;    // 6 warps: producer, MMA, 4 epilogue
 constexpr int kEpilogueWarps = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Pause between an epilogue warp's 64-column chunk stores (see the epilogue).
+constexpr uint32_t kStorePaceNs = 1000;
+constexpr int kStorePaceMinKBlocks = 32;
 
 // Status word layout: bits 0..7 = reason, bits 8..15 = role.
 enum : uint32_t { kReasonTimeout = 1u, kReasonCounter = 2u };
@@ -620,6 +623,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             auto release = [&](uint32_t b) {
                 if (!last_unit) release_acc(b);
             };
+            // Store pacing: the epilogue's TMA stores share the SM's TMA engine with
+            // the operand loads, whose latency the ring only just covers; four
+            // warps storing a tile at once delay the loads behind them (measured
+            // ~700 cycles of MMA per 4096-deep tile).  Spreading each warp's chunk
+            // stores 1 us apart leaves the loads room.  The pauses also delay the
+            // accumulator hand-back, so they are used only where the next tile's
+            // MMAs (>= 32 k-blocks) outlast them and a second accumulator exists.
+            const bool pace = (C::NUM_ACC == 2) && !last_unit && w.kb1 - w.kb0 >= kStorePaceMinKBlocks;
             if (w.range < 0) {
                 // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
                 // the CTA's A rows 128h..128h+127).
@@ -636,6 +647,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                 *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
                         ptx::tmem_wait_ld();
                         if (last_h && j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release(ab);
+                        if (pace && j > 0) __nanosleep(kStorePaceNs);
                         store_chunk(bits, col0 + 64 * j, rh, last_unit ? h * C::FULL_CHUNKS + j : -1);
                     }
                     if constexpr (C::HALF_CHUNK) {
