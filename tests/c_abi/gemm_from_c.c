@@ -2,10 +2,12 @@
  * gemm_from_c.c -- drives the GEMM library through its C ABI from plain C.
  *
  * Usage: gemm_from_c <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin
- * Reads A (M x K) and B (N x K for abt, K x N for ab) as raw 16-bit patterns,
- * runs gemm_abt / gemm_ab on cudaMalloc'd buffers on a created stream, writes
- * D (M x N) to D.bin, and checks that a few invalid calls return the
- * documented status codes.  Exit status 0 on success.
+ *        gemm_from_c fp8 <e4m3|e5m2> M N K A.bin B.bin D.bin alpha
+ * Reads A (M x K) and B (N x K for abt / fp8, K x N for ab) as raw 16-bit
+ * patterns (bytes for fp8), runs gemm_abt / gemm_ab / gemm_fp8_abt (BF16 D)
+ * on cudaMalloc'd buffers on a created stream, writes D (M x N, 16-bit) to
+ * D.bin, and checks that a few invalid calls return the documented status
+ * codes.  Exit status 0 on success.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -39,14 +41,20 @@ static void* read_file(const char* path, size_t bytes) {
     } while (0)
 
 int main(int argc, char** argv) {
-    if (argc != 9) {
-        fprintf(stderr, "usage: %s <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin\n", argv[0]);
+    const int fp8 = argc >= 2 && strcmp(argv[1], "fp8") == 0;
+    if (argc != (fp8 ? 10 : 9)) {
+        fprintf(stderr, "usage: %s <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin\n"
+                        "       %s fp8 <e4m3|e5m2> M N K A.bin B.bin D.bin alpha\n",
+                argv[0], argv[0]);
         return 2;
     }
     const int ab = strcmp(argv[1], "ab") == 0;
-    const int dtype = strcmp(argv[2], "bf16") == 0 ? GEMM_BF16 : GEMM_F16;
+    const int dtype = fp8 ? GEMM_BF16 : strcmp(argv[2], "bf16") == 0 ? GEMM_BF16 : GEMM_F16;
+    const int fmt = strcmp(argv[2], "e5m2") == 0 ? GEMM_E5M2 : GEMM_E4M3;
+    const float alpha = fp8 ? (float)atof(argv[9]) : 1.0f;
     const int64_t M = atoll(argv[3]), N = atoll(argv[4]), K = atoll(argv[5]);
-    const size_t a_bytes = (size_t)(M * K) * 2, b_bytes = (size_t)(N * K) * 2,
+    const size_t esize = fp8 ? 1 : 2;
+    const size_t a_bytes = (size_t)(M * K) * esize, b_bytes = (size_t)(N * K) * esize,
                  d_bytes = (size_t)(M * N) * 2;
     void* hA = read_file(argv[6], a_bytes);
     void* hB = read_file(argv[7], b_bytes);
@@ -63,8 +71,9 @@ int main(int argc, char** argv) {
     CHECK_CUDA(cudaMemcpy(dA, hA, a_bytes, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dB, hB, b_bytes, cudaMemcpyHostToDevice));
 
-    int st = ab ? gemm_ab(dA, dB, dD, M, N, K, K, N, N, dtype, s)
-                : gemm_abt(dA, dB, dD, M, N, K, K, K, N, dtype, s);
+    int st = fp8  ? gemm_fp8_abt(dA, dB, dD, M, N, K, K, K, N, fmt, dtype, alpha, s)
+             : ab ? gemm_ab(dA, dB, dD, M, N, K, K, N, N, dtype, s)
+                  : gemm_abt(dA, dB, dD, M, N, K, K, K, N, dtype, s);
     if (st != GEMM_OK) {
         fprintf(stderr, "gemm: %s\n", gemm_status_string(st));
         return 1;
@@ -82,6 +91,13 @@ int main(int argc, char** argv) {
     fclose(f);
 
     /* documented errors */
+    if (fp8) {
+        if (gemm_fp8_abt(dA, dB, dD, M, N, K, K, K, N, GEMM_F16, dtype, 1.0f, s) != GEMM_ERR_DTYPE)
+            return 3;
+        if (gemm_fp8_abt(dA, dB, dD, M, N, K, K + 8, K, N, fmt, dtype, 1.0f, s) != GEMM_ERR_ALIGN)
+            return 3;
+        if (gemm_abt(dA, dB, dD, M, N, K, K, K, N, fmt, s) != GEMM_ERR_DTYPE) return 3;
+    }
     if (gemm_abt(dA, dB, dD, M, N, K, K, K, N, 7, s) != GEMM_ERR_DTYPE) return 3;
     if (gemm_abt(NULL, dB, dD, M, N, K, K, K, N, dtype, s) != GEMM_ERR_NULL) return 3;
     if (gemm_abt((char*)dA + 2, dB, dD, M, N, K, K, K, N, dtype, s) != GEMM_ERR_ALIGN) return 3;

@@ -56,3 +56,27 @@ def test_gemm_from_plain_c(tmp_path, layout, dtype, M, N, K):
     D = np.fromfile(tmp_path / "D.bin", dtype=np.uint16).reshape(M, N)
     ref = oracle.gemm(A, B, layout=layout, dtype=dtype)
     check_close(D, ref, dtype, "plain C caller")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_gemm_from_plain_c(tmp_path, fmt):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    exe = str(tmp_path / "gemm_from_c")
+    r = _compile(exe)
+    assert r.returncode == 0, r.stderr
+    M, N, K, alpha = 300, 520, 272, 0.75
+    A, B = inputs.operands(M, N, K, "abt", fmt, "uniform", 32)
+    A.tofile(tmp_path / "A.bin")
+    B.tofile(tmp_path / "B.bin")
+    r = subprocess.run([exe, "fp8", fmt, str(M), str(N), str(K), str(tmp_path / "A.bin"),
+                        str(tmp_path / "B.bin"), str(tmp_path / "D.bin"), str(alpha)],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+    D = np.fromfile(tmp_path / "D.bin", dtype=np.uint16).reshape(M, N)
+    ref = oracle.gemm_fp8(A, B, fmt=fmt, out_dtype="bf16", alpha=alpha)
+    check_close(D, ref, "bf16", "plain C caller, FP8")
