@@ -332,6 +332,25 @@ def peak_for(cfg, peaks):
     return bf16, "bf16 burst (MEASURED_PEAKS.json); FP16:BF16 nominal ratio 1:1"
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm part)."""
+    import platform
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        info = ""
+    for key in ("model name", "Model Name", "Processor"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", info, re.M)
+        if m:
+            return m.group(1).strip()
+    m = re.search(r"^CPU implementer\s*:\s*(\S+)[\s\S]*?^CPU part\s*:\s*(\S+)$", info, re.M)
+    if m:
+        return f"{platform.machine()} implementer {m.group(1)} part {m.group(2)}"
+    return platform.processor() or platform.machine()
+
+
 def oracle_sample(cfg, A, B, target_s: float):
     """Time the oracle on the first rows of D, sized to about target_s seconds."""
     import oracle
@@ -347,7 +366,7 @@ def oracle_sample(cfg, A, B, target_s: float):
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cfg.N * cfg.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
-            "kind": "oracle",
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"rows 0..{rows} of D ({rows} x {cfg.N} outputs, K={cfg.K}), "
                       f"{dt:.1f} s"}, rows, dt
 
