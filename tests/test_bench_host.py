@@ -117,7 +117,7 @@ def test_source_hash_ignores_comments_but_not_code():
     assert '"// not a comment"' in bench.strip_c_comments(code)
 
 
-def test_single_core_oracle_context_restores_threads():
+def test_single_core_oracle_baseline_restores_threads():
     import oracle
     from dense_gemm_engineering_gb300 import configs
 
