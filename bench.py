@@ -286,7 +286,8 @@ def metric_for(cfg) -> str:
 
     if cfg.name == configs.HEADLINE.name:
         return METRIC
-    kind = f"{cfg.dtype.upper()}->{cfg.out.upper()}" if cfg.is_fp8 else cfg.dtype.upper()
+    names = {"f16": "FP16", "bf16": "BF16", "e4m3": "E4M3", "e5m2": "E5M2"}
+    kind = f"{names[cfg.dtype]}->{names[cfg.out]}" if cfg.is_fp8 else names[cfg.dtype]
     op = "A·Bᵀ" if cfg.layout == "abt" else "A·B"
     return f"GEMM TFLOP/s ({kind} {op}, {cfg.M}x{cfg.N}x{cfg.K})"
 
@@ -427,8 +428,9 @@ def run_reference(args, cfg):
     import oracle
 
     orc = oracle.get()
-    # Size one step to ~1.5 s so warm-up + steps end within a few minutes.
-    _, rows, dt = oracle_sample(cfg, A, B, target_s=1.5)
+    # Size each step so that warm-up + steps end within about two minutes.
+    step_s = max(0.02, min(1.5, 120.0 / max(1, args.warmup + args.steps)))
+    _, rows, dt = oracle_sample(cfg, A, B, target_s=step_s)
     step_rows = rows
     times = []
     for i in range(args.warmup + args.steps):
