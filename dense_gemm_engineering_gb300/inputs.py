@@ -26,6 +26,11 @@ largest finite value saturate to it, which the drawn values never reach).
 
 Stream 0 draws A, stream 1 draws B.  Padding columns (row stride > cols) are
 filled with a quiet NaN so that any read of padding poisons the result.
+
+Block scales (MX): one UE8M0 byte per 32 K elements of each row of A (stream 2)
+and of B (stream 3), row-major with ceil(K/32) bytes per row; byte i of a
+stream is lo + (draw_i >> 11) mod (hi - lo + 1), a power-of-two scale
+2^(byte - 127).  Padding bytes hold 255, the UE8M0 NaN.
 """
 from __future__ import annotations
 
@@ -179,6 +184,33 @@ def matrix(seed: int, stream: int, rows: int, cols: int, dtype: str, dist: str,
     buf = np.full((rows, ld), NAN_BITS[dtype], dtype=flat.dtype)
     buf[:, :cols] = flat.reshape(rows, cols)
     return buf[:, :cols]
+
+
+def mx_scales(seed: int, stream: int, rows: int, K: int, lo: int = 124, hi: int = 130,
+              ld: int | None = None) -> np.ndarray:
+    """UE8M0 scale bytes of a rows x K block-scaled operand: (rows, ceil(K/32))
+    uint8, uniform integers in [lo, hi]; row stride ld (padding is 255)."""
+    if not (0 <= lo <= hi <= 254):
+        raise ValueError("scale bytes must lie in [0, 254]")
+    groups = -(-K // 32)
+    ld = groups if ld is None else ld
+    if ld < groups:
+        raise ValueError("ld < ceil(K / 32)")
+    d = draws(seed, stream, 0, rows * groups)
+    x = (np.uint64(lo) + (d >> np.uint64(11)) % np.uint64(hi - lo + 1)).astype(np.uint8)
+    if ld == groups:
+        return x.reshape(rows, groups)
+    buf = np.full((rows, ld), 255, dtype=np.uint8)
+    buf[:, :groups] = x.reshape(rows, groups)
+    return buf[:, :groups]
+
+
+def mx_operands(M: int, N: int, K: int, fmt: str, dist: str, seed: int, lda: int | None = None,
+                ldb: int | None = None, lo: int = 124, hi: int = 130):
+    """(A, B, SA, SB) of a block-scaled FP8 D = A.Bt: FP8 patterns as operands()
+    draws them, and the scale bytes of mx_scales() (streams 2 and 3)."""
+    A, B = operands(M, N, K, "abt", fmt, dist, seed, lda=lda, ldb=ldb)
+    return A, B, mx_scales(seed, 2, M, K, lo, hi), mx_scales(seed, 3, N, K, lo, hi)
 
 
 def operands(M: int, N: int, K: int, layout: str, dtype: str, dist: str, seed: int,

@@ -88,6 +88,12 @@ class Oracle:
                                         ctypes.c_int, ctypes.c_double, i64, i64, i64, i64,
                                         u16p, f64p, i64]
         lib.oracle_gemm_fp8.restype = None
+        lib.oracle_ue8m0_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_ue8m0_to_double.restype = ctypes.c_double
+        lib.oracle_gemm_mx.argtypes = [u8p, u8p, u8p, u8p, i64, i64, i64, i64, i64, i64, i64,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, i64, i64, i64,
+                                       i64, u16p, f64p, i64]
+        lib.oracle_gemm_mx.restype = None
         self._lib = lib
         self.path = so_path
 
@@ -226,6 +232,62 @@ def _fp8_methods():
 
 Oracle.fp8_to_double, Oracle.gemm_fp8 = _fp8_methods()
 
+
+def _row_stride(X: np.ndarray) -> int:
+    return X.strides[0] if X.shape[0] > 1 else max(X.shape[1], 1)
+
+
+def _mx_methods():
+    def ue8m0_to_double(self, bits) -> np.ndarray:
+        """Value 2^(x - 127) of each UE8M0 scale byte (NaN for 255)."""
+        b = np.asarray(bits, dtype=np.uint8)
+        return np.array([self._lib.oracle_ue8m0_to_double(int(v)) for v in b.ravel()],
+                        dtype=np.float64).reshape(b.shape)
+
+    def gemm_mx(self, A, B, SA, SB, *, fmt="e4m3", out_dtype="bf16", alpha=1.0, rows=None,
+                cols=None, want_f64: bool = False):
+        """Oracle block-scaled FP8 GEMM: D = round(alpha * sum_k (A[i,k] sa) (B[j,k] sb))
+        with one UE8M0 scale per 32 K elements of each row: SA (M, ceil(K/32)) and
+        SB (N, ceil(K/32)) uint8, row-major (row stride free, unit inner stride)."""
+        f = _fp8(fmt)
+        d = _dt(out_dtype)
+        A, B, SA, SB = (np.asarray(x) for x in (A, B, SA, SB))
+        for x in (A, B, SA, SB):
+            if x.dtype != np.uint8 or x.ndim != 2:
+                raise TypeError("oracle.gemm_mx takes 2-D uint8 patterns")
+        A, B, SA, SB = (np.ascontiguousarray(x) if x.size and x.strides[1] != 1 else x
+                        for x in (A, B, SA, SB))
+        M, K = A.shape
+        N, Kb = B.shape
+        groups = -(-K // 32)
+        if Kb != K:
+            raise ValueError(f"K mismatch: {K} vs {Kb}")
+        if SA.shape != (M, groups) or SB.shape != (N, groups):
+            raise ValueError(f"scale shapes {SA.shape}, {SB.shape}; want ({M}, {groups}), "
+                             f"({N}, {groups})")
+        i0, i1 = rows if rows is not None else (0, M)
+        j0, j1 = cols if cols is not None else (0, N)
+        if not (0 <= i0 <= i1 <= M and 0 <= j0 <= j1 <= N):
+            raise ValueError("rows/cols out of range")
+        out16 = np.zeros((i1 - i0, j1 - j0), dtype=np.uint16)
+        out64 = np.zeros((i1 - i0, j1 - j0), dtype=np.float64) if want_f64 else None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        ptr = (lambda x: x.ctypes.data_as(u8p) if x.size else None)
+        if out16.size:
+            self._lib.oracle_gemm_mx(ptr(A), ptr(B), ptr(SA), ptr(SB), M, N, K,
+                                     _row_stride(A), _row_stride(B), _row_stride(SA),
+                                     _row_stride(SB), f, d, float(np.float32(alpha)),
+                                     i0, i1, j0, j1, out16.ctypes.data_as(u16p),
+                                     out64.ctypes.data_as(f64p) if want_f64 else None, j1 - j0)
+        return (out16, out64) if want_f64 else out16
+
+    return ue8m0_to_double, gemm_mx
+
+
+Oracle.ue8m0_to_double, Oracle.gemm_mx = _mx_methods()
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -260,3 +322,11 @@ def gemm_fp8(A, B, **kw):
 
 def fp8_to_double(bits, fmt):
     return get().fp8_to_double(bits, fmt)
+
+
+def gemm_mx(A, B, SA, SB, **kw):
+    return get().gemm_mx(A, B, SA, SB, **kw)
+
+
+def ue8m0_to_double(bits):
+    return get().ue8m0_to_double(bits)

@@ -30,7 +30,9 @@
  * bias 127, 7 fraction bits).
  *
  * The FP8 variant (oracle_gemm_fp8, below) follows the same rule from exact
- * E4M3 / E5M2 inputs, with one FP32 scale applied to the sum.
+ * E4M3 / E5M2 inputs, with one FP32 scale applied to the sum; the block-scaled
+ * variant (oracle_gemm_mx) adds one power-of-two scale per 32 K elements of
+ * each row of A and of B.
  *
  * Parity pins (tests/test_oracle.py): hand-computed products, identity and
  * permutation operands, the transpose invariant (A.Bt)t == B.At, closed forms
@@ -214,6 +216,61 @@ void oracle_gemm_fp8(const uint8_t* A, const uint8_t* B, int64_t M, int64_t N, i
         for (int64_t j = j0; j < j1; ++j) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) acc += dec[A[i * lda + k]] * dec[B[j * ldb + k]];
+            const double d = alpha * acc;
+            int64_t o = (i - i0) * ldo + (j - j0);
+            if (out_f64) out_f64[o] = d;
+            if (out16) out16[o] = oracle_from_double(d, out_dtype);
+        }
+    }
+}
+
+/* ---- Block-scaled FP8 inputs (MX) --------------------------------------------
+ *
+ * "TIRx: A Unified Tile Primitive ML Compiler", kernel performance, names FP8
+ * block-scaled matrix multiplication: groups of input values share scale
+ * factors that adjust their numerical range.  The page gives neither the group
+ * size nor the scale encoding.  Reading taken here: the OCP Microscaling (MX)
+ * formats, the block-scaled form that the tcgen05 kind::mxf8f6f4 MMA consumes.
+ * Each run of 32 consecutive K elements of a row of A, and of a row of B (both
+ * K-major), shares one 8-bit scale X in the UE8M0 encoding: the value is
+ * 2^(X - 127), and X = 255 is NaN.  An element's value is its FP8 value times
+ * its group's scale, so
+ *
+ *   D[i,j] = round_RNE( alpha * sum_{k<K} (A[i,k] * 2^(SA[i][k/32] - 127))
+ *                                      * (B[j,k] * 2^(SB[j][k/32] - 127)) )
+ *
+ * Scaling by a power of two is exact in binary64 over the whole UE8M0 range,
+ * so every term is exact; the sum runs over k in order and the result is
+ * rounded once.  SA is M x ceil(K/32) bytes and SB is N x ceil(K/32) bytes,
+ * row-major with row strides ldsa and ldsb.  With every scale equal to 127
+ * this is oracle_gemm_fp8.
+ */
+double oracle_ue8m0_to_double(uint8_t x) {
+    if (x == 255) return NAN;
+    return ldexp(1.0, (int)x - 127);
+}
+
+void oracle_gemm_mx(const uint8_t* A, const uint8_t* B, const uint8_t* SA, const uint8_t* SB,
+                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsa,
+                    int64_t ldsb, int in_fmt, int out_dtype, double alpha,
+                    int64_t i0, int64_t i1, int64_t j0, int64_t j1,
+                    uint16_t* out16, double* out_f64, int64_t ldo) {
+    (void)M;
+    (void)N;
+    double dec[256], scale[256];
+    for (int c = 0; c < 256; ++c) {
+        dec[c] = oracle_fp8_to_double((uint8_t)c, in_fmt);
+        scale[c] = oracle_ue8m0_to_double((uint8_t)c);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = i0; i < i1; ++i) {
+        for (int64_t j = j0; j < j1; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = dec[A[i * lda + k]] * scale[SA[i * ldsa + k / 32]];
+                const double b = dec[B[j * ldb + k]] * scale[SB[j * ldsb + k / 32]];
+                acc += a * b;
+            }
             const double d = alpha * acc;
             int64_t o = (i - i0) * ldo + (j - j0);
             if (out_f64) out_f64[o] = d;

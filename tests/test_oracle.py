@@ -286,6 +286,103 @@ def pin_fp8_transpose_invariant(orc):
     assert np.array_equal(d1.T, d2)
 
 
+def pin_ue8m0_decode_hand_values(orc):
+    # UE8M0 (OCP Microscaling): 8 exponent bits, bias 127, no sign or fraction;
+    # 255 is NaN.
+    codes = np.array([0, 1, 120, 126, 127, 128, 130, 254], dtype=np.uint8)
+    want = [2.0 ** -127, 2.0 ** -126, 2.0 ** -7, 0.5, 1.0, 2.0, 8.0, 2.0 ** 127]
+    assert np.array_equal(orc.ue8m0_to_double(codes), want)
+    assert np.isnan(orc.ue8m0_to_double(np.array([255], np.uint8))).all()
+
+
+def pin_mx_hand_product(orc):
+    # K = 33: group 0 = 32 ones, group 1 = one element.  A = [1 x32, 2],
+    # B = [1 x33]; SA = [128, 126] (x2, x0.5), SB = [127, 129] (x1, x4):
+    # D = 32 * 2 * 1 + 2 * 0.5 * 4 = 68.
+    A = np.array([[0x38] * 32 + [0x40]], dtype=np.uint8)
+    B = np.array([[0x38] * 33], dtype=np.uint8)
+    SA = np.array([[128, 126]], dtype=np.uint8)
+    SB = np.array([[127, 129]], dtype=np.uint8)
+    _, d64 = orc.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="f16", want_f64=True)
+    assert np.array_equal(d64, [[68.0]])
+    d16 = orc.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16", alpha=0.25)
+    assert np.array_equal(dec(d16, "bf16"), [[17.0]])
+
+
+def pin_mx_unit_scales_equal_fp8(orc):
+    # Every scale 2^0: the block-scaled product is the plain FP8 product.
+    for fmt in ("e4m3", "e5m2"):
+        A, B = inputs.operands(9, 14, 77, "abt", fmt, "uniform", 12)
+        ones = lambda r: np.full((r, 3), 127, dtype=np.uint8)
+        got, g64 = orc.gemm_mx(A, B, ones(9), ones(14), fmt=fmt, out_dtype="bf16", alpha=0.75,
+                               want_f64=True)
+        ref, r64 = orc.gemm_fp8(A, B, fmt=fmt, out_dtype="bf16", alpha=0.75, want_f64=True)
+        assert np.array_equal(g64, r64) and np.array_equal(got, ref), fmt
+
+
+def pin_mx_uniform_scales_scale_the_result(orc):
+    # SA = 127 + a and SB = 127 + b everywhere: D = 2^(a + b) * (A . Bt), exactly.
+    A, B = inputs.operands(11, 8, 96, "abt", "e4m3", "normal", 13)
+    _, base = orc.gemm_fp8(A, B, fmt="e4m3", out_dtype="bf16", want_f64=True)
+    for a, b in ((3, -5), (-2, 0), (6, 1)):
+        SA = np.full((11, 3), 127 + a, dtype=np.uint8)
+        SB = np.full((8, 3), 127 + b, dtype=np.uint8)
+        _, got = orc.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16", want_f64=True)
+        assert np.array_equal(got, base * 2.0 ** (a + b)), (a, b)
+
+
+def pin_mx_groups_closed_form(orc):
+    # Small-integer FP8 values and a different scale per (row, group): the sum
+    # splits into one exact product per 32-column group,
+    #   D = sum_g 2^(SA[:,g] - 127) 2^(SB[:,g] - 127)^T * (A_g . B_g^T),
+    # computed with numpy's float64 matmul (all partial sums exact here).
+    # K = 100: groups of 32, 32, 32 and 4 columns.
+    rng = np.random.default_rng(14)
+    M, N, K = 6, 5, 100
+    for fmt in ("e4m3", "e5m2"):
+        a = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+        b = rng.integers(-3, 4, size=(N, K)).astype(np.float32)
+        A, B = inputs.f32_to_fp8_bits(a, fmt), inputs.f32_to_fp8_bits(b, fmt)
+        SA = rng.integers(121, 134, size=(M, 4)).astype(np.uint8)
+        SB = rng.integers(121, 134, size=(N, 4)).astype(np.uint8)
+        want = np.zeros((M, N))
+        for g in range(4):
+            cols = slice(32 * g, min(32 * g + 32, K))
+            sa = np.ldexp(1.0, SA[:, g].astype(int) - 127)
+            sb = np.ldexp(1.0, SB[:, g].astype(int) - 127)
+            want += np.outer(sa, sb) * (a[:, cols].astype(np.float64) @ b[:, cols].astype(np.float64).T)
+        _, got = orc.gemm_mx(A, B, SA, SB, fmt=fmt, out_dtype="bf16", want_f64=True)
+        assert np.array_equal(got, want), fmt
+
+
+def pin_mx_strided_scales_ignore_padding(orc):
+    # Scale rows with padding (255 = NaN there) and operands with NaN padding:
+    # nothing outside the logical shapes may be read.
+    A, B, SA, SB = inputs.mx_operands(7, 9, 70, "e5m2", "uniform", 15, lda=96, ldb=80)
+    SA2 = inputs.mx_scales(15, 2, 7, 70, ld=8)
+    SB2 = inputs.mx_scales(15, 3, 9, 70, ld=5)
+    assert np.array_equal(SA2, SA) and np.array_equal(SB2, SB)
+    got = orc.gemm_mx(A, B, SA2, SB2, fmt="e5m2", out_dtype="bf16")
+    ref = orc.gemm_mx(np.ascontiguousarray(A), np.ascontiguousarray(B), np.ascontiguousarray(SA),
+                      np.ascontiguousarray(SB), fmt="e5m2", out_dtype="bf16")
+    assert np.array_equal(got, ref) and not np.isnan(dec(got, "bf16")).any()
+
+
+def pin_mx_nan_scale_poisons_its_row(orc):
+    A, B, SA, SB = inputs.mx_operands(4, 3, 64, "e4m3", "uniform", 16)
+    SA = SA.copy()
+    SA[2, 1] = 255
+    _, d64 = orc.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16", want_f64=True)
+    assert np.isnan(d64[2]).all() and not np.isnan(np.delete(d64, 2, axis=0)).any()
+
+
+def pin_mx_transpose_invariant(orc):
+    A, B, SA, SB = inputs.mx_operands(10, 13, 90, "e4m3", "normal", 17)
+    d1 = orc.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="f16")
+    d2 = orc.gemm_mx(B, A, SB, SA, fmt="e4m3", out_dtype="f16")
+    assert np.array_equal(d1.T, d2)
+
+
 PINS = {name: fn for name, fn in sorted(globals().items()) if name.startswith("pin_")}
 
 

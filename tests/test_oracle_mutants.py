@@ -41,6 +41,15 @@ MUTANTS = {
                  "acc -= dec[A[i * lda + k]] * dec[B[j * ldb + k]];"),
     "fp8_formats_swapped": ("dec[c] = oracle_fp8_to_double((uint8_t)c, in_fmt);",
                             "dec[c] = oracle_fp8_to_double((uint8_t)c, 1 - in_fmt);"),
+    "mx_group_64": ("scale[SA[i * ldsa + k / 32]]", "scale[SA[i * ldsa + k / 64]]"),
+    "mx_b_group_16_clamped": ("scale[SB[j * ldsb + k / 32]]",
+                              "scale[SB[j * ldsb + (k / 16 < ldsb ? k / 16 : ldsb - 1)]]"),
+    "mx_ue8m0_bias": ("return ldexp(1.0, (int)x - 127);", "return ldexp(1.0, (int)x - 128);"),
+    "mx_b_scale_dropped": ("dec[B[j * ldb + k]] * scale[SB[j * ldsb + k / 32]]", "dec[B[j * ldb + k]]"),
+    "mx_a_scale_first_group_only": ("scale[SA[i * ldsa + k / 32]]", "scale[SA[i * ldsa]]"),
+    "mx_a_scale_unpadded_stride": ("scale[SA[i * ldsa + k / 32]]", "scale[SA[i * (K / 32) + k / 32]]"),
+    "mx_scale_linear": ("scale[c] = oracle_ue8m0_to_double((uint8_t)c);", "scale[c] = (double)c;"),
+    "mx_nan_ignored": ("if (x == 255) return NAN;", "if (x == 255) return 0.0;"),
 }
 
 
