@@ -33,7 +33,8 @@ STATUS_NAMES = {
 EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_workspace_size",
            "gemm_run_no_alloc", "gemm_status_string", "gemm_plan", "gemm_tile_origin",
            "gemm_device_status", "gemm_selftest_wait_timeout", "gemm_fp8_abt", "gemm_fp8_run",
-           "gemm_fp8_run_workspace")
+           "gemm_fp8_run_workspace", "gemm_mx_abt", "gemm_mx_run", "gemm_mx_scales_size",
+           "gemm_mx_pack_scales", "gemm_mx_plan")
 
 
 class GemmError(RuntimeError):
@@ -70,6 +71,7 @@ def load(path: str | None = None):
             "`python -c 'import __graft_entry__ as g; g.build()'`")
     lib = ctypes.CDLL(p)
     vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    ip = ctypes.POINTER(c_int)
     for name in ("gemm_abt", "gemm_ab"):
         f = getattr(lib, name)
         f.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, vp]
@@ -95,9 +97,21 @@ def load(path: str | None = None):
     lib.gemm_fp8_run_workspace.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
                                            f32, ctypes.POINTER(GemmOptions), vp, ctypes.c_size_t, vp]
     lib.gemm_fp8_run_workspace.restype = c_int
+    lib.gemm_mx_abt.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                f32, vp]
+    lib.gemm_mx_abt.restype = c_int
+    lib.gemm_mx_run.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                f32, ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_mx_run.restype = c_int
+    lib.gemm_mx_scales_size.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.gemm_mx_scales_size.restype = c_int
+    lib.gemm_mx_pack_scales.argtypes = [vp, i64, i64, i64, vp, vp]
+    lib.gemm_mx_pack_scales.restype = c_int
+    lib.gemm_mx_plan.argtypes = [i64, i64, i64, c_int, ctypes.POINTER(GemmOptions), ip, ip, ip,
+                                 ip, ip, ctypes.POINTER(i64)]
+    lib.gemm_mx_plan.restype = c_int
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
-    ip = ctypes.POINTER(c_int)
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions), ip, ip,
                               ip, ip, ip, ctypes.POINTER(i64), ip]
     lib.gemm_plan.restype = c_int
@@ -342,6 +356,89 @@ def gemm_run_ptr(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: 
                                          _options(options), workspace, workspace_bytes, stream)
     return load().gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, layout, _options(options),
                            stream)
+
+
+def mx_scales_size(rows: int, K: int) -> int:
+    """Bytes of the tiled block scales of a rows x K FP8 operand."""
+    n = ctypes.c_size_t()
+    st = load().gemm_mx_scales_size(int(rows), int(K), ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "gemm_mx_scales_size")
+    return n.value
+
+
+def mx_pack_scales(S, K: int, out=None, *, stream=None):
+    """Tiled block scales (the layout gemm_mx reads) from row-major ones: S is a
+    CUDA uint8 tensor (rows, ceil(K / 32)) of UE8M0 bytes (row stride free,
+    inner stride 1).  Returns a uint8 tensor of mx_scales_size(rows, K) bytes."""
+    import torch
+
+    if S.device.type != "cuda" or S.dtype != torch.uint8 or S.dim() != 2:
+        raise GemmError(-2, "scales: a 2-D uint8 CUDA tensor")
+    rows, groups = S.shape
+    if groups != (int(K) + 31) // 32:
+        raise GemmError(-3, f"scales have {groups} groups per row; K = {K} needs {(K + 31) // 32}")
+    nbytes = mx_scales_size(rows, K)
+    if out is None:
+        out = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=S.device)
+    elif out.numel() * out.element_size() < nbytes or out.device != S.device:
+        raise GemmError(-3, "out is too small or on another device")
+    ld = int(S.stride(0)) if rows > 1 else max(groups, 1)
+    if rows > 0 and groups > 1 and S.stride(1) != 1:
+        raise GemmError(-3, "scales: inner dimension must be contiguous")
+    st = load().gemm_mx_pack_scales(S.data_ptr(), rows, int(K), ld, out.data_ptr(),
+                                    _stream_handle(stream, S.device))
+    if st != 0:
+        raise GemmError(st, "gemm_mx_pack_scales")
+    return out
+
+
+def gemm_mx(A, B, SA, SB, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0,
+            options=None, stream=None):
+    """Block-scaled FP8: D[i, j] = alpha * sum_k (A[i, k] sa) (B[j, k] sb), one UE8M0
+    scale per 32 K elements of each row.  A (M, K) and B (N, K) as for gemm_fp8;
+    SA / SB the tiled scales (mx_pack_scales output, uint8 CUDA tensors)."""
+    import torch
+
+    for t in (A, B, SA, SB):
+        if t.device.type != "cuda":
+            raise GemmError(-1, "operands must be CUDA tensors")
+    code = _fp8_code(A, fmt)
+    if _fp8_code(B, fmt) != code:
+        raise GemmError(-2, "A and B must share an FP8 format")
+    M, K = A.shape
+    N, Kb = B.shape
+    if Kb != K:
+        raise GemmError(-3, f"K mismatch ({K} vs {Kb})")
+    for t, rows in ((SA, M), (SB, N)):
+        if t.dtype != torch.uint8 or t.numel() < mx_scales_size(rows, K):
+            raise GemmError(-3, "scales: uint8 tensors of mx_scales_size(rows, K) bytes")
+    odt = out_dtype if out_dtype is not None else (D.dtype if D is not None else torch.bfloat16)
+    if D is None:
+        D = torch.empty((M, N), dtype=odt, device=A.device)
+    elif D.dtype != odt or tuple(D.shape) != (M, N):
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    st = load().gemm_mx_run(A.data_ptr(), B.data_ptr(), SA.data_ptr(), SB.data_ptr(),
+                            D.data_ptr(), M, N, K, _ld(A, 16), _ld(B, 16), _ld(D), code,
+                            _dtype_code(D), float(alpha), _options(options),
+                            _stream_handle(stream, A.device))
+    if st != 0:
+        raise GemmError(st, "gemm_mx_run")
+    return D
+
+
+def gemm_mx_plan(M: int, N: int, K: int, in_format: int = GEMM_E4M3, options=None) -> dict:
+    """The tile shape and persistent grid gemm_mx would use on the current device."""
+    vals = [ctypes.c_int() for _ in range(5)]
+    tiles = ctypes.c_int64()
+    st = load().gemm_mx_plan(M, N, K, in_format, _options(options),
+                             *[ctypes.byref(v) for v in vals], ctypes.byref(tiles))
+    if st != 0:
+        raise GemmError(st, "gemm_mx_plan")
+    keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
+    out = {k: v.value for k, v in zip(keys, vals)}
+    out["num_tiles"] = tiles.value
+    return out
 
 
 def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOUT_ABT,

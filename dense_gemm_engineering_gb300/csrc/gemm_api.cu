@@ -62,6 +62,25 @@ bool encode_2d(CUtensorMap* map, const void* ptr, int fmt, uint64_t inner, uint6
            CUDA_SUCCESS;
 }
 
+// Block scales (MX) of a rows x K FP8 operand, in the tiled layout of
+// include/gemm.h: ceil(rows / 128) x ceil(K / 128) atoms of 512 bytes, atom
+// (rb, kc) at byte (rb * ceil(K / 128) + kc) * 512.  Seen as a 2-D tensor of
+// 32-bit words: ceil(K / 128) * 128 words per 128-row block, one block per row;
+// boxes of one atom (128 words) x box_atoms consecutive row blocks, no
+// swizzle, zero fill past the last block.
+bool encode_scales(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_atoms) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t kc = (K + 127) / 128, rb = (rows + 127) / 128;
+    const cuuint64_t dims[2] = {kc * 128, rb};
+    const cuuint64_t strides[1] = {kc * 512};
+    const cuuint32_t box[2] = {128, box_atoms};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- per-device facts, cached -------------------------------------------------
 
 struct DeviceInfo {
@@ -110,13 +129,16 @@ cudaError_t ensure_smem_attribute() {
     return e;
 }
 
+// `msa` / `msb`: the scale maps of a block-scaled (MX) variant; other
+// variants ignore them (any valid map may be passed).
 template <class C>
 void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                    const GemmArgs& args, int clusters, cudaStream_t stream, cudaError_t* err) {
+                    const GemmArgs& args, const CUtensorMap& msa, const CUtensorMap& msb,
+                    int clusters, cudaStream_t stream, cudaError_t* err) {
     if ((*err = ensure_smem_attribute<C>()) != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(clusters * C::CLUSTER), 1, 1);
-    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.blockDim = dim3(unsigned(C::THREADS), 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -126,7 +148,7 @@ void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args);
+    *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args, msa, msb);
 }
 
 // Co-resident clusters for a variant on the current device (queried once).
@@ -136,7 +158,7 @@ int query_max_clusters(int dev, int sm_count) {
     if (ensure_smem_attribute<C>() != cudaSuccess) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(C::CLUSTER * (sm_count / C::CLUSTER)), 1, 1);
-    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.blockDim = dim3(unsigned(C::THREADS), 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -167,6 +189,14 @@ struct Stages {
 
 template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1, int F8 = 0>
 using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC, F8>;
+
+// Block-scaled FP8 (MX) stages: a stage also holds 2 KiB of scales as loaded
+// and 4 KiB of realigned B scales; 5 stages of 2-CTA 224-wide tiles.
+constexpr int stages_for_mx(int cg, int bn) {
+    return (227 * 1024 - 32768 - 1024 - 512) / (128 * 128 + (bn / cg) * 128 + 2048 + 4096);
+}
+template <int CG, int BN, bool BF16, int F8>
+using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, 1, F8, true>;
 
 struct Plan {
     int cg, bm, bn, stages;
@@ -240,7 +270,7 @@ std::atomic<uint32_t> g_epoch{0};
 template <class C>
 int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
              int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha,
-             void* workspace, cudaStream_t stream) {
+             void* workspace, cudaStream_t stream, const void* SA, const void* SB) {
     CUtensorMap ma, mb, md;
     if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_BOX_ROWS))
         return GEMM_ERR_CUDA;
@@ -274,8 +304,19 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
         args.counters = reinterpret_cast<unsigned long long*>(ws);
         args.partials = reinterpret_cast<float*>(ws + ((p.ws_counter_bytes + 255u) & ~size_t(255)));
     }
+    // Scale maps: one A atom (this CTA's 128 rows) and three B atoms (the tile's
+    // 224 columns from the 128-row block holding its first) per k-block.
+    CUtensorMap msa = ma, msb = ma;
+    if constexpr (C::MX) {
+        if (!encode_scales(&msa, SA, uint64_t(M), uint64_t(K), 1) ||
+            !encode_scales(&msb, SB, uint64_t(N), uint64_t(K), 3))
+            return GEMM_ERR_CUDA;
+    } else {
+        (void)SA;
+        (void)SB;
+    }
     cudaError_t err;
-    launch_variant<C>(ma, mb, md, args, p.clusters, stream, &err);
+    launch_variant<C>(ma, mb, md, args, msa, msb, p.clusters, stream, &err);
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -339,6 +380,21 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, int f8, Ts&
     return GEMM_ERR_OPTION;
 }
 
+// Block-scaled FP8 (MX) variants: 2-CTA 224-wide tiles, E4M3 / E5M2 inputs,
+// FP16 / BF16 output.
+template <template <class> class Fn, class... Ts>
+int dispatch_mx(int cg, int bn, bool bf16, int f8, Ts&&... ts) {
+#define GB300_CASEMX(F8_, BF_)                                                           \
+    if (cg == 2 && bn == 224 && f8 == F8_ && bf16 == BF_)                                \
+        return Fn<CfgMX<2, 224, BF_, F8_>>::call(std::forward<Ts>(ts)...);
+    GB300_CASEMX(1, false)
+    GB300_CASEMX(1, true)
+    GB300_CASEMX(2, false)
+    GB300_CASEMX(2, true)
+#undef GB300_CASEMX
+    return GEMM_ERR_OPTION;
+}
+
 template <class C>
 struct QueryFn {
     static int call(int dev, int sms, int* out) {
@@ -358,9 +414,10 @@ template <class C>
 struct RunFn {
     static int call(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N,
                     int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype,
-                    float alpha, void* workspace, cudaStream_t stream) {
+                    float alpha, void* workspace, cudaStream_t stream, const void* SA,
+                    const void* SB) {
         return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace,
-                           stream);
+                           stream, SA, SB);
     }
 };
 
@@ -436,12 +493,38 @@ int choose_block_n(int64_t M, int64_t N, int bm, int b_layout, int cg, int dtype
 // Choose the tile shape and grid.  Needs the current device (for its SM count
 // and cluster occupancy).
 int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const gemm_options_t* o,
-              bool have_workspace, Plan* p) {
+              bool have_workspace, Plan* p, bool mx = false) {
     DeviceInfo di;
     int st = current_device(&di);
     if (st != GEMM_OK) return st;
     int dev = 0;
     cudaGetDevice(&dev);
+    if (mx) {
+        // Block-scaled FP8: 2-CTA clusters, 224-wide tiles, whole tiles only.
+        if (!is_fp8(dtype) || b_layout != 0) return GEMM_ERR_DTYPE;
+        if (o && ((o->cta_group && o->cta_group != 2) || (o->block_n && o->block_n != 224) ||
+                  o->consumers > 1 || o->multicast > 1 || o->tail_split > 1))
+            return GEMM_ERR_OPTION;
+        p->mc = 1;
+        p->cg = 2;
+        p->cons = 1;
+        p->bm = 256;
+        p->bn = 224;
+        p->group = (o && o->raster_group) ? o->raster_group : 16;
+        const int64_t m_tiles = (M + p->bm - 1) / p->bm;
+        p->tiles = m_tiles * ((N + p->bn - 1) / p->bn);
+        if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
+        if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
+        int max_clusters = 0;
+        st = dispatch_mx<QueryFn>(p->cg, p->bn, false, f8_code(dtype), dev, di.sm_count, &max_clusters);
+        if (st != GEMM_OK) return st;
+        if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
+        p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
+        p->stages = stages_for_mx(p->cg, p->bn);
+        p->k_blocks = (K + kBlockK8 - 1) / kBlockK8;
+        plan_split(p, 0, false);
+        return GEMM_OK;
+    }
     p->mc = (o && o->multicast) ? o->multicast : 1;
     p->cg = (o && o->cta_group) ? o->cta_group : ((M <= 128 && p->mc == 1) ? 1 : 2);
     p->cons = (o && o->consumers) ? o->consumers : 1;
@@ -501,10 +584,16 @@ namespace {
 
 // Shared body of the 16-bit and FP8 entry points.  in_fmt: GEMM_F16 /
 // GEMM_BF16 (then out_dtype == in_fmt) or GEMM_E4M3 / GEMM_E5M2 (A.Bt only).
+// Bytes of the tiled block scales (MX) of a rows x K FP8 operand.
+int64_t mx_scale_bytes(int64_t rows, int64_t K) {
+    return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
+
 int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
              int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha, int b_layout,
              const gemm_options_t* opts, void* workspace, size_t workspace_bytes,
-             cudaStream_t stream) {
+             cudaStream_t stream, const void* SA = nullptr, const void* SB = nullptr,
+             bool mx = false) {
     int st = check_sizes(M, N, K, in_fmt, b_layout);
     if (st != GEMM_OK) return st;
     if (out_dtype != GEMM_F16 && out_dtype != GEMM_BF16) return GEMM_ERR_DTYPE;
@@ -525,6 +614,14 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
     if (K > 0 && (overlaps(D, M, N, ldd, 2, A, M, K, lda, esize) ||
                   overlaps(D, M, N, ldd, 2, B, b_rows, b_cols, ldb, esize)))
         return GEMM_ERR_ALIAS;
+    if (mx && K > 0) {
+        if (!SA || !SB) return GEMM_ERR_NULL;
+        if ((reinterpret_cast<uintptr_t>(SA) & 15u) || (reinterpret_cast<uintptr_t>(SB) & 15u))
+            return GEMM_ERR_ALIGN;
+        const int64_t sa = mx_scale_bytes(M, K), sb = mx_scale_bytes(N, K);
+        if (overlaps(D, M, N, ldd, 2, SA, 1, sa, sa, 1) || overlaps(D, M, N, ldd, 2, SB, 1, sb, sb, 1))
+            return GEMM_ERR_ALIAS;
+    }
 
     if (K == 0) {
         DeviceInfo di;
@@ -538,12 +635,17 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
 
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GEMM_ERR_WORKSPACE;
     Plan p;
-    if ((st = make_plan(M, N, K, in_fmt, b_layout, opts, workspace != nullptr, &p)) != GEMM_OK)
+    if ((st = make_plan(M, N, K, in_fmt, b_layout, opts, workspace != nullptr, &p, mx)) != GEMM_OK)
         return st;
     if (workspace_bytes < workspace_bytes_needed(p)) return GEMM_ERR_WORKSPACE;
+    if (mx)
+        return dispatch_mx<RunFn>(p.cg, p.bn, out_dtype == GEMM_BF16, f8_code(in_fmt), p, A, B, D, M,
+                                  N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace, stream,
+                                  SA, SB);
     return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, p.mc,
                            f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
-                           alpha, workspace, stream);
+                           alpha, workspace, stream, static_cast<const void*>(nullptr),
+                           static_cast<const void*>(nullptr));
 }
 
 }  // namespace
@@ -580,6 +682,69 @@ extern "C" int gemm_fp8_abt(const void* A, const void* B, void* D, int64_t M, in
                             float alpha, cudaStream_t stream) {
     return gemm_fp8_run(A, B, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha, nullptr,
                         stream);
+}
+
+extern "C" int gemm_mx_run(const void* A, const void* B, const void* SA, const void* SB, void* D,
+                           int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                           int in_format, int out_dtype, float alpha, const gemm_options_t* opts,
+                           cudaStream_t stream) {
+    if (!is_fp8(in_format)) return GEMM_ERR_DTYPE;
+    return run_impl(A, B, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha, 0, opts, nullptr,
+                    0, stream, SA, SB, true);
+}
+
+extern "C" int gemm_mx_abt(const void* A, const void* B, const void* SA, const void* SB, void* D,
+                           int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                           int in_format, int out_dtype, float alpha, cudaStream_t stream) {
+    return gemm_mx_run(A, B, SA, SB, D, M, N, K, lda, ldb, ldd, in_format, out_dtype, alpha, nullptr,
+                       stream);
+}
+
+extern "C" int gemm_mx_scales_size(int64_t rows, int64_t K, size_t* bytes) {
+    if (!bytes) return GEMM_ERR_NULL;
+    if (rows < 0 || K < 0 || rows > INT32_MAX || K > INT32_MAX) return GEMM_ERR_SHAPE;
+    *bytes = size_t(mx_scale_bytes(rows, K));
+    return GEMM_OK;
+}
+
+extern "C" int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst,
+                                   cudaStream_t stream) {
+    if (rows < 0 || K < 0 || rows > INT32_MAX || K > INT32_MAX) return GEMM_ERR_SHAPE;
+    const int64_t groups = (K + 31) / 32;
+    const int64_t bytes = mx_scale_bytes(rows, K);
+    if (bytes == 0) return GEMM_OK;
+    if (!src || !dst) return GEMM_ERR_NULL;
+    if (ld < groups || ld <= 0) return GEMM_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(dst) & 15u) return GEMM_ERR_ALIGN;
+    if (overlaps(dst, 1, bytes, bytes, 1, src, rows, groups, ld, 1)) return GEMM_ERR_ALIAS;
+    DeviceInfo di;
+    const int st = current_device(&di);
+    if (st != GEMM_OK) return st;
+    const int64_t words = bytes / 4;
+    int64_t blocks = (words + 255) / 256;
+    if (blocks > 8L * di.sm_count) blocks = 8L * di.sm_count;
+    mx_pack_scales_kernel<<<unsigned(blocks), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), rows, groups, ld, (K + 127) / 128, static_cast<uint32_t*>(dst),
+        words);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+extern "C" int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,
+                            int* cta_group, int* block_m, int* block_n, int* stages,
+                            int* num_clusters, int64_t* num_tiles) {
+    if (!is_fp8(in_format)) return GEMM_ERR_DTYPE;
+    int st = check_sizes(M, N, K, in_format, 0);
+    if (st != GEMM_OK) return st;
+    if ((st = check_options(opts)) != GEMM_OK) return st;
+    Plan p;
+    if ((st = make_plan(M, N, K, in_format, 0, opts, false, &p, true)) != GEMM_OK) return st;
+    if (cta_group) *cta_group = p.cg;
+    if (block_m) *block_m = p.bm;
+    if (block_n) *block_n = p.bn;
+    if (stages) *stages = p.stages;
+    if (num_clusters) *num_clusters = p.clusters;
+    if (num_tiles) *num_tiles = p.tiles;
+    return GEMM_OK;
 }
 
 extern "C" int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,

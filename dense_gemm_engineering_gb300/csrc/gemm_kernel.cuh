@@ -68,11 +68,12 @@ enum : uint32_t {
     kRoleMma = 2u,
     kRoleEpilogue = 3u,
     kRoleDrain = 4u,
-    kRoleSelfTest = 5u
+    kRoleSelfTest = 5u,
+    kRoleScales = 6u
 };
 
 template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1,
-          int F8_ = 0>
+          int F8_ = 0, bool MX_ = false>
 struct KernelConfig {
     static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
     // CTA pairs per cluster: 1, or 2 side by side along N that share A — each
@@ -96,6 +97,16 @@ struct KernelConfig {
     static constexpr int ELEM_BYTES = F8 ? 1 : 2;
     static constexpr int MMA_K = F8 ? 32 : 16;         // K per MMA: 32 bytes either way
     static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
+    // Block-scaled FP8 (MX): one UE8M0 scale per 32 K elements of every row of A
+    // and of B, multiplied on tcgen05.mma kind::mxf8f6f4.block_scale.  A seventh
+    // warp realigns each stage's B scales for the tile (see the scale warp).
+    static constexpr bool MX = MX_;
+    static constexpr int THREADS = MX ? kNumThreads + 32 : kNumThreads;
+    // MX shared memory per stage: the scale atoms as loaded (512 B of A scales
+    // for this CTA's 128 rows, then three 512 B atoms of B scales covering the
+    // tile's columns) and the tile's B scales realigned (128 rows x 32 B).
+    static constexpr uint32_t SF_IN_BYTES = MX ? 2048u : 0u;
+    static constexpr uint32_t SFB_OUT_BYTES = MX ? 4096u : 0u;
 
     static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * BK * ELEM_BYTES;  // 16 KiB per consumer
     static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * BK * ELEM_BYTES;
@@ -118,10 +129,13 @@ struct KernelConfig {
 
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SF_IN = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB_OUT = OFF_SF_IN + STAGES * SF_IN_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_SFB_OUT + STAGES * SFB_OUT_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * 2u * EPI_BUF_BYTES;
-    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue warp
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps;
+    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue
+    // warp, and (MX) scales_loaded[STAGES]
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + (MX ? STAGES : 0u);
     // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
     // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
     // (32 rows x 64 FP32 columns).
@@ -144,6 +158,17 @@ struct KernelConfig {
     static constexpr uint32_t IDESC = (1u << 4) | (AB_TYPE << 7) | (AB_TYPE << 10) |
                                       ((B_MN ? 1u : 0u) << 16) | (uint32_t(BN >> 3) << 17) |
                                       (uint32_t(MMA_M >> 4) << 24);
+    // Block-scaled (kind::mxf8f6f4) descriptor: no D-type field (D is F32);
+    // bits 4-5 and 29-30 carry the B and A scale ids (the byte of each 32-bit
+    // TMEM scale cell: the 32-element K group within the k-block), added per
+    // MMA; bit 23 = 1 selects UE8M0 scales.
+    static constexpr uint32_t IDESC_MX = (AB_TYPE << 7) | (AB_TYPE << 10) | (uint32_t(BN >> 3) << 17) |
+                                         (1u << 23) | (uint32_t(MMA_M >> 4) << 24);
+    // MX scale factors in TMEM: two buffers, each in the 32 columns after one
+    // accumulator's 224: buffer b holds the A scales at column 256 b + 224 (4
+    // columns) and the B scales at 256 b + 240 (8 columns); every scale address
+    // is a multiple of 16 columns.
+    static constexpr uint32_t SF_COL = 224u;
     static_assert(F8 == 0 || F8 == 1 || F8 == 2, "FP8 input: none, E4M3 or E5M2");
     static_assert(!(F8 && B_MN), "FP8 operands are K-major (A.Bt only)");
     static_assert(BK * ELEM_BYTES == 128 && MMA_K * ELEM_BYTES == 32,
@@ -166,6 +191,9 @@ struct KernelConfig {
                   "the last unit's epilogue chunks fit in each warp's share of the ring");
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
+    static_assert(!MX || (F8 && BN == 224 && CONS == 1 && MC == 1 && !B_MN && ACC_STRIDE == 256 &&
+                          NUM_ACC == 2 && BK == 128),
+                  "MX: FP8 A.Bt, 224-wide tiles (224 accumulator + 32 scale columns per buffer)");
     static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
 };
 
@@ -240,6 +268,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
+// tcgen05 shared-memory descriptor without swizzling (the scale-factor
+// copies): core matrices of 8 rows x 16 B stored contiguously; LBO = byte
+// distance between the two 16-byte halves of a 32-byte row, SBO = byte
+// distance between groups of 8 rows.
+__device__ __forceinline__ uint64_t noswizzle_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = uint64_t((addr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;
+    return d;
+}
+
 __device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint32_t role) {
     *abort_flag = 1u;
     atomicCAS(&g_gemm_status, 0u, kReasonTimeout | (role << 8));
@@ -298,10 +338,12 @@ __device__ __forceinline__ uint32_t count_range_done(unsigned long long* word, u
 }
 
 template <class C>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args,
+                        const __grid_constant__ CUtensorMap tmap_sa,
+                        const __grid_constant__ CUtensorMap tmap_sb) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -325,14 +367,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
     };
     auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
+    auto scales_bar = [&](uint32_t s) {
+        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + s);
+    };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
 
     // ---- one-time setup -------------------------------------------------
     if (warp == 0 && lane == 0) {
         for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
-            ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
+            // the leader's expect_tx arrival (MX: and each CTA's scale warp)
+            ptx::mbar_init(full_bar(s), C::MX ? 1u + uint32_t(C::CG) : 1u);
             ptx::mbar_init(empty_bar(s), uint32_t(C::MC));  // one tcgen05.commit per pair
+            if constexpr (C::MX) ptx::mbar_init(scales_bar(s), 1);  // expect_tx arrival
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
@@ -344,6 +391,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_d);
+        if constexpr (C::MX) {
+            ptx::prefetch_tensormap(&tmap_sa);
+            ptx::prefetch_tensormap(&tmap_sb);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc<C::CG>(base + C::OFF_TMEM_SLOT, C::TMEM_COLS);
@@ -414,6 +465,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                       b_row + 64 * c, k0);
                         }
                     }
+                    if constexpr (C::MX) {
+                        // Scales of k-block kb (one 512-byte atom = 128 rows x 4 groups
+                        // per 128-row block), into this CTA's shared memory, completing
+                        // on this CTA's scales barrier: the A atom of this CTA's rows
+                        // and the three B atoms from the one holding the tile's first
+                        // column (TMA fills atoms past the last with zeros).
+                        const uint32_t sf_dst = base + C::OFF_SF_IN + s * C::SF_IN_BYTES;
+                        ptx::mbar_arrive_expect_tx(scales_bar(s), C::SF_IN_BYTES);
+                        ptx::tma_load_2d(sf_dst, &tmap_sa, scales_bar(s), kb * 128, a_row / 128);
+                        ptx::tma_load_2d(sf_dst + 512u, &tmap_sb, scales_bar(s), kb * 128,
+                                         (nt * C::BN) / 128);
+                    }
                 }
                 __syncwarp();
                 if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
@@ -436,6 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // ---- MMA issuer (leader CTA) ------------------------------------------
         if (leader) {
             uint32_t s = 0, ph = 0, ab = 0, aph = 0;
+            uint32_t sfbuf = 0;  // MX: TMEM scale buffer of the next k-block
             bool ok = true;
             for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
                 const WorkUnit w = unit_of(args, u);
@@ -453,7 +517,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t a_addr = base + C::OFF_A + s * C::A_BYTES;
                     const uint32_t b_addr = base + C::OFF_B + s * C::B_BYTES;
+                    const uint32_t sf_t = tmem_base + (sfbuf << 8) + C::SF_COL;
                     if (ptx::elect_one_sync()) {
+                        if constexpr (C::MX) {
+                            // This k-block's scales into TMEM (each CTA of the pair
+                            // from its own shared memory): A's atom as loaded, B's
+                            // as realigned by the scale warp.  Ordered before the
+                            // MMAs below, which read them.
+                            ptx::tmem_cp_32x128b_warpx4<C::CG>(
+                                sf_t, noswizzle_desc(base + C::OFF_SF_IN + s * C::SF_IN_BYTES, 128u, 128u));
+                            ptx::tmem_cp_128x256b<C::CG>(
+                                sf_t + 16u,
+                                noswizzle_desc(base + C::OFF_SFB_OUT + s * C::SFB_OUT_BYTES, 128u, 256u));
+                        }
 #pragma unroll
                         for (int k = 0; k < C::BK / C::MMA_K; ++k) {
                             const uint64_t bd = C::B_MN
@@ -464,7 +540,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 // consumer h: A rows 128h..128h+127 of this stage (16 KiB each)
                                 const uint64_t ad = sw128_desc(a_addr + 16384u * h + 32u * k, 16u, 1024u);
                                 const uint32_t acc = uint32_t(kb != w.kb0 || k != 0);
-                                if constexpr (C::F8)
+                                if constexpr (C::MX)
+                                    ptx::mma_mxf8f6f4<C::CG>(d_tmem, ad, bd,
+                                                             C::IDESC_MX | (uint32_t(k) << 4) | (uint32_t(k) << 29),
+                                                             sf_t, sf_t + 16u, acc);
+                                else if constexpr (C::F8)
                                     ptx::mma_f8f6f4<C::CG>(d_tmem + uint32_t(h) * C::ACC_STRIDE, ad, bd,
                                                            C::IDESC, acc);
                                 else
@@ -476,6 +556,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::mma_commit<C::CG>(empty_bar(s), uint16_t((1u << C::CLUSTER) - 1u));
                     }
                     __syncwarp();
+                    sfbuf ^= 1u;
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -500,6 +581,63 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok) settle_after_abort();
         }
         __syncwarp();
+    } else if (C::MX && warp == 2u + kEpilogueWarps) {
+        // ---- scale warp (MX) -------------------------------------------------
+        // The MMA reads the B scale of tile column n at TMEM column sfb + n/32,
+        // and a scale address must be a multiple of 16 columns, so column group
+        // 0 of the tile must start a buffer.  A tile of 224 columns starts at
+        // column group (n0 / 32) mod 4 of the first 512-byte atom loaded, so
+        // this warp shifts each stage's B scales down by that many 4-byte cells
+        // into the layout of a 128 x 256-bit TMEM copy (row r = 8 column groups
+        // of lane r % 32; the four lane quarters hold the same rows), then
+        // marks the stage full for the MMA issuer.
+        if constexpr (C::MX) {
+            uint32_t s = 0, ph = 0;
+            bool ok = true;
+            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
+                const WorkUnit w = unit_of(args, u);
+                int32_t mt, nt;
+                tile_of_task(args.grid, w.tile, mt, nt);
+                const uint32_t shift = uint32_t((nt * C::BN) / 32) & 3u;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bounded_warp(scales_bar(s), ph, abort_flag, kRoleScales)) {
+                        ok = false;
+                        break;
+                    }
+                    // lane l: row l of the three loaded B atoms = column groups 0..11
+                    const uint32_t in = base + C::OFF_SF_IN + s * C::SF_IN_BYTES + 512u + lane * 16u;
+                    const uint4 q0 = ptx::ld_shared_v4_u32(in);
+                    const uint4 q1 = ptx::ld_shared_v4_u32(in + 512u);
+                    const uint4 q2 = ptx::ld_shared_v4_u32(in + 1024u);
+                    const uint32_t g[11] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y,
+                                            q1.z, q1.w, q2.x, q2.y, q2.z};
+                    uint32_t r[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        r[j] = shift == 0u ? g[j] : shift == 1u ? g[j + 1] : shift == 2u ? g[j + 2] : g[j + 3];
+                    const uint32_t out = base + C::OFF_SFB_OUT + s * C::SFB_OUT_BYTES;
+#pragma unroll
+                    for (uint32_t q = 0; q < 4; ++q) {
+                        const uint32_t row = lane + 32u * q;
+                        const uint32_t addr = out + (row / 8u) * 256u + (row % 8u) * 16u;
+                        ptx::st_shared_v4(addr, r[0], r[1], r[2], r[3]);
+                        ptx::st_shared_v4(addr + 128u, r[4], r[5], r[6], r[7]);
+                    }
+                    ptx::fence_proxy_async_smem();  // visible to the tensor core's copy
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (C::CG == 2)
+                            ptx::mbar_arrive_cluster(ptx::map_to_rank(full_bar(s), pair_leader));
+                        else
+                            ptx::mbar_arrive(full_bar(s));
+                    }
+                    __syncwarp();
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) settle_after_abort();
+            __syncwarp();
+        }
     } else {
         // ---- epilogue warps 2..5 ----------------------------------------------
         const uint32_t quarter = warp & 3u;  // this warp may read TMEM lanes 32q..32q+31
@@ -810,7 +948,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // CTA's shared memory and arrives on its barriers); TMEM is freed after
     // every warp's last TMEM read.
     if constexpr (C::CLUSTER > 1) {
-        if (warp < 2) {
+        if (warp < 2 || warp >= 2u + kEpilogueWarps) {  // the epilogue warps arrived already
             ptx::tc_fence_before();
             ptx::cluster_arrive();
         }
@@ -836,6 +974,32 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
         ptx::mbar_init(ptx::smem_addr(&bar), 1);
         ptx::fence_mbar_init();
         wait_bounded(ptx::smem_addr(&bar), 0u, &abort_flag, kRoleSelfTest, limit_ns);
+    }
+}
+
+// Block scales (MX) from row-major bytes (rows x groups, row stride ld,
+// groups = ceil(K / 32)) to the tiled layout the GEMM loads: ceil(rows / 128)
+// x kchunks atoms of 512 bytes (kchunks = ceil(K / 128)), atom (rb, kc) at byte
+// (rb * kchunks + kc) * 512; inside it the scale of row rb * 128 + r, group
+// kc * 4 + g sits at byte (r % 32) * 16 + (r / 32) * 4 + g.  Rows and groups
+// past the ends get 127 (a scale of 1).  One thread per 32-bit word (the four
+// groups of one row in one atom): word w of an atom is row (w % 4) * 32 + w / 4.
+__global__ void mx_pack_scales_kernel(const uint8_t* __restrict__ src, int64_t rows,
+                                      int64_t groups, int64_t ld, int64_t kchunks,
+                                      uint32_t* __restrict__ dst, int64_t words) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t atom = i / 128;
+        const int64_t w = i % 128;
+        const int64_t row = (atom / kchunks) * 128 + (w % 4) * 32 + w / 4;
+        const int64_t g0 = (atom % kchunks) * 4;
+        uint32_t v = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t b = (row < rows && g0 + g < groups) ? src[row * ld + g0 + g] : 127u;
+            v |= b << (8 * g);
+        }
+        dst[i] = v;
     }
 }
 

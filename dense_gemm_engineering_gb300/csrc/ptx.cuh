@@ -291,6 +291,57 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
             : "memory");
 }
 
+// Block-scaled FP8 MMA (kind::mxf8f6f4, one UE8M0 scale per 32 K elements of
+// each row of A and of each column of D): D(tmem) (+)= (A . sa) . (B . sb)^T.
+// The scale bytes sit in TMEM: for A row m (of this CTA's 128) at lane m,
+// column sfa + m/32; for D column n at column sfb + n/32 of every lane quarter
+// (lane 32q + n%32 serves rows 32q..32q+31); the byte within each 32-bit cell
+// is the scale id in the instruction descriptor (bits 29-30 for A, 4-5 for B).
+// sfa / sfb must be multiples of 16 columns (a column offset of 1 raised a
+// misaligned-address fault).
+template <int CG>
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+}
+
+// Shared memory -> TMEM copies (asynchronous, ordered with this thread's later
+// tcgen05.mma; tcgen05.commit tracks them).  A CTA pair's leader copies each
+// CTA's own shared memory into that CTA's TMEM.
+// 32 rows x 16 bytes (rows 16 B apart) -> 4 columns, the same in all four lane
+// quarters: lane 32q + r, column c <- bytes 4c..4c+3 of row r.
+template <int CG>
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                     : "memory");
+}
+// 128 rows x 32 bytes -> 8 columns: lane r, column c <- bytes 4c..4c+3 of row r.
+template <int CG>
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued MMAs of this thread have
 // completed.  For a CTA pair the arrive goes to the barrier at the same offset
 // in every CTA of `cta_mask` (the pair itself by default).
@@ -339,6 +390,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     else
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4_u32(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

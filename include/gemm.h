@@ -196,6 +196,68 @@ int gemm_fp8_run_workspace(const void* A, const void* B, void* D, int64_t M, int
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Block-scaled FP8 GEMM (MX):
+ *
+ *   D[i,j] = alpha * sum_k (A[i,k] * 2^(sa[i][k/32] - 127)) * (B[j,k] * 2^(sb[j][k/32] - 127))
+ *
+ * A (M x K) and B (N x K) FP8 (in_format GEMM_E4M3 or GEMM_E5M2), row-major
+ * with ld in elements as for gemm_fp8_run; D 16-bit (out_dtype GEMM_F16 or
+ * GEMM_BF16).  "TIRx: A Unified Tile Primitive ML Compiler" (kernel
+ * performance) names FP8 block-scaled matrix multiplication, in which groups
+ * of input values share scale factors; the page fixes neither the group nor
+ * the scale encoding, and this library takes the OCP Microscaling (MX)
+ * reading that the tcgen05.mma kind::mxf8f6f4 instruction implements: every
+ * run of 32 consecutive K elements of a row of A and of a row of B shares one
+ * scale byte in the UE8M0 encoding (value 2^(x - 127); x = 255 is NaN).
+ * Products and scales are applied in the tensor core, the sum accumulates in
+ * FP32 in tensor memory, alpha multiplies it, and the result is rounded once
+ * (nearest even) to out_dtype.
+ *
+ * Scale layout.  SA (scales of A) and SB (scales of B) are device buffers in
+ * a tiled layout, gemm_mx_scales_size(rows, K) bytes each (rows = M for SA,
+ * N for SB), 16-byte aligned: ceil(rows / 128) x ceil(K / 128) atoms of 512
+ * bytes, atom (rb, kc) at byte offset (rb * ceil(K / 128) + kc) * 512; inside
+ * an atom the scale of row rb * 128 + r and K group kc * 4 + g (elements
+ * 32 (kc * 4 + g) .. +31) is the byte at (r % 32) * 16 + (r / 32) * 4 + g.
+ * Bytes for rows >= rows or groups >= ceil(K / 32) are padding: they must
+ * not be 255.  gemm_mx_pack_scales() writes this layout from plain row-major
+ * scales.  The caller owns SA and SB; neither may overlap D.
+ *
+ * Options: cta_group 0 or 2, block_n 0 or 224, raster_group and
+ * max_clusters as for gemm_run; consumers, multicast and tail_split 0 or 1
+ * (GEMM_ERR_OPTION otherwise).  Errors as gemm_fp8_run, plus GEMM_ERR_NULL
+ * for a null SA or SB and GEMM_ERR_ALIGN for a misaligned one (when K > 0).
+ * K = 0 writes zeros; M = 0 or N = 0 does nothing.  No library allocation.
+ */
+int gemm_mx_abt(const void* A, const void* B, const void* SA, const void* SB, void* D,
+                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                int in_format, int out_dtype, float alpha, cudaStream_t stream);
+int gemm_mx_run(const void* A, const void* B, const void* SA, const void* SB, void* D,
+                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                int in_format, int out_dtype, float alpha, const gemm_options_t* opts,
+                cudaStream_t stream);
+
+/* Bytes of the tiled scales of a rows x K operand:
+ * ceil(rows / 128) * ceil(K / 128) * 512 (written to *bytes). */
+int gemm_mx_scales_size(int64_t rows, int64_t K, size_t* bytes);
+
+/*
+ * Tiled scales (the layout above) from row-major ones: src is a device buffer
+ * of rows x ceil(K / 32) scale bytes with row stride ld bytes (ld >=
+ * ceil(K / 32)); dst (gemm_mx_scales_size(rows, K) bytes, 16-byte aligned,
+ * not overlapping src) receives the tiled layout, padding bytes set to 127.
+ * One kernel on `stream`, asynchronous.  Errors: GEMM_ERR_SHAPE, _NULL,
+ * _ALIGN, _ALIAS, _DEVICE, _CUDA.
+ */
+int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst,
+                        cudaStream_t stream);
+
+/* The plan gemm_mx_run would use (outputs as gemm_plan; may be NULL). */
+int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,
+                 int* cta_group, int* block_m, int* block_n, int* stages, int* num_clusters,
+                 int64_t* num_tiles);
+
+/*
  * Bytes of workspace gemm_run_workspace needs for these sizes and options on
  * the current device (written to *bytes; 0 = the call would not split).  At
  * most (co-resident clusters) x 256 KiB plus a few KiB of counters.

@@ -205,3 +205,53 @@ def test_fp8_types_are_rejected_by_the_16bit_entry_points(lib):
 
 def test_fp8_empty_output_is_a_no_op(lib):
     assert call8(M=0) == 0 and call8(N=0) == 0 and call8(M=0, A=0, B=0, D=0) == 0
+
+
+def call_mx(A=P, B=Q, SA=P, SB=Q, D=R, M=128, N=128, K=128, lda=128, ldb=128, ldd=128, fmt=2,
+            out=1, alpha=1.0, opts=None):
+    o = binding._options(opts)
+    return binding.load().gemm_mx_run(A, B, SA, SB, D, M, N, K, lda, ldb, ldd, fmt, out, alpha, o,
+                                      None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=0), -2),            # a 16-bit input type
+    (dict(fmt=1), -2),
+    (dict(out=3), -2),
+    (dict(M=-1), -3),
+    (dict(lda=64), -3),
+    (dict(lda=136), -4),
+    (dict(A=P + 8), -4),
+    (dict(D=P + 64), -5),         # D overlaps A
+    (dict(A=0), -1),
+    (dict(SA=0), -1),             # the scales are operands too
+    (dict(SB=0), -1),
+    (dict(SA=P + 4), -4),
+    (dict(SB=Q + 8), -4),
+])
+def test_mx_argument_errors(lib, kw, status):
+    assert call_mx(**kw) == status
+
+
+def test_mx_empty_output_and_empty_k(lib):
+    assert call_mx(M=0) == 0 and call_mx(N=0, SA=0, SB=0) == 0
+
+
+def test_mx_scales_size(lib):
+    n = binding.ctypes.c_size_t()
+    for rows, K, want in [(0, 128, 0), (1, 1, 512), (128, 128, 512), (129, 128, 1024),
+                          (300, 1000, 3 * 8 * 512), (8192, 8192, 64 * 64 * 512)]:
+        assert binding.load().gemm_mx_scales_size(rows, K, binding.ctypes.byref(n)) == 0
+        assert n.value == want == binding.mx_scales_size(rows, K)
+    assert binding.load().gemm_mx_scales_size(-1, 8, binding.ctypes.byref(n)) == -3
+    assert binding.load().gemm_mx_scales_size(8, 8, None) == -1
+
+
+def test_mx_pack_argument_errors(lib):
+    pack = binding.load().gemm_mx_pack_scales
+    assert pack(P, -1, 64, 2, Q, None) == -3
+    assert pack(P, 4, 64, 1, Q, None) == -3     # ld < ceil(K / 32)
+    assert pack(0, 4, 64, 2, Q, None) == -1
+    assert pack(P, 4, 64, 2, Q + 4, None) == -4
+    assert pack(P + 4, 4, 64, 2, P, None) == -5   # dst overlaps src
+    assert pack(P, 0, 64, 2, 0, None) == 0        # nothing to write
