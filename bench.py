@@ -274,8 +274,12 @@ def clock_sampler(uuid: str):
 
 
 def make_inputs(cfg):
+    """The workload's host inputs as numpy bit patterns: (A, B), or for the
+    block-scaled workloads (A, B, SA, SB) with row-major scale bytes."""
     from dense_gemm_engineering_gb300 import inputs
 
+    if cfg.mx:
+        return inputs.mx_operands(cfg.M, cfg.N, cfg.K, cfg.dtype, cfg.dist, cfg.seed)
     return inputs.operands(cfg.M, cfg.N, cfg.K, cfg.layout, cfg.dtype, cfg.dist, cfg.seed)
 
 
@@ -288,6 +292,8 @@ def metric_for(cfg) -> str:
         return METRIC
     names = {"f16": "FP16", "bf16": "BF16", "e4m3": "E4M3", "e5m2": "E5M2"}
     kind = f"{names[cfg.dtype]}->{names[cfg.out]}" if cfg.is_fp8 else names[cfg.dtype]
+    if cfg.mx:
+        kind = f"block-scaled MX {kind}"
     op = "A·Bᵀ" if cfg.layout == "abt" else "A·B"
     return f"GEMM TFLOP/s ({kind} {op}, {cfg.M}x{cfg.N}x{cfg.K})"
 
@@ -312,14 +318,37 @@ def operand(t, cfg):
 
 
 def gemm_for(cfg):
+    """gemm(xs, d): one GEMM through the public binding on device inputs xs =
+    [A, B] (block-scaled: [A, B, SA, SB] with the scales in the tiled layout)."""
     from dense_gemm_engineering_gb300 import binding
 
+    if cfg.mx:
+        return lambda xs, d: binding.gemm_mx(xs[0], xs[1], xs[2], xs[3], d, fmt=cfg.dtype,
+                                             alpha=cfg.alpha)
     if cfg.is_fp8:
-        return lambda a, b, d: binding.gemm_fp8(a, b, d, fmt=cfg.dtype, alpha=cfg.alpha)
-    return binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+        return lambda xs, d: binding.gemm_fp8(xs[0], xs[1], d, fmt=cfg.dtype, alpha=cfg.alpha)
+    f = binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+    return lambda xs, d: f(xs[0], xs[1], d)
 
 
-def oracle_rows(orc, cfg, A, B, rows):
+def device_inputs(cfg, dX, packed=None):
+    """Device storage tensors (as uploaded) -> the inputs the GEMM takes: the
+    16-bit views, and for block-scaled workloads the row-major scales packed
+    into the tiled layout (into `packed` buffers when given)."""
+    from dense_gemm_engineering_gb300 import binding
+
+    xs = [operand(dX[0], cfg), operand(dX[1], cfg)]
+    if cfg.mx:
+        xs += [binding.mx_pack_scales(dX[2], cfg.K, packed[0] if packed else None),
+               binding.mx_pack_scales(dX[3], cfg.K, packed[1] if packed else None)]
+    return xs
+
+
+def oracle_rows(orc, cfg, X, rows):
+    A, B = X[0], X[1]
+    if cfg.mx:
+        return orc.gemm_mx(A, B, X[2], X[3], fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha,
+                           rows=rows)
     if cfg.is_fp8:
         return orc.gemm_fp8(A, B, fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha, rows=rows)
     return orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=rows)
@@ -353,18 +382,18 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def oracle_sample(cfg, A, B, target_s: float):
+def oracle_sample(cfg, X, target_s: float):
     """Time the oracle on the first rows of D, sized to about target_s seconds."""
     import oracle
 
     orc = oracle.get()
     probe_rows = min(cfg.M, 8)
     t0 = time.perf_counter()
-    oracle_rows(orc, cfg, A, B, (0, probe_rows))
+    oracle_rows(orc, cfg, X, (0, probe_rows))
     t_probe = max(time.perf_counter() - t0, 1e-6)
     rows = max(probe_rows, min(cfg.M, int(target_s / (t_probe / probe_rows))))
     t0 = time.perf_counter()
-    oracle_rows(orc, cfg, A, B, (0, rows))
+    oracle_rows(orc, cfg, X, (0, rows))
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cfg.N * cfg.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
@@ -373,7 +402,7 @@ def oracle_sample(cfg, A, B, target_s: float):
                       f"{dt:.1f} s"}, rows, dt
 
 
-def oracle_single_core(cfg, A, B, rows: int = 64):
+def oracle_single_core(cfg, X, rows: int = 64):
     """The oracle on one host core over the first `rows` rows of D, with the
     time of the whole of D extrapolated from it (a context figure)."""
     import oracle
@@ -384,7 +413,7 @@ def oracle_single_core(cfg, A, B, rows: int = 64):
     orc.set_num_threads(1)
     try:
         t0 = time.perf_counter()
-        oracle_rows(orc, cfg, A, B, (0, rows))
+        oracle_rows(orc, cfg, X, (0, rows))
         dt = time.perf_counter() - t0
     finally:
         orc.set_num_threads(threads)
@@ -424,19 +453,19 @@ def run_reference(args, cfg):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    A, B = make_inputs(cfg)
+    X = make_inputs(cfg)
     import oracle
 
     orc = oracle.get()
     # Size each step so that warm-up + steps end within about two minutes.
     step_s = max(0.02, min(1.5, 120.0 / max(1, args.warmup + args.steps)))
-    _, rows, dt = oracle_sample(cfg, A, B, target_s=step_s)
+    _, rows, dt = oracle_sample(cfg, X, target_s=step_s)
     step_rows = rows
     times = []
     for i in range(args.warmup + args.steps):
         r0 = (i * step_rows) % max(1, cfg.M - step_rows + 1)
         t0 = time.perf_counter()
-        oracle_rows(orc, cfg, A, B, (r0, r0 + step_rows))
+        oracle_rows(orc, cfg, X, (r0, r0 + step_rows))
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
@@ -461,31 +490,35 @@ def run_reference(args, cfg):
     return 0
 
 
-def end_to_end(A, B, cfg, gemm, dev, steps, world):
-    """The metric end to end: every step copies its A and B from pinned host
-    memory to the device, runs the GEMM through the public API and copies D
-    back to pinned host memory.
+def end_to_end(X, cfg, gemm, dev, steps, world):
+    """The metric end to end: every step copies its inputs (A and B, and for a
+    block-scaled workload the row-major scales of A and B) from pinned host
+    memory to the device, runs the public API (packing the scales, then the
+    GEMM) and copies D back to pinned host memory.
 
     Steps are pipelined the way a caller streaming host-resident operands
-    would run them: two device slots, A and B uploaded on two copy streams, the
-    GEMM on the compute stream, D downloaded on a fourth stream, so the copies
-    of step i+1 and i-1 overlap the GEMM of step i.  Each step still moves its
-    own inputs in and its own result out.  The serial figure (one step at a
-    time, everything on one stream) is reported beside it.
+    would run them: two device slots, the inputs uploaded on two copy streams,
+    the GEMM on the compute stream, D downloaded on a fourth stream, so the
+    copies of step i+1 and i-1 overlap the GEMM of step i.  Each step still
+    moves its own inputs in and its own result out.  The serial figure (one
+    step at a time, everything on one stream) is reported beside it.
     """
-    import numpy as np
     import torch
 
+    from dense_gemm_engineering_gb300 import binding
+
     flops = 2.0 * cfg.M * cfg.N * cfg.K
-    hA = storage_tensor(A).pin_memory()
-    hB = storage_tensor(B).pin_memory()
+    hX = [storage_tensor(x).pin_memory() for x in X]
     slots = 2
-    dA = [torch.empty(hA.shape, dtype=hA.dtype, device=dev) for _ in range(slots)]
-    dB = [torch.empty(hB.shape, dtype=hB.dtype, device=dev) for _ in range(slots)]
+    dX = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in hX] for _ in range(slots)]
+    packed = [[torch.empty(max(16, binding.mx_scales_size(r, cfg.K)), dtype=torch.uint8,
+                           device=dev) for r in (cfg.M, cfg.N)] if cfg.mx else None
+              for _ in range(slots)]
     dD = [torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev) for _ in range(slots)]
     hD = [torch.empty((cfg.M, cfg.N), dtype=torch.int16).pin_memory() for _ in range(slots)]
     comp = torch.cuda.current_stream(dev)
     s_a, s_b, s_d = (torch.cuda.Stream(dev) for _ in range(3))
+    copy_stream = [s_a if j % 2 == 0 else s_b for j in range(len(hX))]  # A (+SA), B (+SB)
     n = max(4, min(steps, 40))
 
     def run_pipelined(count):
@@ -497,20 +530,19 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
         s_b.wait_event(e0)
         for i in range(count):
             k = i % slots
-            ev_in = []
-            for st, dst, src in ((s_a, dA[k], hA), (s_b, dB[k], hB)):
-                if i >= slots:
+            if i >= slots:
+                for st in (s_a, s_b):
                     st.wait_event(gemm_done[i - slots])  # slot k no longer read
+            for st, dst, src in zip(copy_stream, dX[k], hX):
                 with torch.cuda.stream(st):
                     dst.copy_(src, non_blocking=True)
+            for st in (s_a, s_b):
                 ev = torch.cuda.Event()
                 ev.record(st)
-                ev_in.append(ev)
-            for ev in ev_in:
                 comp.wait_event(ev)
             if i >= slots:
                 comp.wait_event(d2h_done[i - slots])  # D slot k downloaded
-            gemm(operand(dA[k], cfg), operand(dB[k], cfg), dD[k])
+            gemm(device_inputs(cfg, dX[k], packed[k]), dD[k])
             gemm_done[i].record(comp)
             s_d.wait_event(gemm_done[i])
             with torch.cuda.stream(s_d):
@@ -525,9 +557,9 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(comp)
         for _ in range(count):
-            dA[0].copy_(hA, non_blocking=True)
-            dB[0].copy_(hB, non_blocking=True)
-            gemm(operand(dA[0], cfg), operand(dB[0], cfg), dD[0])
+            for dst, src in zip(dX[0], hX):
+                dst.copy_(src, non_blocking=True)
+            gemm(device_inputs(cfg, dX[0], packed[0]), dD[0])
             hD[0].copy_(dD[0].view(torch.int16), non_blocking=True)
         e1.record(comp)
         torch.cuda.synchronize(dev)
@@ -537,10 +569,12 @@ def end_to_end(A, B, cfg, gemm, dev, steps, world):
     run_serial(2)
     ms = max_over_ranks(run_pipelined(n), world, dev)
     ms_serial = max_over_ranks(run_serial(n), world, dev)
+    what = "A, B and the row-major scales of A and B" if cfg.mx else "A, B"
+    call = "the scale packing and the public GEMM call" if cfg.mx else "the public GEMM call"
     return {"value": job_throughput(flops, world, ms), "unit": UNIT, "ms_per_step": ms,
-            "steps": n, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+            "steps": n, "h2d_bytes_per_step": int(sum(x.nbytes for x in X)),
             "d2h_bytes_per_step": int(cfg.M * cfg.N * 2),
-            "path": "pinned host A, B -> device (2 copy streams) -> the public GEMM call -> device D "
+            "path": f"pinned host {what} -> device (2 copy streams) -> {call} -> device D "
                     "-> pinned host (copy stream); 2 device slots, step i+1's uploads and step "
                     "i-1's download overlap step i's GEMM",
             "serial_value": job_throughput(flops, world, ms_serial),
@@ -562,9 +596,9 @@ def run_ours(args, cfg):
     build.build()
     binding.load()
 
-    A, B = make_inputs(cfg)
-    dA = operand(storage_tensor(A).to(dev), cfg)
-    dB = operand(storage_tensor(B).to(dev), cfg)
+    X = make_inputs(cfg)
+    xs = device_inputs(cfg, [storage_tensor(x).to(dev) for x in X])  # scales packed once
+    dA, dB = xs[0], xs[1]
     dD = torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev)
     gemm = gemm_for(cfg)
     stream = torch.cuda.current_stream(dev)
@@ -576,7 +610,7 @@ def run_ours(args, cfg):
 
     for _ in range(args.warmup):
         flush.zero_()
-        gemm(dA, dB, dD)
+        gemm(xs, dD)
     torch.cuda.synchronize(dev)
     if binding.gemm_device_status(clear=True) != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -593,7 +627,7 @@ def run_ours(args, cfg):
     for i in range(args.steps):
         flush.zero_()  # 512 MiB write evicts the previous step's operands from L2
         starts[i].record(stream)
-        gemm(dA, dB, dD)
+        gemm(xs, dD)
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
@@ -613,7 +647,7 @@ def run_ours(args, cfg):
     # ---- end to end through the public API, host buffers -------------------------
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(A, B, cfg, gemm, dev, args.steps, world)
+        e2e = end_to_end(X, cfg, gemm, dev, args.steps, world)
 
     peaks, peak_src = measured_peaks()
     peak, peak_basis = peak_for(cfg, peaks)
@@ -624,7 +658,10 @@ def run_ours(args, cfg):
     nominal = props.multi_processor_count * flop_clk * sm_max * 1e6 / 1e12
     dtype_code = {"f16": binding.GEMM_F16, "bf16": binding.GEMM_BF16, "e4m3": binding.GEMM_E4M3,
                   "e5m2": binding.GEMM_E5M2}[cfg.dtype]
-    plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, dtype_code, 0 if cfg.layout == "abt" else 1)
+    if cfg.mx:
+        plan = binding.gemm_mx_plan(cfg.M, cfg.N, cfg.K, dtype_code)
+    else:
+        plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, dtype_code, 0 if cfg.layout == "abt" else 1)
 
     if rank != 0:
         if world > 1:
@@ -633,15 +670,26 @@ def run_ours(args, cfg):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu, _, _ = oracle_sample(cfg, A, B, args.cpu_seconds)
+        cpu, _, _ = oracle_sample(cfg, X, args.cpu_seconds)
         # the same oracle on one core over 64 rows, whole-D time extrapolated
-        cpu["single_core"] = oracle_single_core(cfg, A, B)
+        cpu["single_core"] = oracle_single_core(cfg, X)
 
     # ---- context figures (GPU only), measured after the timed region --------------
     context = None
     if not args.no_context:
         n_ctx = max(5, min(args.steps, 20))
-        if cfg.is_fp8:
+        if cfg.mx:
+            # cuBLASLt's block-scaled FP8 GEMM through torch: the tiled scale
+            # layout is the one torch._scaled_mm takes for 32-element UE8M0 scales
+            f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
+            e8 = getattr(torch, "float8_e8m0fnu", None)
+            a8, b8 = dA.view(f8), dB.view(f8)
+            sa = xs[2][:binding.mx_scales_size(cfg.M, cfg.K)]
+            sb = xs[3][:binding.mx_scales_size(cfg.N, cfg.K)]
+            mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa.view(e8),  # noqa: E731
+                                          scale_b=sb.view(e8), out_dtype=torch_dtype(cfg.out))
+            mm_what = "torch._scaled_mm (cuBLASLt block-scaled FP8, UE8M0 per 32)"
+        elif cfg.is_fp8:
             # cuBLASLt's FP8 GEMM through torch (scales of 1, alpha folded in by D's scale)
             f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
             a8, b8 = dA.view(f8), dB.view(f8)
@@ -658,9 +706,9 @@ def run_ours(args, cfg):
             mm_what = "torch.mm (cuBLAS)"
         try:
             t_mm = time_launches(mm, n_ctx, dev, flush)
-        except RuntimeError as e:  # e.g. an FP8 format the library does not take
+        except (RuntimeError, TypeError) as e:  # e.g. a format the library does not take
             t_mm, mm_what = None, f"{mm_what} unavailable: {str(e).splitlines()[0][:120]}"
-        t_warm = time_launches(lambda: gemm(dA, dB, dD), n_ctx, dev)
+        t_warm = time_launches(lambda: gemm(xs, dD), n_ctx, dev)
         context = {
             "torch_mm": {"value": flops / (t_mm / 1e3) / 1e12 if t_mm else None, "unit": UNIT,
                          "ms_per_step": t_mm,
@@ -679,7 +727,9 @@ def run_ours(args, cfg):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K,
-                   "layout": cfg.layout, "inputs": f"{cfg.dist}, seed {cfg.seed}",
+                   "layout": cfg.layout, "inputs": f"{cfg.dist}, seed {cfg.seed}"
+                   + (", UE8M0 scales per 32 K uniform in [124, 130], packed once before "
+                      "the timed region" if cfg.mx else ""),
                    "accumulate": "fp32 (TMEM)",
                    "l2": "flushed before every timed step (512 MiB write, outside the events)",
                    "plan": plan, "parallelism": f"replicas x{world}",

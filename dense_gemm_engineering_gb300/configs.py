@@ -14,7 +14,9 @@ Sources of the shapes:
 FP8 workloads (E4M3 inputs, BF16 output; "TIRx: A Unified Tile Primitive ML
 Compiler", kernel performance: FP8 GEMMs with M = 8192 and model-derived weight
 shapes, which the page does not list): the headline square shape in FP8, and
-M = N = K = 8192.
+M = N = K = 8192.  The block-scaled (MX) workloads take the same two shapes
+with one UE8M0 scale per 32 K elements of each row, scale bytes uniform in
+[124, 130] (scales 2^-3 .. 2^3).
 """
 from __future__ import annotations
 
@@ -33,6 +35,7 @@ class GemmConfig:
     seed: int
     out_dtype: str = ""  # FP8 inputs: the 16-bit output type ("" = dtype)
     alpha: float = 1.0  # FP8 inputs: D = alpha * A.Bt
+    mx: bool = False  # FP8 inputs with one UE8M0 scale per 32 K elements of each row
 
     @property
     def is_fp8(self) -> bool:
@@ -52,7 +55,8 @@ class GemmConfig:
 
     @property
     def min_bytes(self) -> int:
-        return self.elem_bytes * (self.M * self.K + self.N * self.K) + 2 * self.M * self.N
+        scales = (self.M + self.N) * -(-self.K // 32) if self.mx else 0
+        return self.elem_bytes * (self.M * self.K + self.N * self.K) + 2 * self.M * self.N + scales
 
     @property
     def rtol(self) -> float:
@@ -77,7 +81,14 @@ FP8_CONFIGS = [
                out_dtype="bf16"),
 ]
 
-BY_NAME = {c.name: c for c in CONFIGS + FP8_CONFIGS}
+MX_CONFIGS = [
+    GemmConfig("mx_square_4096x4096x4096_e4m3_abt", "abt", 4096, 4096, 4096, "e4m3", "uniform",
+               22, out_dtype="bf16", mx=True),
+    GemmConfig("mx_8192x8192x8192_e4m3_abt", "abt", 8192, 8192, 8192, "e4m3", "normal", 23,
+               out_dtype="bf16", mx=True),
+]
+
+BY_NAME = {c.name: c for c in CONFIGS + FP8_CONFIGS + MX_CONFIGS}
 
 # The measured workload: FP16 A.Bt at 4096^3.
 HEADLINE = CONFIGS[2]

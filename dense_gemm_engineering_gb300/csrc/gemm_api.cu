@@ -190,10 +190,11 @@ struct Stages {
 template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1, int F8 = 0>
 using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC, F8>;
 
-// Block-scaled FP8 (MX) stages: a stage also holds 2 KiB of scales as loaded
-// and 4 KiB of realigned B scales; 5 stages of 2-CTA 224-wide tiles.
+// Block-scaled FP8 (MX) stages: a stage also holds 512 B of A scales and
+// 4 KiB of B scales laid out for the TMEM copy, next to the scale warp's 6 KiB
+// ring; 5 stages of 2-CTA 224-wide tiles.
 constexpr int stages_for_mx(int cg, int bn) {
-    return (227 * 1024 - 32768 - 1024 - 512) / (128 * 128 + (bn / cg) * 128 + 2048 + 4096);
+    return (227 * 1024 - 32768 - 1024 - 512 - 6144) / (128 * 128 + (bn / cg) * 128 + 512 + 4096);
 }
 template <int CG, int BN, bool BF16, int F8>
 using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, 1, F8, true>;
@@ -304,8 +305,8 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
         args.counters = reinterpret_cast<unsigned long long*>(ws);
         args.partials = reinterpret_cast<float*>(ws + ((p.ws_counter_bytes + 255u) & ~size_t(255)));
     }
-    // Scale maps: one A atom (this CTA's 128 rows) and three B atoms (the tile's
-    // 224 columns from the 128-row block holding its first) per k-block.
+    // Block-scale maps: one A atom (this CTA's 128 rows) and three B atoms (the
+    // tile's 224 columns from the 128-row block holding its first) per k-block.
     CUtensorMap msa = ma, msb = ma;
     if constexpr (C::MX) {
         if (!encode_scales(&msa, SA, uint64_t(M), uint64_t(K), 1) ||

@@ -99,18 +99,23 @@ struct KernelConfig {
     static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
     // Block-scaled FP8 (MX): one UE8M0 scale per 32 K elements of every row of A
     // and of B, multiplied on tcgen05.mma kind::mxf8f6f4.block_scale.  A seventh
-    // warp realigns each stage's B scales for the tile (see the scale warp).
+    // warp writes each stage's B scales for the tile (see the scale warp).
     static constexpr bool MX = MX_;
     static constexpr int THREADS = MX ? kNumThreads + 32 : kNumThreads;
-    // MX shared memory per stage: the scale atoms as loaded (512 B of A scales
-    // for this CTA's 128 rows, then three 512 B atoms of B scales covering the
-    // tile's columns) and the tile's B scales realigned (128 rows x 32 B).
-    static constexpr uint32_t SF_IN_BYTES = MX ? 2048u : 0u;
-    static constexpr uint32_t SFB_OUT_BYTES = MX ? 4096u : 0u;
+    // MX shared memory per stage: the A scales of this CTA's 128 rows as loaded
+    // (one 512-byte atom) and the tile's B scales as the scale warp lays them
+    // out for the TMEM copy (128 rows x 32 B).
+    static constexpr uint32_t SFA_BYTES = MX ? 512u : 0u;
+    static constexpr uint32_t SFB_BYTES = MX ? 4096u : 0u;
+    // The scale warp's own ring of B-scale atoms as loaded (three 512-byte atoms
+    // per k-block), SF_RAW_SLOTS deep, loaded SF_RAW_AHEAD k-blocks ahead.
+    static constexpr int SF_RAW_SLOTS = MX ? 4 : 0;
+    static constexpr int SF_RAW_AHEAD = SF_RAW_SLOTS - 1;
+    static constexpr uint32_t SF_RAW_BYTES = 1536u;
 
     static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * BK * ELEM_BYTES;  // 16 KiB per consumer
     static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * BK * ELEM_BYTES;
-    static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES);
+    static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES + SFA_BYTES);
     // Two accumulators of BN FP32 columns at a power-of-two stride (the TMEM
     // allocation is a power of two of at least 32 columns).
     static constexpr uint32_t ACC_STRIDE = BN <= 128 ? 128u : 256u;
@@ -129,13 +134,15 @@ struct KernelConfig {
 
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr uint32_t OFF_SF_IN = OFF_B + STAGES * B_BYTES;
-    static constexpr uint32_t OFF_SFB_OUT = OFF_SF_IN + STAGES * SF_IN_BYTES;
-    static constexpr uint32_t OFF_EPI = OFF_SFB_OUT + STAGES * SFB_OUT_BYTES;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr uint32_t OFF_SF_RAW = OFF_SFB + STAGES * SFB_BYTES;
+    // (the epilogue staging is 128-byte swizzled: 1 KiB aligned)
+    static constexpr uint32_t OFF_EPI = (OFF_SF_RAW + SF_RAW_SLOTS * SF_RAW_BYTES + 1023u) & ~1023u;
     static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * 2u * EPI_BUF_BYTES;
     // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue
-    // warp, and (MX) scales_loaded[STAGES]
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + (MX ? STAGES : 0u);
+    // warp, and (MX) one per scale-ring slot
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + SF_RAW_SLOTS;
     // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
     // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
     // (32 rows x 64 FP32 columns).
@@ -195,6 +202,9 @@ struct KernelConfig {
                           NUM_ACC == 2 && BK == 128),
                   "MX: FP8 A.Bt, 224-wide tiles (224 accumulator + 32 scale columns per buffer)");
     static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
+    static_assert((OFF_EPI % 1024) == 0 && (OFF_SFA % 512) == 0 && (OFF_SFB % 16) == 0 &&
+                      (OFF_SF_RAW % 512) == 0,
+                  "swizzled staging 1 KiB aligned; scale buffers aligned for TMA and tcgen05.cp");
 };
 
 struct GemmArgs {
@@ -367,8 +377,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
     };
     auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
-    auto scales_bar = [&](uint32_t s) {
-        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + s);
+    auto raw_bar = [&](uint32_t i) {
+        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + i);
     };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
@@ -379,13 +389,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // the leader's expect_tx arrival (MX: and each CTA's scale warp)
             ptx::mbar_init(full_bar(s), C::MX ? 1u + uint32_t(C::CG) : 1u);
             ptx::mbar_init(empty_bar(s), uint32_t(C::MC));  // one tcgen05.commit per pair
-            if constexpr (C::MX) ptx::mbar_init(scales_bar(s), 1);  // expect_tx arrival
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
             ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
         }
         for (uint32_t e = 0; e < uint32_t(kEpilogueWarps); ++e) ptx::mbar_init(epi_bar(e), 1);
+        for (uint32_t i = 0; i < uint32_t(C::SF_RAW_SLOTS); ++i) ptx::mbar_init(raw_bar(i), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_a);
@@ -466,16 +476,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         }
                     }
                     if constexpr (C::MX) {
-                        // Scales of k-block kb (one 512-byte atom = 128 rows x 4 groups
-                        // per 128-row block), into this CTA's shared memory, completing
-                        // on this CTA's scales barrier: the A atom of this CTA's rows
-                        // and the three B atoms from the one holding the tile's first
-                        // column (TMA fills atoms past the last with zeros).
-                        const uint32_t sf_dst = base + C::OFF_SF_IN + s * C::SF_IN_BYTES;
-                        ptx::mbar_arrive_expect_tx(scales_bar(s), C::SF_IN_BYTES);
-                        ptx::tma_load_2d(sf_dst, &tmap_sa, scales_bar(s), kb * 128, a_row / 128);
-                        ptx::tma_load_2d(sf_dst + 512u, &tmap_sb, scales_bar(s), kb * 128,
-                                         (nt * C::BN) / 128);
+                        // The A scales of k-block kb for this CTA's 128 rows: one
+                        // 512-byte atom (128 rows x 4 groups), into this CTA's shared
+                        // memory, completing with the operands.
+                        const uint32_t sfa_dst = base + C::OFF_SFA + s * C::SFA_BYTES;
+                        if constexpr (C::CG == 1)
+                            ptx::tma_load_2d(sfa_dst, &tmap_sa, full_bar(s), kb * 128, a_row / 128);
+                        else
+                            ptx::tma_load_2d_pair(sfa_dst, &tmap_sa,
+                                                  ptx::map_to_rank(full_bar(s), pair_leader), kb * 128,
+                                                  a_row / 128);
                     }
                 }
                 __syncwarp();
@@ -522,13 +532,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if constexpr (C::MX) {
                             // This k-block's scales into TMEM (each CTA of the pair
                             // from its own shared memory): A's atom as loaded, B's
-                            // as realigned by the scale warp.  Ordered before the
+                            // as laid out by the scale warp.  Ordered before the
                             // MMAs below, which read them.
                             ptx::tmem_cp_32x128b_warpx4<C::CG>(
-                                sf_t, noswizzle_desc(base + C::OFF_SF_IN + s * C::SF_IN_BYTES, 128u, 128u));
+                                sf_t, noswizzle_desc(base + C::OFF_SFA + s * C::SFA_BYTES, 128u, 128u));
                             ptx::tmem_cp_128x256b<C::CG>(
-                                sf_t + 16u,
-                                noswizzle_desc(base + C::OFF_SFB_OUT + s * C::SFB_OUT_BYTES, 128u, 256u));
+                                sf_t + 16u, noswizzle_desc(base + C::OFF_SFB + s * C::SFB_BYTES, 128u, 256u));
                         }
 #pragma unroll
                         for (int k = 0; k < C::BK / C::MMA_K; ++k) {
@@ -585,55 +594,103 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ---- scale warp (MX) -------------------------------------------------
         // The MMA reads the B scale of tile column n at TMEM column sfb + n/32,
         // and a scale address must be a multiple of 16 columns, so column group
-        // 0 of the tile must start a buffer.  A tile of 224 columns starts at
-        // column group (n0 / 32) mod 4 of the first 512-byte atom loaded, so
-        // this warp shifts each stage's B scales down by that many 4-byte cells
-        // into the layout of a 128 x 256-bit TMEM copy (row r = 8 column groups
-        // of lane r % 32; the four lane quarters hold the same rows), then
-        // marks the stage full for the MMA issuer.
+        // 0 of the tile must start a buffer.  A 224-column tile starts at column
+        // group (n0 / 32) mod 4 of the 512-byte atom that holds its first
+        // column, so this warp loads the three atoms that cover the tile (TMA,
+        // into its own ring, SF_RAW_AHEAD k-blocks ahead), shifts each lane's
+        // row down by that many 4-byte cells and writes it in the layout of a
+        // 128 x 256-bit TMEM copy (row r = the 8 column groups of lane r % 32;
+        // the four lane quarters hold the same rows).  It fills stage s as soon
+        // as the stage is free and counts as one arrival on the stage's full
+        // barrier, so the MMA issuer waits for nothing the operands do not
+        // already bring.
         if constexpr (C::MX) {
-            uint32_t s = 0, ph = 0;
-            bool ok = true;
-            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
-                const WorkUnit w = unit_of(args, u);
-                int32_t mt, nt;
-                tile_of_task(args.grid, w.tile, mt, nt);
-                const uint32_t shift = uint32_t((nt * C::BN) / 32) & 3u;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded_warp(scales_bar(s), ph, abort_flag, kRoleScales)) {
-                        ok = false;
-                        break;
-                    }
-                    // lane l: row l of the three loaded B atoms = column groups 0..11
-                    const uint32_t in = base + C::OFF_SF_IN + s * C::SF_IN_BYTES + 512u + lane * 16u;
-                    const uint4 q0 = ptx::ld_shared_v4_u32(in);
-                    const uint4 q1 = ptx::ld_shared_v4_u32(in + 512u);
-                    const uint4 q2 = ptx::ld_shared_v4_u32(in + 1024u);
-                    const uint32_t g[11] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y,
-                                            q1.z, q1.w, q2.x, q2.y, q2.z};
-                    uint32_t r[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        r[j] = shift == 0u ? g[j] : shift == 1u ? g[j + 1] : shift == 2u ? g[j + 2] : g[j + 3];
-                    const uint32_t out = base + C::OFF_SFB_OUT + s * C::SFB_OUT_BYTES;
-#pragma unroll
-                    for (uint32_t q = 0; q < 4; ++q) {
-                        const uint32_t row = lane + 32u * q;
-                        const uint32_t addr = out + (row / 8u) * 256u + (row % 8u) * 16u;
-                        ptx::st_shared_v4(addr, r[0], r[1], r[2], r[3]);
-                        ptx::st_shared_v4(addr + 128u, r[4], r[5], r[6], r[7]);
-                    }
-                    ptx::fence_proxy_async_smem();  // visible to the tensor core's copy
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (C::CG == 2)
-                            ptx::mbar_arrive_cluster(ptx::map_to_rank(full_bar(s), pair_leader));
-                        else
-                            ptx::mbar_arrive(full_bar(s));
-                    }
-                    __syncwarp();
-                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+            // Two cursors over this cluster's k-blocks (unit by unit, whole tiles
+            // only): one for the loads, SF_RAW_AHEAD ahead, one for the writes.
+            // They advance by increments; the tile is looked up once per unit.
+            struct Cursor {
+                int64_t u;   // unit (tile)
+                int32_t kb;  // k-block within it
+                int32_t g0;  // the tile's first column group (32 columns each)
+            };
+            auto locate = [&](Cursor& c) {
+                if (c.u < units) {
+                    int32_t mt, nt;
+                    tile_of_task(args.grid, c.u, mt, nt);
+                    c.g0 = (nt * C::BN) / 32;
                 }
+            };
+            auto advance = [&](Cursor& c) {
+                if (++c.kb == args.k_blocks) {
+                    c.kb = 0;
+                    c.u += num_clusters;
+                    locate(c);
+                }
+            };
+            uint32_t issued = 0;  // loads issued so far (slot = count mod SF_RAW_SLOTS)
+            auto issue = [&](Cursor& c) {
+                if (c.u >= units) return;
+                const uint32_t slot = issued % uint32_t(C::SF_RAW_SLOTS);
+                if (ptx::elect_one_sync()) {
+                    ptx::mbar_arrive_expect_tx(raw_bar(slot), 3u * 512u);
+                    ptx::tma_load_2d(base + C::OFF_SF_RAW + slot * C::SF_RAW_BYTES, &tmap_sb,
+                                     raw_bar(slot), c.kb * 128, c.g0 / 4);
+                }
+                __syncwarp();
+                ++issued;
+                advance(c);
+            };
+            Cursor ld{cluster_id, 0, 0}, wr{cluster_id, 0, 0};
+            locate(ld);
+            locate(wr);
+            for (int i = 0; i < C::SF_RAW_AHEAD; ++i) issue(ld);
+            uint32_t s = 0, ph = 0, slot = 0, rph = 0;
+            bool ok = true;
+            while (wr.u < units) {
+                // The slot this fills was read in the previous iteration, whose
+                // proxy fence ordered those reads before this copy.
+                issue(ld);
+                if (!wait_bounded_warp(raw_bar(slot), rph, abort_flag, kRoleScales) ||
+                    !wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleScales)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t in = base + C::OFF_SF_RAW + slot * C::SF_RAW_BYTES + lane * 16u;
+                const uint4 q0 = ptx::ld_shared_v4_u32(in);
+                const uint4 q1 = ptx::ld_shared_v4_u32(in + 512u);
+                const uint4 q2 = ptx::ld_shared_v4_u32(in + 1024u);
+                uint32_t r[8];
+                switch (uint32_t(wr.g0) & 3u) {  // the same for the whole warp
+                    case 0u: r[0] = q0.x; r[1] = q0.y; r[2] = q0.z; r[3] = q0.w;
+                             r[4] = q1.x; r[5] = q1.y; r[6] = q1.z; r[7] = q1.w; break;
+                    case 1u: r[0] = q0.y; r[1] = q0.z; r[2] = q0.w; r[3] = q1.x;
+                             r[4] = q1.y; r[5] = q1.z; r[6] = q1.w; r[7] = q2.x; break;
+                    case 2u: r[0] = q0.z; r[1] = q0.w; r[2] = q1.x; r[3] = q1.y;
+                             r[4] = q1.z; r[5] = q1.w; r[6] = q2.x; r[7] = q2.y; break;
+                    default: r[0] = q0.w; r[1] = q1.x; r[2] = q1.y; r[3] = q1.z;
+                             r[4] = q1.w; r[5] = q2.x; r[6] = q2.y; r[7] = q2.z; break;
+                }
+                const uint32_t out = base + C::OFF_SFB + s * C::SFB_BYTES + (lane / 8u) * 256u + (lane % 8u) * 16u;
+#pragma unroll
+                for (uint32_t q = 0; q < 4; ++q) {  // row lane + 32 q: 4 groups of 8 rows further
+                    ptx::st_shared_v4(out + q * 1024u, r[0], r[1], r[2], r[3]);
+                    ptx::st_shared_v4(out + q * 1024u + 128u, r[4], r[5], r[6], r[7]);
+                }
+                ptx::fence_proxy_async_smem();  // visible to the tensor core's copy
+                __syncwarp();
+                if (lane == 0) {
+                    // A release at CTA scope orders this thread's writes before
+                    // the arrival; a cluster-scope release here cost ~1.5 k cycles
+                    // per k-block (it waits for far more than these writes).
+                    if constexpr (C::CG == 2)
+                        ptx::mbar_arrive_remote_cta(ptx::map_to_rank(full_bar(s), pair_leader));
+                    else
+                        ptx::mbar_arrive(full_bar(s));
+                }
+                __syncwarp();
+                advance(wr);
+                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                if (++slot == uint32_t(C::SF_RAW_SLOTS)) { slot = 0; rph ^= 1u; }
             }
             if (!ok) settle_after_abort();
             __syncwarp();

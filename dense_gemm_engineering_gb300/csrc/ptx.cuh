@@ -102,6 +102,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                  : "memory");
 }
 
+// Arrive on a barrier of another CTA of the cluster (a shared::cluster
+// address) with release semantics at CTA scope: this thread's earlier writes
+// are ordered before the arrival, without the cluster-wide flush of a
+// cluster-scope release.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
 // True once the phase with parity `parity` has completed (the hardware may
 // suspend the thread for a short while before returning false).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

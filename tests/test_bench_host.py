@@ -6,6 +6,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -76,12 +77,16 @@ def test_metric_names_follow_the_workload():
     from dense_gemm_engineering_gb300 import configs
 
     assert bench.metric_for(configs.HEADLINE) == bench.METRIC
-    names = {bench.metric_for(c) for c in configs.CONFIGS + configs.FP8_CONFIGS}
-    assert len(names) == len(configs.CONFIGS) + len(configs.FP8_CONFIGS)
+    every = configs.CONFIGS + configs.FP8_CONFIGS + configs.MX_CONFIGS
+    names = {bench.metric_for(c) for c in every}
+    assert len(names) == len(every)
     fp8 = configs.FP8_CONFIGS[0]
     assert "E4M3->BF16" in bench.metric_for(fp8)
     peak, basis = bench.peak_for(fp8, {"bf16_tflops": 1910.0})
     assert peak == 3820.0 and "x 2" in basis
+    mx = configs.MX_CONFIGS[0]
+    assert "block-scaled MX E4M3->BF16" in bench.metric_for(mx)
+    assert bench.peak_for(mx, {"bf16_tflops": 1910.0})[0] == 3820.0
 
 
 def test_reference_arm_runs_the_fp8_oracle():
@@ -92,6 +97,30 @@ def test_reference_arm_runs_the_fp8_oracle():
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and "E4M3" in line["metric"]
+
+
+def test_reference_arm_runs_the_block_scaled_oracle():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--config",
+                        "mx_square_4096x4096x4096_e4m3_abt"], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and "MX" in line["metric"]
+
+
+def test_block_scaled_inputs_and_oracle_rows():
+    import oracle
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.MX_CONFIGS[0]
+    X = bench.make_inputs(cfg)
+    assert len(X) == 4 and X[2].shape == (cfg.M, cfg.K // 32) and X[3].shape == (cfg.N, cfg.K // 32)
+    assert 124 <= X[2].min() and X[2].max() <= 130
+    rows = bench.oracle_rows(oracle.get(), cfg, X, (5, 7))
+    want = oracle.gemm_mx(X[0][5:7], X[1], X[2][5:7], X[3], fmt="e4m3", out_dtype="bf16")
+    assert np.array_equal(rows, want)
+    assert cfg.min_bytes == 2 * 4096 * 4096 + 2 * 4096 * 4096 + 2 * 4096 * 128
 
 
 def test_traffic_lookup_matches_only_current_kernel(tmp_path, monkeypatch):
@@ -122,9 +151,9 @@ def test_single_core_oracle_baseline_restores_threads():
     from dense_gemm_engineering_gb300 import configs
 
     cfg = configs.CONFIGS[0]  # 128 x 128 x 64
-    A, B = bench.make_inputs(cfg)
+    X = bench.make_inputs(cfg)
     before = oracle.get().num_threads()
-    ctx = bench.oracle_single_core(cfg, A, B, rows=16)
+    ctx = bench.oracle_single_core(cfg, X, rows=16)
     assert oracle.get().num_threads() == before
     assert ctx["cores"] == 1 and ctx["value"] > 0
     assert ctx["extrapolated_full_s"] > 0 and "rows 0..16" in ctx["sample"]
