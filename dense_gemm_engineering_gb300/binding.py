@@ -34,7 +34,7 @@ EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_worksp
            "gemm_run_no_alloc", "gemm_status_string", "gemm_plan", "gemm_tile_origin",
            "gemm_device_status", "gemm_selftest_wait_timeout", "gemm_fp8_abt", "gemm_fp8_run",
            "gemm_fp8_run_workspace", "gemm_mx_abt", "gemm_mx_run", "gemm_mx_scales_size",
-           "gemm_mx_pack_scales", "gemm_mx_plan")
+           "gemm_mx_scales_b_size", "gemm_mx_pack_scales", "gemm_mx_pack_scales_b", "gemm_mx_plan")
 
 
 class GemmError(RuntimeError):
@@ -105,8 +105,12 @@ def load(path: str | None = None):
     lib.gemm_mx_run.restype = c_int
     lib.gemm_mx_scales_size.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.gemm_mx_scales_size.restype = c_int
+    lib.gemm_mx_scales_b_size.argtypes = [i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.gemm_mx_scales_b_size.restype = c_int
     lib.gemm_mx_pack_scales.argtypes = [vp, i64, i64, i64, vp, vp]
     lib.gemm_mx_pack_scales.restype = c_int
+    lib.gemm_mx_pack_scales_b.argtypes = [vp, i64, i64, i64, vp, vp]
+    lib.gemm_mx_pack_scales_b.restype = c_int
     lib.gemm_mx_plan.argtypes = [i64, i64, i64, c_int, ctypes.POINTER(GemmOptions), ip, ip, ip,
                                  ip, ip, ctypes.POINTER(i64)]
     lib.gemm_mx_plan.restype = c_int
@@ -359,7 +363,7 @@ def gemm_run_ptr(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: 
 
 
 def mx_scales_size(rows: int, K: int) -> int:
-    """Bytes of the tiled block scales of a rows x K FP8 operand."""
+    """Bytes of the block scales of A (rows = M) in the layout gemm_mx reads."""
     n = ctypes.c_size_t()
     st = load().gemm_mx_scales_size(int(rows), int(K), ctypes.byref(n))
     if st != 0:
@@ -367,10 +371,16 @@ def mx_scales_size(rows: int, K: int) -> int:
     return n.value
 
 
-def mx_pack_scales(S, K: int, out=None, *, stream=None):
-    """Tiled block scales (the layout gemm_mx reads) from row-major ones: S is a
-    CUDA uint8 tensor (rows, ceil(K / 32)) of UE8M0 bytes (row stride free,
-    inner stride 1).  Returns a uint8 tensor of mx_scales_size(rows, K) bytes."""
+def mx_scales_b_size(N: int, K: int) -> int:
+    """Bytes of the block scales of B in the layout gemm_mx reads."""
+    n = ctypes.c_size_t()
+    st = load().gemm_mx_scales_b_size(int(N), int(K), ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "gemm_mx_scales_b_size")
+    return n.value
+
+
+def _pack(S, K, out, stream, for_b):
     import torch
 
     if S.device.type != "cuda" or S.dtype != torch.uint8 or S.dim() != 2:
@@ -378,7 +388,7 @@ def mx_pack_scales(S, K: int, out=None, *, stream=None):
     rows, groups = S.shape
     if groups != (int(K) + 31) // 32:
         raise GemmError(-3, f"scales have {groups} groups per row; K = {K} needs {(K + 31) // 32}")
-    nbytes = mx_scales_size(rows, K)
+    nbytes = mx_scales_b_size(rows, K) if for_b else mx_scales_size(rows, K)
     if out is None:
         out = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=S.device)
     elif out.numel() * out.element_size() < nbytes or out.device != S.device:
@@ -386,18 +396,33 @@ def mx_pack_scales(S, K: int, out=None, *, stream=None):
     ld = int(S.stride(0)) if rows > 1 else max(groups, 1)
     if rows > 0 and groups > 1 and S.stride(1) != 1:
         raise GemmError(-3, "scales: inner dimension must be contiguous")
-    st = load().gemm_mx_pack_scales(S.data_ptr(), rows, int(K), ld, out.data_ptr(),
-                                    _stream_handle(stream, S.device))
+    lib = load()
+    fn = lib.gemm_mx_pack_scales_b if for_b else lib.gemm_mx_pack_scales
+    st = fn(S.data_ptr(), rows, int(K), ld, out.data_ptr(), _stream_handle(stream, S.device))
     if st != 0:
-        raise GemmError(st, "gemm_mx_pack_scales")
+        raise GemmError(st, "gemm_mx_pack_scales_b" if for_b else "gemm_mx_pack_scales")
     return out
+
+
+def mx_pack_scales(S, K: int, out=None, *, stream=None):
+    """The scales of A in the layout gemm_mx reads, from row-major ones: S is a
+    CUDA uint8 tensor (M, ceil(K / 32)) of UE8M0 bytes (row stride free, inner
+    stride 1).  Returns a uint8 tensor of mx_scales_size(M, K) bytes."""
+    return _pack(S, K, out, stream, False)
+
+
+def mx_pack_scales_b(S, K: int, out=None, *, stream=None):
+    """The scales of B (N, ceil(K / 32)) in the layout gemm_mx reads (blocks
+    for 224-column tiles); a uint8 tensor of mx_scales_b_size(N, K) bytes."""
+    return _pack(S, K, out, stream, True)
 
 
 def gemm_mx(A, B, SA, SB, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0,
             options=None, stream=None):
     """Block-scaled FP8: D[i, j] = alpha * sum_k (A[i, k] sa) (B[j, k] sb), one UE8M0
     scale per 32 K elements of each row.  A (M, K) and B (N, K) as for gemm_fp8;
-    SA / SB the tiled scales (mx_pack_scales output, uint8 CUDA tensors)."""
+    SA / SB the scales of A and B as mx_pack_scales / mx_pack_scales_b lay them
+    out (uint8 CUDA tensors)."""
     import torch
 
     for t in (A, B, SA, SB):
@@ -410,9 +435,10 @@ def gemm_mx(A, B, SA, SB, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.
     N, Kb = B.shape
     if Kb != K:
         raise GemmError(-3, f"K mismatch ({K} vs {Kb})")
-    for t, rows in ((SA, M), (SB, N)):
-        if t.dtype != torch.uint8 or t.numel() < mx_scales_size(rows, K):
-            raise GemmError(-3, "scales: uint8 tensors of mx_scales_size(rows, K) bytes")
+    for t, need in ((SA, mx_scales_size(M, K)), (SB, mx_scales_b_size(N, K))):
+        if t.dtype != torch.uint8 or t.numel() < need:
+            raise GemmError(-3, "scales: uint8 tensors of mx_scales_size(M, K) and "
+                                "mx_scales_b_size(N, K) bytes")
     odt = out_dtype if out_dtype is not None else (D.dtype if D is not None else torch.bfloat16)
     if D is None:
         D = torch.empty((M, N), dtype=odt, device=A.device)

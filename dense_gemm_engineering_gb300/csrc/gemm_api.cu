@@ -81,6 +81,22 @@ bool encode_scales(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t K,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Block scales (MX) of B, pre-laid-out for 224-column tiles (include/gemm.h):
+// ceil(N / 224) * ceil(K / 128) blocks of 4096 bytes, seen as a 2-D tensor of
+// 32-bit words with rows of 1 KiB; a box is one block (256 words x 4 rows).
+bool encode_scales_b(CUtensorMap* map, const void* ptr, uint64_t N, uint64_t K) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t blocks = ((N + 223) / 224) * ((K + 127) / 128);
+    const cuuint64_t dims[2] = {256, blocks * 4};
+    const cuuint64_t strides[1] = {1024};
+    const cuuint32_t box[2] = {256, 4};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- per-device facts, cached -------------------------------------------------
 
 struct DeviceInfo {
@@ -138,7 +154,7 @@ void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
     if ((*err = ensure_smem_attribute<C>()) != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(clusters * C::CLUSTER), 1, 1);
-    cfg.blockDim = dim3(unsigned(C::THREADS), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -158,7 +174,7 @@ int query_max_clusters(int dev, int sm_count) {
     if (ensure_smem_attribute<C>() != cudaSuccess) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(C::CLUSTER * (sm_count / C::CLUSTER)), 1, 1);
-    cfg.blockDim = dim3(unsigned(C::THREADS), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -190,11 +206,11 @@ struct Stages {
 template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1, int F8 = 0>
 using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC, F8>;
 
-// Block-scaled FP8 (MX) stages: a stage also holds 512 B of A scales and
-// 4 KiB of B scales laid out for the TMEM copy, next to the scale warp's 6 KiB
-// ring; 5 stages of 2-CTA 224-wide tiles.
+// Block-scaled FP8 (MX) stages: a stage also holds 512 B of A scales and the
+// tile's 4 KiB block of B scales, and the epilogue stages through one 4 KiB
+// buffer per warp; 6 stages of 2-CTA 224-wide tiles.
 constexpr int stages_for_mx(int cg, int bn) {
-    return (227 * 1024 - 32768 - 1024 - 512 - 6144) / (128 * 128 + (bn / cg) * 128 + 512 + 4096);
+    return (227 * 1024 - 16384 - 1024 - 512) / (128 * 128 + (bn / cg) * 128 + 512 + 4096);
 }
 template <int CG, int BN, bool BF16, int F8>
 using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, 1, F8, true>;
@@ -305,12 +321,12 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
         args.counters = reinterpret_cast<unsigned long long*>(ws);
         args.partials = reinterpret_cast<float*>(ws + ((p.ws_counter_bytes + 255u) & ~size_t(255)));
     }
-    // Block-scale maps: one A atom (this CTA's 128 rows) and three B atoms (the
-    // tile's 224 columns from the 128-row block holding its first) per k-block.
+    // Block-scale maps: one A atom (this CTA's 128 rows) and the tile's B block
+    // per k-block.
     CUtensorMap msa = ma, msb = ma;
     if constexpr (C::MX) {
         if (!encode_scales(&msa, SA, uint64_t(M), uint64_t(K), 1) ||
-            !encode_scales(&msb, SB, uint64_t(N), uint64_t(K), 3))
+            !encode_scales_b(&msb, SB, uint64_t(N), uint64_t(K)))
             return GEMM_ERR_CUDA;
     } else {
         (void)SA;
@@ -585,9 +601,12 @@ namespace {
 
 // Shared body of the 16-bit and FP8 entry points.  in_fmt: GEMM_F16 /
 // GEMM_BF16 (then out_dtype == in_fmt) or GEMM_E4M3 / GEMM_E5M2 (A.Bt only).
-// Bytes of the tiled block scales (MX) of a rows x K FP8 operand.
+// Bytes of the block scales (MX) of A (rows = M) and of B.
 int64_t mx_scale_bytes(int64_t rows, int64_t K) {
     return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
+int64_t mx_scale_b_bytes(int64_t N, int64_t K) {
+    return ((N + 223) / 224) * ((K + 127) / 128) * 4096;
 }
 
 int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -619,9 +638,10 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
         if (!SA || !SB) return GEMM_ERR_NULL;
         if ((reinterpret_cast<uintptr_t>(SA) & 15u) || (reinterpret_cast<uintptr_t>(SB) & 15u))
             return GEMM_ERR_ALIGN;
-        const int64_t sa = mx_scale_bytes(M, K), sb = mx_scale_bytes(N, K);
+        const int64_t sa = mx_scale_bytes(M, K), sb = mx_scale_b_bytes(N, K);
         if (overlaps(D, M, N, ldd, 2, SA, 1, sa, sa, 1) || overlaps(D, M, N, ldd, 2, SB, 1, sb, sb, 1))
             return GEMM_ERR_ALIAS;
+        if (sb / 1024 > INT32_MAX) return GEMM_ERR_SHAPE;  // TMA row coordinates are 32-bit
     }
 
     if (K == 0) {
@@ -708,11 +728,15 @@ extern "C" int gemm_mx_scales_size(int64_t rows, int64_t K, size_t* bytes) {
     return GEMM_OK;
 }
 
-extern "C" int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst,
-                                   cudaStream_t stream) {
+namespace gb300 {
+namespace {
+
+// Shared checks and launch of the two scale-packing kernels.
+int pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst, bool for_b,
+                cudaStream_t stream) {
     if (rows < 0 || K < 0 || rows > INT32_MAX || K > INT32_MAX) return GEMM_ERR_SHAPE;
     const int64_t groups = (K + 31) / 32;
-    const int64_t bytes = mx_scale_bytes(rows, K);
+    const int64_t bytes = for_b ? mx_scale_b_bytes(rows, K) : mx_scale_bytes(rows, K);
     if (bytes == 0) return GEMM_OK;
     if (!src || !dst) return GEMM_ERR_NULL;
     if (ld < groups || ld <= 0) return GEMM_ERR_SHAPE;
@@ -724,10 +748,35 @@ extern "C" int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int
     const int64_t words = bytes / 4;
     int64_t blocks = (words + 255) / 256;
     if (blocks > 8L * di.sm_count) blocks = 8L * di.sm_count;
-    mx_pack_scales_kernel<<<unsigned(blocks), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), rows, groups, ld, (K + 127) / 128, static_cast<uint32_t*>(dst),
-        words);
+    if (for_b)
+        mx_pack_scales_b_kernel<<<unsigned(blocks), 256, 0, stream>>>(
+            static_cast<const uint8_t*>(src), rows, groups, ld, (K + 127) / 128,
+            static_cast<uint32_t*>(dst), words);
+    else
+        mx_pack_scales_kernel<<<unsigned(blocks), 256, 0, stream>>>(
+            static_cast<const uint8_t*>(src), rows, groups, ld, (K + 127) / 128,
+            static_cast<uint32_t*>(dst), words);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gb300
+
+extern "C" int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst,
+                                   cudaStream_t stream) {
+    return pack_scales(src, rows, K, ld, dst, false, stream);
+}
+
+extern "C" int gemm_mx_pack_scales_b(const void* src, int64_t N, int64_t K, int64_t ld, void* dst,
+                                     cudaStream_t stream) {
+    return pack_scales(src, N, K, ld, dst, true, stream);
+}
+
+extern "C" int gemm_mx_scales_b_size(int64_t N, int64_t K, size_t* bytes) {
+    if (!bytes) return GEMM_ERR_NULL;
+    if (N < 0 || K < 0 || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_SHAPE;
+    *bytes = size_t(mx_scale_b_bytes(N, K));
+    return GEMM_OK;
 }
 
 extern "C" int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,

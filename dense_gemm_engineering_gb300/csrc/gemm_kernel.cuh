@@ -68,8 +68,7 @@ enum : uint32_t {
     kRoleMma = 2u,
     kRoleEpilogue = 3u,
     kRoleDrain = 4u,
-    kRoleSelfTest = 5u,
-    kRoleScales = 6u
+    kRoleSelfTest = 5u
 };
 
 template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1,
@@ -98,24 +97,17 @@ struct KernelConfig {
     static constexpr int MMA_K = F8 ? 32 : 16;         // K per MMA: 32 bytes either way
     static constexpr int B_ROWS = BN / CG;    // tile columns whose B this CTA loads
     // Block-scaled FP8 (MX): one UE8M0 scale per 32 K elements of every row of A
-    // and of B, multiplied on tcgen05.mma kind::mxf8f6f4.block_scale.  A seventh
-    // warp writes each stage's B scales for the tile (see the scale warp).
+    // and of B, multiplied on tcgen05.mma kind::mxf8f6f4.block_scale.  Shared
+    // memory per stage adds the A scales of this CTA's 128 rows (one 512-byte
+    // atom) and the tile's B scales (one 4 KiB block, already laid out for the
+    // TMEM copy), both loaded by TMA with the operands.
     static constexpr bool MX = MX_;
-    static constexpr int THREADS = MX ? kNumThreads + 32 : kNumThreads;
-    // MX shared memory per stage: the A scales of this CTA's 128 rows as loaded
-    // (one 512-byte atom) and the tile's B scales as the scale warp lays them
-    // out for the TMEM copy (128 rows x 32 B).
     static constexpr uint32_t SFA_BYTES = MX ? 512u : 0u;
     static constexpr uint32_t SFB_BYTES = MX ? 4096u : 0u;
-    // The scale warp's own ring of B-scale atoms as loaded (three 512-byte atoms
-    // per k-block), SF_RAW_SLOTS deep, loaded SF_RAW_AHEAD k-blocks ahead.
-    static constexpr int SF_RAW_SLOTS = MX ? 4 : 0;
-    static constexpr int SF_RAW_AHEAD = SF_RAW_SLOTS - 1;
-    static constexpr uint32_t SF_RAW_BYTES = 1536u;
 
     static constexpr uint32_t A_BYTES = uint32_t(A_ROWS) * BK * ELEM_BYTES;  // 16 KiB per consumer
     static constexpr uint32_t B_BYTES = uint32_t(B_ROWS) * BK * ELEM_BYTES;
-    static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES + SFA_BYTES);
+    static constexpr uint32_t STAGE_TX = uint32_t(CG) * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
     // Two accumulators of BN FP32 columns at a power-of-two stride (the TMEM
     // allocation is a power of two of at least 32 columns).
     static constexpr uint32_t ACC_STRIDE = BN <= 128 ? 128u : 256u;
@@ -130,19 +122,22 @@ struct KernelConfig {
     static constexpr int FULL_CHUNKS = BN / 64;
     static constexpr bool HALF_CHUNK = (BN % 64) != 0;
     static constexpr uint32_t EPI_BUF_BYTES = 32u * 128u;              // 32 rows x 64 cols
+    // Staging buffers per epilogue warp: two (a chunk's store may still be
+    // reading one while the next is written), or one for MX, whose scales take
+    // the shared memory of the second (each chunk store then waits for the
+    // previous one's reads; the stores of a tile are paced 1 us apart anyway).
+    static constexpr uint32_t EPI_BUFS = MX ? 1u : 2u;
     static constexpr uint32_t MN_ATOM_BYTES = 64u * 128u;              // MN-major: 64 K x 64 N
 
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr uint32_t OFF_SF_RAW = OFF_SFB + STAGES * SFB_BYTES;
     // (the epilogue staging is 128-byte swizzled: 1 KiB aligned)
-    static constexpr uint32_t OFF_EPI = (OFF_SF_RAW + SF_RAW_SLOTS * SF_RAW_BYTES + 1023u) & ~1023u;
-    static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * 2u * EPI_BUF_BYTES;
-    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue
-    // warp, and (MX) one per scale-ring slot
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + SF_RAW_SLOTS;
+    static constexpr uint32_t OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023u) & ~1023u;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * EPI_BUFS * EPI_BUF_BYTES;
+    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue warp
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps;
     // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
     // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
     // (32 rows x 64 FP32 columns).
@@ -202,8 +197,7 @@ struct KernelConfig {
                           NUM_ACC == 2 && BK == 128),
                   "MX: FP8 A.Bt, 224-wide tiles (224 accumulator + 32 scale columns per buffer)");
     static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
-    static_assert((OFF_EPI % 1024) == 0 && (OFF_SFA % 512) == 0 && (OFF_SFB % 16) == 0 &&
-                      (OFF_SF_RAW % 512) == 0,
+    static_assert((OFF_EPI % 1024) == 0 && (OFF_SFA % 512) == 0 && (OFF_SFB % 512) == 0,
                   "swizzled staging 1 KiB aligned; scale buffers aligned for TMA and tcgen05.cp");
 };
 
@@ -348,7 +342,7 @@ __device__ __forceinline__ uint32_t count_range_done(unsigned long long* word, u
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args,
@@ -377,17 +371,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
     };
     auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
-    auto raw_bar = [&](uint32_t i) {
-        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + i);
-    };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
 
     // ---- one-time setup -------------------------------------------------
     if (warp == 0 && lane == 0) {
         for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
-            // the leader's expect_tx arrival (MX: and each CTA's scale warp)
-            ptx::mbar_init(full_bar(s), C::MX ? 1u + uint32_t(C::CG) : 1u);
+            ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
             ptx::mbar_init(empty_bar(s), uint32_t(C::MC));  // one tcgen05.commit per pair
         }
         for (uint32_t b = 0; b < 2; ++b) {
@@ -395,7 +385,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
         }
         for (uint32_t e = 0; e < uint32_t(kEpilogueWarps); ++e) ptx::mbar_init(epi_bar(e), 1);
-        for (uint32_t i = 0; i < uint32_t(C::SF_RAW_SLOTS); ++i) ptx::mbar_init(raw_bar(i), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_a);
@@ -476,16 +465,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         }
                     }
                     if constexpr (C::MX) {
-                        // The A scales of k-block kb for this CTA's 128 rows: one
-                        // 512-byte atom (128 rows x 4 groups), into this CTA's shared
-                        // memory, completing with the operands.
+                        // The scales of k-block kb, into this CTA's shared memory,
+                        // completing with the operands: the A atom of this CTA's 128
+                        // rows (128 rows x 4 groups) and the tile's B block (the
+                        // image of its TMEM copy; both CTAs of a pair load it).
                         const uint32_t sfa_dst = base + C::OFF_SFA + s * C::SFA_BYTES;
-                        if constexpr (C::CG == 1)
+                        const uint32_t sfb_dst = base + C::OFF_SFB + s * C::SFB_BYTES;
+                        const int32_t sfb_block = nt * args.k_blocks + kb;
+                        if constexpr (C::CG == 1) {
                             ptx::tma_load_2d(sfa_dst, &tmap_sa, full_bar(s), kb * 128, a_row / 128);
-                        else
-                            ptx::tma_load_2d_pair(sfa_dst, &tmap_sa,
-                                                  ptx::map_to_rank(full_bar(s), pair_leader), kb * 128,
-                                                  a_row / 128);
+                            ptx::tma_load_2d(sfb_dst, &tmap_sb, full_bar(s), 0, sfb_block * 4);
+                        } else {
+                            const uint32_t fb = ptx::map_to_rank(full_bar(s), pair_leader);
+                            ptx::tma_load_2d_pair(sfa_dst, &tmap_sa, fb, kb * 128, a_row / 128);
+                            ptx::tma_load_2d_pair(sfb_dst, &tmap_sb, fb, 0, sfb_block * 4);
+                        }
                     }
                 }
                 __syncwarp();
@@ -531,9 +525,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (ptx::elect_one_sync()) {
                         if constexpr (C::MX) {
                             // This k-block's scales into TMEM (each CTA of the pair
-                            // from its own shared memory): A's atom as loaded, B's
-                            // as laid out by the scale warp.  Ordered before the
-                            // MMAs below, which read them.
+                            // from its own shared memory), ordered before the MMAs
+                            // below, which read them.
                             ptx::tmem_cp_32x128b_warpx4<C::CG>(
                                 sf_t, noswizzle_desc(base + C::OFF_SFA + s * C::SFA_BYTES, 128u, 128u));
                             ptx::tmem_cp_128x256b<C::CG>(
@@ -590,115 +583,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (!ok) settle_after_abort();
         }
         __syncwarp();
-    } else if (C::MX && warp == 2u + kEpilogueWarps) {
-        // ---- scale warp (MX) -------------------------------------------------
-        // The MMA reads the B scale of tile column n at TMEM column sfb + n/32,
-        // and a scale address must be a multiple of 16 columns, so column group
-        // 0 of the tile must start a buffer.  A 224-column tile starts at column
-        // group (n0 / 32) mod 4 of the 512-byte atom that holds its first
-        // column, so this warp loads the three atoms that cover the tile (TMA,
-        // into its own ring, SF_RAW_AHEAD k-blocks ahead), shifts each lane's
-        // row down by that many 4-byte cells and writes it in the layout of a
-        // 128 x 256-bit TMEM copy (row r = the 8 column groups of lane r % 32;
-        // the four lane quarters hold the same rows).  It fills stage s as soon
-        // as the stage is free and counts as one arrival on the stage's full
-        // barrier, so the MMA issuer waits for nothing the operands do not
-        // already bring.
-        if constexpr (C::MX) {
-            // Two cursors over this cluster's k-blocks (unit by unit, whole tiles
-            // only): one for the loads, SF_RAW_AHEAD ahead, one for the writes.
-            // They advance by increments; the tile is looked up once per unit.
-            struct Cursor {
-                int64_t u;   // unit (tile)
-                int32_t kb;  // k-block within it
-                int32_t g0;  // the tile's first column group (32 columns each)
-            };
-            auto locate = [&](Cursor& c) {
-                if (c.u < units) {
-                    int32_t mt, nt;
-                    tile_of_task(args.grid, c.u, mt, nt);
-                    c.g0 = (nt * C::BN) / 32;
-                }
-            };
-            auto advance = [&](Cursor& c) {
-                if (++c.kb == args.k_blocks) {
-                    c.kb = 0;
-                    c.u += num_clusters;
-                    locate(c);
-                }
-            };
-            uint32_t issued = 0;  // loads issued so far (slot = count mod SF_RAW_SLOTS)
-            auto issue = [&](Cursor& c) {
-                if (c.u >= units) return;
-                const uint32_t slot = issued % uint32_t(C::SF_RAW_SLOTS);
-                if (ptx::elect_one_sync()) {
-                    ptx::mbar_arrive_expect_tx(raw_bar(slot), 3u * 512u);
-                    ptx::tma_load_2d(base + C::OFF_SF_RAW + slot * C::SF_RAW_BYTES, &tmap_sb,
-                                     raw_bar(slot), c.kb * 128, c.g0 / 4);
-                }
-                __syncwarp();
-                ++issued;
-                advance(c);
-            };
-            Cursor ld{cluster_id, 0, 0}, wr{cluster_id, 0, 0};
-            locate(ld);
-            locate(wr);
-            for (int i = 0; i < C::SF_RAW_AHEAD; ++i) issue(ld);
-            uint32_t s = 0, ph = 0, slot = 0, rph = 0;
-            bool ok = true;
-            while (wr.u < units) {
-                // The slot this fills was read in the previous iteration, whose
-                // proxy fence ordered those reads before this copy.
-                issue(ld);
-                if (!wait_bounded_warp(raw_bar(slot), rph, abort_flag, kRoleScales) ||
-                    !wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleScales)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t in = base + C::OFF_SF_RAW + slot * C::SF_RAW_BYTES + lane * 16u;
-                const uint4 q0 = ptx::ld_shared_v4_u32(in);
-                const uint4 q1 = ptx::ld_shared_v4_u32(in + 512u);
-                const uint4 q2 = ptx::ld_shared_v4_u32(in + 1024u);
-                uint32_t r[8];
-                switch (uint32_t(wr.g0) & 3u) {  // the same for the whole warp
-                    case 0u: r[0] = q0.x; r[1] = q0.y; r[2] = q0.z; r[3] = q0.w;
-                             r[4] = q1.x; r[5] = q1.y; r[6] = q1.z; r[7] = q1.w; break;
-                    case 1u: r[0] = q0.y; r[1] = q0.z; r[2] = q0.w; r[3] = q1.x;
-                             r[4] = q1.y; r[5] = q1.z; r[6] = q1.w; r[7] = q2.x; break;
-                    case 2u: r[0] = q0.z; r[1] = q0.w; r[2] = q1.x; r[3] = q1.y;
-                             r[4] = q1.z; r[5] = q1.w; r[6] = q2.x; r[7] = q2.y; break;
-                    default: r[0] = q0.w; r[1] = q1.x; r[2] = q1.y; r[3] = q1.z;
-                             r[4] = q1.w; r[5] = q2.x; r[6] = q2.y; r[7] = q2.z; break;
-                }
-                const uint32_t out = base + C::OFF_SFB + s * C::SFB_BYTES + (lane / 8u) * 256u + (lane % 8u) * 16u;
-#pragma unroll
-                for (uint32_t q = 0; q < 4; ++q) {  // row lane + 32 q: 4 groups of 8 rows further
-                    ptx::st_shared_v4(out + q * 1024u, r[0], r[1], r[2], r[3]);
-                    ptx::st_shared_v4(out + q * 1024u + 128u, r[4], r[5], r[6], r[7]);
-                }
-                ptx::fence_proxy_async_smem();  // visible to the tensor core's copy
-                __syncwarp();
-                if (lane == 0) {
-                    // A release at CTA scope orders this thread's writes before
-                    // the arrival; a cluster-scope release here cost ~1.5 k cycles
-                    // per k-block (it waits for far more than these writes).
-                    if constexpr (C::CG == 2)
-                        ptx::mbar_arrive_remote_cta(ptx::map_to_rank(full_bar(s), pair_leader));
-                    else
-                        ptx::mbar_arrive(full_bar(s));
-                }
-                __syncwarp();
-                advance(wr);
-                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
-                if (++slot == uint32_t(C::SF_RAW_SLOTS)) { slot = 0; rph ^= 1u; }
-            }
-            if (!ok) settle_after_abort();
-            __syncwarp();
-        }
     } else {
         // ---- epilogue warps 2..5 ----------------------------------------------
         const uint32_t quarter = warp & 3u;  // this warp may read TMEM lanes 32q..32q+31
-        const uint32_t buf0 = base + C::OFF_EPI + (warp - 2u) * 2u * C::EPI_BUF_BYTES;
+        const uint32_t buf0 = base + C::OFF_EPI + (warp - 2u) * C::EPI_BUFS * C::EPI_BUF_BYTES;
         const uint32_t my_epi_bar = epi_bar(warp - 2u);
         const uint32_t my_ring = base + C::OFF_A + (warp - 2u) * C::PIECES_PER_WARP * C::PIECE_BYTES;
         uint32_t ab = 0, aph = 0, chunk = 0, eph = 0;
@@ -731,8 +619,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (ring_slot >= 0) {
                 buf = my_ring + uint32_t(ring_slot) * C::EPI_BUF_BYTES;
             } else {
-                buf = buf0 + (chunk & 1u) * C::EPI_BUF_BYTES;
-                if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store 2 chunks ago read `buf`
+                buf = buf0 + (chunk % C::EPI_BUFS) * C::EPI_BUF_BYTES;
+                // the store EPI_BUFS chunks ago read `buf`
+                if (lane == 0) ptx::bulk_wait_group_read<int(C::EPI_BUFS) - 1>();
             }
             __syncwarp();
             // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
@@ -1005,7 +894,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // CTA's shared memory and arrives on its barriers); TMEM is freed after
     // every warp's last TMEM read.
     if constexpr (C::CLUSTER > 1) {
-        if (warp < 2 || warp >= 2u + kEpilogueWarps) {  // the epilogue warps arrived already
+        if (warp < 2) {  // the epilogue warps arrived already
             ptx::tc_fence_before();
             ptx::cluster_arrive();
         }
@@ -1055,6 +944,35 @@ __global__ void mx_pack_scales_kernel(const uint8_t* __restrict__ src, int64_t r
         for (int g = 0; g < 4; ++g) {
             const uint32_t b = (row < rows && g0 + g < groups) ? src[row * ld + g0 + g] : 127u;
             v |= b << (8 * g);
+        }
+        dst[i] = v;
+    }
+}
+
+// B scales (MX) from row-major bytes (rows x groups, row stride ld) to the
+// blocks the GEMM loads: block (t, kc) of 4096 bytes at (t * kchunks + kc) *
+// 4096 holds, for the 224 columns of tile t and K groups 4 kc .. 4 kc + 3, the
+// image of the tile's 128 x 256-bit TMEM copy: byte (r / 8) * 256 + (r % 8) *
+// 16 + (c / 4) * 128 + (c % 4) * 4 + g is the scale of column 224 t + 32 c +
+// r % 32 (c < 7), group 4 kc + g; every lane quarter r / 32 holds the same
+// rows.  Past the matrix, and for c = 7, 127 (a scale of 1).  One thread per
+// 32-bit word.
+__global__ void mx_pack_scales_b_kernel(const uint8_t* __restrict__ src, int64_t rows,
+                                        int64_t groups, int64_t ld, int64_t kchunks,
+                                        uint32_t* __restrict__ dst, int64_t words) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < words;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t block = i / 1024;
+        const uint32_t o = uint32_t(i % 1024) * 4u;  // byte offset in the block
+        const uint32_t r = (o / 256u) * 8u + (o % 128u) / 16u;
+        const uint32_t c = ((o % 256u) / 128u) * 4u + (o % 16u) / 4u;
+        const int64_t col = (block / kchunks) * 224 + 32 * int64_t(c) + (r % 32u);
+        const int64_t g0 = (block % kchunks) * 4;
+        uint32_t v = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const bool inside = c < 7u && col < rows && g0 + g < groups;
+            v |= (inside ? uint32_t(src[col * ld + g0 + g]) : 127u) << (8 * g);
         }
         dst[i] = v;
     }

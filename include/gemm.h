@@ -213,15 +213,24 @@ int gemm_fp8_run_workspace(const void* A, const void* B, void* D, int64_t M, int
  * FP32 in tensor memory, alpha multiplies it, and the result is rounded once
  * (nearest even) to out_dtype.
  *
- * Scale layout.  SA (scales of A) and SB (scales of B) are device buffers in
- * a tiled layout, gemm_mx_scales_size(rows, K) bytes each (rows = M for SA,
- * N for SB), 16-byte aligned: ceil(rows / 128) x ceil(K / 128) atoms of 512
- * bytes, atom (rb, kc) at byte offset (rb * ceil(K / 128) + kc) * 512; inside
- * an atom the scale of row rb * 128 + r and K group kc * 4 + g (elements
- * 32 (kc * 4 + g) .. +31) is the byte at (r % 32) * 16 + (r / 32) * 4 + g.
- * Bytes for rows >= rows or groups >= ceil(K / 32) are padding: they must
- * not be 255.  gemm_mx_pack_scales() writes this layout from plain row-major
- * scales.  The caller owns SA and SB; neither may overlap D.
+ * Scale layouts.  SA and SB are device buffers, 16-byte aligned, owned by the
+ * caller, not overlapping D; padding bytes (rows or columns past the matrix,
+ * K groups past ceil(K / 32)) must not be 255.
+ *   SA, the scales of A: gemm_mx_scales_size(M, K) bytes, ceil(M / 128) x
+ *   ceil(K / 128) atoms of 512 bytes, atom (rb, kc) at byte offset
+ *   (rb * ceil(K / 128) + kc) * 512; inside an atom the scale of row
+ *   rb * 128 + r and K group kc * 4 + g (elements 32 (kc * 4 + g) .. +31) is
+ *   the byte at (r % 32) * 16 + (r / 32) * 4 + g.  gemm_mx_pack_scales()
+ *   writes it from row-major scales.
+ *   SB, the scales of B, pre-laid-out for this library's 224-column tiles:
+ *   gemm_mx_scales_b_size(N, K) bytes, ceil(N / 224) x ceil(K / 128) blocks
+ *   of 4096 bytes, block (t, kc) at byte offset (t * ceil(K / 128) + kc) *
+ *   4096; inside a block the scale of column 224 t + 32 c + l (c < 7,
+ *   l < 32) and K group kc * 4 + g is the byte at (r / 8) * 256 + (r % 8) * 16
+ *   + (c / 4) * 128 + (c % 4) * 4 + g for each r in {l, l + 32, l + 64,
+ *   l + 96} (four copies; c = 7 is padding).  This is the image of the tile's
+ *   scales that the tensor core copies into tensor memory, so the kernel loads
+ *   it in one piece.  gemm_mx_pack_scales_b() writes it from row-major scales.
  *
  * Options: cta_group 0 or 2, block_n 0 or 224, raster_group and
  * max_clusters as for gemm_run; consumers, multicast and tail_split 0 or 1
@@ -237,9 +246,12 @@ int gemm_mx_run(const void* A, const void* B, const void* SA, const void* SB, vo
                 int in_format, int out_dtype, float alpha, const gemm_options_t* opts,
                 cudaStream_t stream);
 
-/* Bytes of the tiled scales of a rows x K operand:
- * ceil(rows / 128) * ceil(K / 128) * 512 (written to *bytes). */
+/* Bytes of SA for a rows x K operand: ceil(rows / 128) * ceil(K / 128) * 512
+ * (written to *bytes). */
 int gemm_mx_scales_size(int64_t rows, int64_t K, size_t* bytes);
+
+/* Bytes of SB for an N x K operand: ceil(N / 224) * ceil(K / 128) * 4096. */
+int gemm_mx_scales_b_size(int64_t N, int64_t K, size_t* bytes);
 
 /*
  * Tiled scales (the layout above) from row-major ones: src is a device buffer
@@ -251,6 +263,11 @@ int gemm_mx_scales_size(int64_t rows, int64_t K, size_t* bytes);
  */
 int gemm_mx_pack_scales(const void* src, int64_t rows, int64_t K, int64_t ld, void* dst,
                         cudaStream_t stream);
+
+/* SB (the layout above) from row-major scales: as gemm_mx_pack_scales, with
+ * rows = N and dst of gemm_mx_scales_b_size(N, K) bytes. */
+int gemm_mx_pack_scales_b(const void* src, int64_t N, int64_t K, int64_t ld, void* dst,
+                          cudaStream_t stream);
 
 /* The plan gemm_mx_run would use (outputs as gemm_plan; may be NULL). */
 int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,

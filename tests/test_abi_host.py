@@ -255,3 +255,17 @@ def test_mx_pack_argument_errors(lib):
     assert pack(P, 4, 64, 2, Q + 4, None) == -4
     assert pack(P + 4, 4, 64, 2, P, None) == -5   # dst overlaps src
     assert pack(P, 0, 64, 2, 0, None) == 0        # nothing to write
+
+
+def test_mx_scales_b_size_and_pack_errors(lib):
+    n = binding.ctypes.c_size_t()
+    for N, K, want in [(0, 128, 0), (1, 1, 4096), (224, 128, 4096), (225, 129, 2 * 2 * 4096),
+                       (8192, 8192, 37 * 64 * 4096)]:
+        assert binding.load().gemm_mx_scales_b_size(N, K, binding.ctypes.byref(n)) == 0
+        assert n.value == want == binding.mx_scales_b_size(N, K)
+    pack = binding.load().gemm_mx_pack_scales_b
+    assert pack(P, -1, 64, 2, Q, None) == -3
+    assert pack(P, 4, 64, 1, Q, None) == -3
+    assert pack(0, 4, 64, 2, Q, None) == -1
+    assert pack(P, 4, 64, 2, Q + 4, None) == -4
+    assert pack(P + 4, 4, 64, 2, P, None) == -5

@@ -2,9 +2,9 @@
 
 D[i,j] = round(alpha * sum_k (A[i,k] 2^(SA[i][k/32]-127)) (B[j,k] 2^(SB[j][k/32]-127)))
 with FP8 A (M x K) and B (N x K), one UE8M0 scale per 32 K elements of each
-row, FP32 accumulation and a 16-bit D.  The scales reach the GEMM in the tiled
-layout written by gemm_mx_pack_scales, whose output is checked byte for byte
-against the layout's definition.  Exact cases are compared bit for bit; the
+row, FP32 accumulation and a 16-bit D.  The scales reach the GEMM in the
+layouts written by gemm_mx_pack_scales (A) and gemm_mx_pack_scales_b (B), whose
+outputs are checked byte for byte against the layouts' definitions.  Exact cases are compared bit for bit; the
 rest within the output type's tolerance (|got - ref| <= 1e-2 + rtol |ref|:
 every scaled product is exact in FP32, so only the FP32 accumulation and the
 one rounding to the output type separate the two sides).
@@ -62,12 +62,37 @@ def tiled_scales(S: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def tiled_scales_b(S: np.ndarray, K: int) -> np.ndarray:
+    """The B-scale layout, from its definition: block (t, kc) of 4096 bytes at
+    (t * ceil(K/128) + kc) * 4096; column 224 t + 32 c + l (c < 7), group
+    kc*4 + g at byte (r/8)*256 + (r%8)*16 + (c/4)*128 + (c%4)*4 + g for
+    r = l, l+32, l+64, l+96; 127 elsewhere."""
+    N, groups = S.shape
+    t_n, kc_n = -(-N // 224), -(-K // 128)
+    full = np.full((t_n * 224 + 32, kc_n * 4), 127, dtype=np.uint8)
+    full[:N, :groups] = S
+    out = np.full(t_n * kc_n * 4096, 127, dtype=np.uint8)
+    r = np.arange(128)
+    for t in range(t_n):
+        for kc in range(kc_n):
+            o = (t * kc_n + kc) * 4096
+            for c in range(7):
+                for g in range(4):
+                    byte = (r // 8) * 256 + (r % 8) * 16 + (c // 4) * 128 + (c % 4) * 4 + g
+                    out[o + byte] = full[t * 224 + 32 * c + r % 32, kc * 4 + g]
+    return out
+
+
 def pack(S: np.ndarray, K: int) -> torch.Tensor:
     return binding.mx_pack_scales(to_dev8(S), K)
 
 
+def pack_b(S: np.ndarray, K: int) -> torch.Tensor:
+    return binding.mx_pack_scales_b(to_dev8(S), K)
+
+
 def run_mx(A, B, SA, SB, K, fmt, out, alpha=1.0, options=None, D=None):
-    D = binding.gemm_mx(to_dev8(A), to_dev8(B), pack(SA, K), pack(SB, K), D, fmt=fmt,
+    D = binding.gemm_mx(to_dev8(A), to_dev8(B), pack(SA, K), pack_b(SB, K), D, fmt=fmt,
                         out_dtype=TDT[out], alpha=alpha, options=options)
     torch.cuda.synchronize()
     return D
@@ -92,6 +117,8 @@ def test_pack_layout_byte_exact(shape):
     S = inputs.mx_scales(rows, 2, rows, K, lo=0, hi=254, ld=groups + 3)  # padded rows (255)
     got = pack(S, K).cpu().numpy()[:binding.mx_scales_size(rows, K)]
     assert np.array_equal(got, tiled_scales(S, K))
+    got_b = pack_b(S, K).cpu().numpy()[:binding.mx_scales_b_size(rows, K)]
+    assert np.array_equal(got_b, tiled_scales_b(S, K))
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -224,7 +251,7 @@ def test_k_zero_writes_zeros():
     A = torch.empty((40, 0), dtype=torch.uint8, device="cuda")
     B = torch.empty((48, 0), dtype=torch.uint8, device="cuda")
     S = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    D = torch.full((40, 48), 7.0, dtype=torch.bfloat16, device="cuda")
+    D = torch.full((40, 48), 7.0, dtype=torch.bfloat16, device="cuda")  # K = 0: no scales read
     binding.gemm_mx(A, B, S, S, D, fmt="e4m3")
     torch.cuda.synchronize()
     assert (D == 0).all()
@@ -232,7 +259,7 @@ def test_k_zero_writes_zeros():
 
 def test_option_limits():
     A = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
-    S = torch.full((binding.mx_scales_size(256, 128),), 127, dtype=torch.uint8, device="cuda")
+    S = torch.full((binding.mx_scales_b_size(256, 128),), 127, dtype=torch.uint8, device="cuda")
     for bad in ({"cta_group": 1}, {"block_n": 256}, {"block_n": 192}, {"consumers": 2},
                 {"multicast": 2}, {"tail_split": 2}):
         with pytest.raises(binding.GemmError) as e:
@@ -257,8 +284,8 @@ def test_scale_argument_errors():
     assert call(S, None) == -1
     assert call(S + 4, S) == -4
     assert call(S, S + 8) == -4
-    assert call(S, S + 4096, S + 256) == -5      # D over the scales of A
-    assert call(S + 4096, S, S + 512) == -5      # D over the scales of B
+    assert call(S, S + 16384, S + 256) == -5     # D over the scales of A
+    assert call(S + 16384, S, S + 512) == -5     # D over the scales of B (8 KiB)
     assert lib.gemm_mx_run(A.data_ptr(), B.data_ptr(), S, S, D.data_ptr(), M, N, K, K, K, N,
                            binding.GEMM_BF16, binding.GEMM_BF16, 1.0, None, None) == -2
     torch.cuda.synchronize()
