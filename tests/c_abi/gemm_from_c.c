@@ -3,10 +3,13 @@
  *
  * Usage: gemm_from_c <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin
  *        gemm_from_c fp8 <e4m3|e5m2> M N K A.bin B.bin D.bin alpha
- * Reads A (M x K) and B (N x K for abt / fp8, K x N for ab) as raw 16-bit
- * patterns (bytes for fp8), runs gemm_abt / gemm_ab / gemm_fp8_abt (BF16 D)
- * on cudaMalloc'd buffers on a created stream, writes D (M x N, 16-bit) to
- * D.bin, and checks that a few invalid calls return the documented status
+ *        gemm_from_c mx <e4m3|e5m2> M N K A.bin B.bin D.bin alpha SA.bin SB.bin
+ * Reads A (M x K) and B (N x K for abt / fp8 / mx, K x N for ab) as raw 16-bit
+ * patterns (bytes for fp8 and mx; for mx also the row-major scale bytes, M and
+ * N rows of ceil(K / 32)), runs gemm_abt / gemm_ab / gemm_fp8_abt /
+ * gemm_mx_abt (BF16 D; mx packs the scales with gemm_mx_pack_scales[_b]
+ * first) on cudaMalloc'd buffers on a created stream, writes D (M x N, 16-bit)
+ * to D.bin, and checks that a few invalid calls return the documented status
  * codes.  Exit status 0 on success.
  */
 #include <stdint.h>
@@ -41,11 +44,13 @@ static void* read_file(const char* path, size_t bytes) {
     } while (0)
 
 int main(int argc, char** argv) {
-    const int fp8 = argc >= 2 && strcmp(argv[1], "fp8") == 0;
-    if (argc != (fp8 ? 10 : 9)) {
+    const int mx = argc >= 2 && strcmp(argv[1], "mx") == 0;
+    const int fp8 = mx || (argc >= 2 && strcmp(argv[1], "fp8") == 0);
+    if (argc != (mx ? 12 : fp8 ? 10 : 9)) {
         fprintf(stderr, "usage: %s <abt|ab> <f16|bf16> M N K A.bin B.bin D.bin\n"
-                        "       %s fp8 <e4m3|e5m2> M N K A.bin B.bin D.bin alpha\n",
-                argv[0], argv[0]);
+                        "       %s fp8 <e4m3|e5m2> M N K A.bin B.bin D.bin alpha\n"
+                        "       %s mx <e4m3|e5m2> M N K A.bin B.bin D.bin alpha SA.bin SB.bin\n",
+                argv[0], argv[0], argv[0]);
         return 2;
     }
     const int ab = strcmp(argv[1], "ab") == 0;
@@ -71,9 +76,40 @@ int main(int argc, char** argv) {
     CHECK_CUDA(cudaMemcpy(dA, hA, a_bytes, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dB, hB, b_bytes, cudaMemcpyHostToDevice));
 
-    int st = fp8  ? gemm_fp8_abt(dA, dB, dD, M, N, K, K, K, N, fmt, dtype, alpha, s)
-             : ab ? gemm_ab(dA, dB, dD, M, N, K, K, N, N, dtype, s)
-                  : gemm_abt(dA, dB, dD, M, N, K, K, K, N, dtype, s);
+    void *dSA = NULL, *dSB = NULL;
+    if (mx) {
+        /* row-major scales -> device -> the layouts gemm_mx_abt reads */
+        const int64_t groups = (K + 31) / 32;
+        size_t sa_bytes = 0, sb_bytes = 0;
+        if (gemm_mx_scales_size(M, K, &sa_bytes) != GEMM_OK ||
+            gemm_mx_scales_b_size(N, K, &sb_bytes) != GEMM_OK)
+            return 1;
+        void* hSA = read_file(argv[10], (size_t)(M * groups));
+        void* hSB = read_file(argv[11], (size_t)(N * groups));
+        if (!hSA || !hSB) {
+            fprintf(stderr, "cannot read scales\n");
+            return 2;
+        }
+        void *rawA, *rawB;
+        CHECK_CUDA(cudaMalloc(&rawA, (size_t)(M * groups)));
+        CHECK_CUDA(cudaMalloc(&rawB, (size_t)(N * groups)));
+        CHECK_CUDA(cudaMalloc(&dSA, sa_bytes));
+        CHECK_CUDA(cudaMalloc(&dSB, sb_bytes));
+        CHECK_CUDA(cudaMemcpy(rawA, hSA, (size_t)(M * groups), cudaMemcpyHostToDevice));
+        CHECK_CUDA(cudaMemcpy(rawB, hSB, (size_t)(N * groups), cudaMemcpyHostToDevice));
+        if (gemm_mx_pack_scales(rawA, M, K, groups, dSA, s) != GEMM_OK ||
+            gemm_mx_pack_scales_b(rawB, N, K, groups, dSB, s) != GEMM_OK)
+            return 1;
+        CHECK_CUDA(cudaStreamSynchronize(s));
+        cudaFree(rawA);
+        cudaFree(rawB);
+        free(hSA);
+        free(hSB);
+    }
+    int st = mx    ? gemm_mx_abt(dA, dB, dSA, dSB, dD, M, N, K, K, K, N, fmt, dtype, alpha, s)
+             : fp8 ? gemm_fp8_abt(dA, dB, dD, M, N, K, K, K, N, fmt, dtype, alpha, s)
+             : ab  ? gemm_ab(dA, dB, dD, M, N, K, K, N, N, dtype, s)
+                   : gemm_abt(dA, dB, dD, M, N, K, K, K, N, dtype, s);
     if (st != GEMM_OK) {
         fprintf(stderr, "gemm: %s\n", gemm_status_string(st));
         return 1;
@@ -91,6 +127,15 @@ int main(int argc, char** argv) {
     fclose(f);
 
     /* documented errors */
+    if (mx) {
+        if (gemm_mx_abt(dA, dB, NULL, dSB, dD, M, N, K, K, K, N, fmt, dtype, 1.0f, s) != GEMM_ERR_NULL)
+            return 3;
+        if (gemm_mx_abt(dA, dB, (char*)dSA + 4, dSB, dD, M, N, K, K, K, N, fmt, dtype, 1.0f, s) !=
+            GEMM_ERR_ALIGN)
+            return 3;
+        cudaFree(dSA);
+        cudaFree(dSB);
+    }
     if (fp8) {
         if (gemm_fp8_abt(dA, dB, dD, M, N, K, K, K, N, GEMM_F16, dtype, 1.0f, s) != GEMM_ERR_DTYPE)
             return 3;

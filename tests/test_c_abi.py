@@ -80,3 +80,28 @@ def test_fp8_gemm_from_plain_c(tmp_path, fmt):
     D = np.fromfile(tmp_path / "D.bin", dtype=np.uint16).reshape(M, N)
     ref = oracle.gemm_fp8(A, B, fmt=fmt, out_dtype="bf16", alpha=alpha)
     check_close(D, ref, "bf16", "plain C caller, FP8")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_block_scaled_gemm_from_plain_c(tmp_path, fmt):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    exe = str(tmp_path / "gemm_from_c")
+    r = _compile(exe)
+    assert r.returncode == 0, r.stderr
+    M, N, K, alpha = 300, 520, 272, 0.75
+    A, B, SA, SB = inputs.mx_operands(M, N, K, fmt, "uniform", 33)
+    for name, x in (("A", A), ("B", B), ("SA", SA), ("SB", SB)):
+        np.ascontiguousarray(x).tofile(tmp_path / f"{name}.bin")
+    r = subprocess.run([exe, "mx", fmt, str(M), str(N), str(K), str(tmp_path / "A.bin"),
+                        str(tmp_path / "B.bin"), str(tmp_path / "D.bin"), str(alpha),
+                        str(tmp_path / "SA.bin"), str(tmp_path / "SB.bin")],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+    D = np.fromfile(tmp_path / "D.bin", dtype=np.uint16).reshape(M, N)
+    ref = oracle.gemm_mx(A, B, SA, SB, fmt=fmt, out_dtype="bf16", alpha=alpha)
+    check_close(D, ref, "bf16", "plain C caller, block-scaled FP8")

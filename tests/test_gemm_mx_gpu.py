@@ -257,6 +257,17 @@ def test_k_zero_writes_zeros():
     assert (D == 0).all()
 
 
+def test_torch_float8_tensors_are_accepted():
+    M, N, K = 256, 448, 512
+    A, B, SA, SB = inputs.mx_operands(M, N, K, "e4m3", "uniform", 41)
+    dA = to_dev8(A).view(torch.float8_e4m3fn)
+    dB = to_dev8(B).view(torch.float8_e4m3fn)
+    got = from_device(binding.gemm_mx(dA, dB, pack(SA, K), pack_b(SB, K)))
+    torch.cuda.synchronize()
+    ref = oracle.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16")
+    check_close(got, ref, "bf16", "float8 tensors")
+
+
 def test_option_limits():
     A = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
     S = torch.full((binding.mx_scales_b_size(256, 128),), 127, dtype=torch.uint8, device="cuda")
