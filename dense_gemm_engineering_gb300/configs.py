@@ -86,6 +86,13 @@ MX_CONFIGS = [
                22, out_dtype="bf16", mx=True),
     GemmConfig("mx_8192x8192x8192_e4m3_abt", "abt", 8192, 8192, 8192, "e4m3", "normal", 23,
                out_dtype="bf16", mx=True),
+    # M = 8192 against a transformer MLP's weights (hidden 4096, inner 14336): the
+    # widening projection (N = 14336, K = 4096) and the narrowing one (N = 4096,
+    # K = 14336); the page names "model-derived weight shapes" without listing them
+    GemmConfig("mx_8192x14336x4096_e4m3_abt", "abt", 8192, 14336, 4096, "e4m3", "normal", 24,
+               out_dtype="bf16", mx=True),
+    GemmConfig("mx_8192x4096x14336_e4m3_abt", "abt", 8192, 4096, 14336, "e4m3", "normal", 25,
+               out_dtype="bf16", mx=True),
 ]
 
 BY_NAME = {c.name: c for c in CONFIGS + FP8_CONFIGS + MX_CONFIGS}

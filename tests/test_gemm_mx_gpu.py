@@ -209,6 +209,27 @@ def test_large_sampled_tiles():
         check_close(D[m0:m1, n0:n1], ref, "bf16", f"tile ({m0},{n0})", ref64)
 
 
+@pytest.mark.parametrize("shape", [(8192, 4096, 14336), (8192, 14336, 4096)],
+                         ids=["narrowing_8192x4096x14336", "widening_8192x14336x4096"])
+def test_mlp_shapes_sampled_tiles(shape):
+    # M = 8192 against MLP-like weights: a seeded cover of the schedule's
+    # positions plus the edge tiles (N = 4096 ends in a partial 224-wide tile).
+    M, N, K = shape
+    A, B, SA, SB = inputs.mx_operands(M, N, K, "e4m3", "normal", 8)
+    D = from_device(run_mx(A, B, SA, SB, K, "e4m3", "bf16"))
+    plan = binding.gemm_mx_plan(M, N, K, binding.GEMM_E4M3)
+    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], 16, plan["num_clusters"],
+                         plan["stages"],
+                         lambda t: binding.gemm_tile_origin(M, N, plan["block_m"],
+                                                            plan["block_n"], 16, t),
+                         seed=4, extra_random=4, block_k=128)
+    for (m0, n0) in tiles:
+        m1, n1 = min(m0 + plan["block_m"], M), min(n0 + plan["block_n"], N)
+        ref, ref64 = oracle.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16",
+                                    rows=(m0, m1), cols=(n0, n1), want_f64=True)
+        check_close(D[m0:m1, n0:n1], ref, "bf16", f"tile ({m0},{n0})", ref64)
+
+
 def test_plan():
     plan = binding.gemm_mx_plan(4096, 4096, 4096, binding.GEMM_E4M3)
     assert (plan["cta_group"], plan["block_m"], plan["block_n"]) == (2, 256, 224)
