@@ -3,7 +3,12 @@
 // One persistent, warp-specialised kernel computes D = A.B^T (B stored N x K,
 // K-major) or D = A.B (B stored K x N, MN-major) with FP16/BF16 operands, an
 // FP32 accumulator in Tensor Memory and a 16-bit output; with F8 set it takes
-// FP8 (E4M3 / E5M2) A and B, K-major, and writes round(alpha * A.B^T).
+// FP8 (E4M3 / E5M2) A and B, K-major, and writes round(alpha * A.B^T); with MX
+// also set every 32 K elements of each row of A and B carry a UE8M0 scale
+// (block-scaled FP8, "TIRx: A Unified Tile Primitive ML Compiler", kernel
+// performance), which the tensor core applies (kind::mxf8f6f4.block_scale):
+// each stage then also carries the k-block's scales, which the MMA issuer
+// copies into TMEM (tcgen05.cp) before its four MMAs.
 //
 // Structure, and the passages it follows:
 //   * Operands move GMEM -> SMEM by TMA into a ring of STAGES slots, 128-byte
@@ -32,7 +37,8 @@
 //     epilogue of tile i overlaps the mainloop of tile i+1 ("write back without
 //     blocking the next tile", Take away 1).
 //   * Epilogue: tcgen05.ld -> FP32 registers -> cvt.rn to 16 bit -> 128-byte
-//     swizzled SMEM staging (two buffers per warp, outside the load ring) ->
+//     swizzled SMEM staging (two buffers per warp, one with MX, outside the
+//     load ring) ->
 //     TMA store, which clips rows/columns outside D (TileFoundry section 5).
 //     D is never cleared: every tile is written exactly once (section 6).
 //
