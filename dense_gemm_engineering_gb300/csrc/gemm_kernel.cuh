@@ -331,7 +331,9 @@ __device__ __forceinline__ void settle_after_abort() {
 
 // Count one finished K-range of a tail tile.  The counter word holds
 // (epoch << 32 | count); a word tagged with another launch's epoch counts as
-// zero, so the workspace never needs clearing between launches.  Returns the
+// zero, and the range that finishes last resets the word to zero, so the
+// workspace never needs clearing between launches (nor between replays of a
+// captured launch, which repeat its epoch).  Returns the
 // number of ranges counted before this one (split - 1 means "this was the
 // last").  No thread ever waits for another here.
 __device__ __forceinline__ uint32_t count_range_done(unsigned long long* word, uint32_t epoch) {
@@ -771,6 +773,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 uint32_t before = 0;
                 if (lane == 0) before = count_range_done(args.counters + quad, args.epoch);
                 before = __shfl_sync(0xffffffffu, before, 0);
+                // The last range resets the word: every range has counted, so
+                // nothing else touches it in this launch, and a later launch
+                // that carries the same epoch (a CUDA graph replaying this one)
+                // starts from zero.
+                if (before == uint32_t(args.split - 1) && lane == 0) atomicExch(args.counters + quad, 0ull);
                 if (before != uint32_t(args.split - 1)) {
                     release(ab);  // another range finishes this block of D
                 } else if (u + num_clusters >= units &&

@@ -438,3 +438,29 @@ def test_multicast_option_limits():
         with pytest.raises(binding.GemmError) as e:
             binding.gemm_abt(A, B, options=bad)
         assert e.value.status == -8
+
+
+def test_cuda_graph_capture_and_replay():
+    # The launch is one cudaLaunchKernelEx on the caller's stream with the tile
+    # descriptors as parameters, so a CUDA graph can capture it: a replay
+    # recomputes D from whatever the captured buffers hold at replay time.
+    M, N, K = 1024, 1536, 2048
+    A1, B1 = inputs.operands(M, N, K, "abt", "f16", "uniform", 51)
+    A2, B2 = inputs.operands(M, N, K, "abt", "f16", "uniform", 52)
+    dA, dB = to_device(A1, "f16"), to_device(B1, "f16")
+    D = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    binding.gemm_abt(dA, dB, D)  # first call outside the capture: plan and attributes cached
+    torch.cuda.synchronize()
+    D.fill_(7.0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.gemm_abt(dA, dB, D)
+    g.replay()
+    torch.cuda.synchronize()
+    check_close(from_device(D), oracle.gemm(A1, B1, layout="abt", dtype="f16"), "f16", "replay 1")
+    dA.copy_(to_device(A2, "f16"))
+    dB.copy_(to_device(B2, "f16"))
+    g.replay()
+    torch.cuda.synchronize()
+    check_close(from_device(D), oracle.gemm(A2, B2, layout="abt", dtype="f16"), "f16", "replay 2")
+    assert binding.gemm_device_status(clear=True) == 0

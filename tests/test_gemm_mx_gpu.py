@@ -321,3 +321,20 @@ def test_scale_argument_errors():
     assert lib.gemm_mx_run(A.data_ptr(), B.data_ptr(), S, S, D.data_ptr(), M, N, K, K, K, N,
                            binding.GEMM_BF16, binding.GEMM_BF16, 1.0, None, None) == -2
     torch.cuda.synchronize()
+
+
+def test_cuda_graph_capture_and_replay():
+    M, N, K = 512, 672, 1024
+    A, B, SA, SB = inputs.mx_operands(M, N, K, "e4m3", "uniform", 53)
+    dA, dB, dSA, dSB = to_dev8(A), to_dev8(B), pack(SA, K), pack_b(SB, K)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    binding.gemm_mx(dA, dB, dSA, dSB, D, fmt="e4m3")  # plan cached outside the capture
+    torch.cuda.synchronize()
+    D.fill_(7.0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.gemm_mx(dA, dB, dSA, dSB, D, fmt="e4m3")
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle.gemm_mx(A, B, SA, SB, fmt="e4m3", out_dtype="bf16")
+    check_close(from_device(D), ref, "bf16", "graph replay")

@@ -66,6 +66,29 @@ def test_no_alloc_matches_workspace_path_twice(case):
     assert binding.gemm_device_status(clear=True) == 0
 
 
+def test_no_alloc_split_tail_in_a_cuda_graph():
+    # A captured launch replays with the same epoch for its split-tail
+    # counters; the range that finishes a tile resets its counter, so every
+    # replay writes the whole of D again.
+    M, N, K, opts = 1024, 1024, 2048, {"cta_group": 2, "max_clusters": 7, "tail_split": 3}
+    A, B = inputs.operands(M, N, K, "abt", "f16", "uniform", 124)
+    dA, dB = to_device(A, "f16"), to_device(B, "f16")
+    ref_bits = from_device(binding.gemm_run(dA, dB, layout=0, options=opts))
+    D = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    assert _raw_no_alloc(dA, dB, D, 0, opts) == 0  # plan cached outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        status = _raw_no_alloc(dA, dB, D, 0, opts)
+    assert status == 0
+    for i in range(3):
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        check_close(from_device(D), ref_bits, "f16", f"graph replay {i}")
+    assert binding.gemm_device_status(clear=True) == 0
+
+
 def test_no_alloc_rejects_plans_beyond_its_scratch():
     # 4096^3 in 256-wide tiles on 76 clusters leaves 28 tail tiles; a forced
     # 16-way split would need 28 x 16 x 256 KiB = 112 MiB of scratch, beyond the
