@@ -393,13 +393,32 @@ def oracle_sample(cfg, X, target_s: float):
     t_probe = max(time.perf_counter() - t0, 1e-6)
     rows = max(probe_rows, min(cfg.M, int(target_s / (t_probe / probe_rows))))
     t0 = time.perf_counter()
-    oracle_rows(orc, cfg, X, (0, rows))
+    ref = oracle_rows(orc, cfg, X, (0, rows))
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cfg.N * cfg.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
             "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"rows 0..{rows} of D ({rows} x {cfg.N} outputs, K={cfg.K}), "
-                      f"{dt:.1f} s"}, rows, dt
+                      f"{dt:.1f} s"}, rows, dt, ref
+
+
+def check_rows(cfg, got_bits, ref_bits) -> dict:
+    """The timed GEMM's D against the oracle's rows from the CPU-baseline leg:
+    |got - ref| <= atol + rtol |ref| (the parity tests' bound)."""
+    import numpy as np
+    import torch
+
+    def dec(b):
+        t = torch.from_numpy(np.ascontiguousarray(b).view(np.int16))
+        return t.view(torch_dtype(cfg.out)).double().numpy()
+
+    got, ref = dec(got_bits), dec(ref_bits)
+    err = np.abs(got - ref)
+    bound = cfg.atol + cfg.rtol * np.abs(ref)
+    return {"rows": int(ref.shape[0]), "max_abs_err": float(err.max()),
+            "max_err_over_bound": float((err / bound).max()),
+            "within_tolerance": bool((err <= bound).all()),
+            "bound": f"|D - oracle| <= {cfg.atol} + {cfg.rtol} |oracle|, element by element"}
 
 
 def oracle_single_core(cfg, X, rows: int = 64):
@@ -459,7 +478,7 @@ def run_reference(args, cfg):
     orc = oracle.get()
     # Size each step so that warm-up + steps end within about two minutes.
     step_s = max(0.02, min(1.5, 120.0 / max(1, args.warmup + args.steps)))
-    _, rows, dt = oracle_sample(cfg, X, target_s=step_s)
+    _, rows, dt, _ = oracle_sample(cfg, X, target_s=step_s)
     step_rows = rows
     times = []
     for i in range(args.warmup + args.steps):
@@ -671,7 +690,10 @@ def run_ours(args, cfg):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu, _, _ = oracle_sample(cfg, X, args.cpu_seconds)
+        cpu, rows, _, ref = oracle_sample(cfg, X, args.cpu_seconds)
+        # the timed launches' D against those oracle rows
+        cpu["check"] = check_rows(cfg, dD[:rows].contiguous().view(torch.int16).cpu().numpy()
+                                  .view(np.uint16), ref)
         # the same oracle on one core over 64 rows, whole-D time extrapolated
         cpu["single_core"] = oracle_single_core(cfg, X)
 

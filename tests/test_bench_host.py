@@ -157,3 +157,17 @@ def test_single_core_oracle_baseline_restores_threads():
     assert oracle.get().num_threads() == before
     assert ctx["cores"] == 1 and ctx["value"] > 0
     assert ctx["extrapolated_full_s"] > 0 and "rows 0..16" in ctx["sample"]
+
+
+def test_check_rows_against_the_oracle():
+    import oracle
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.CONFIGS[0]  # 128 x 128 x 64 FP16
+    X = bench.make_inputs(cfg)
+    ref = bench.oracle_rows(oracle.get(), cfg, X, (0, 8))
+    ok = bench.check_rows(cfg, ref.copy(), ref)
+    assert ok["within_tolerance"] and ok["max_abs_err"] == 0.0 and ok["rows"] == 8
+    bad = ref.copy()
+    bad[3, 5] ^= np.uint16(0x4000)  # flip a high exponent bit
+    assert not bench.check_rows(cfg, bad, ref)["within_tolerance"]
