@@ -532,3 +532,44 @@ def gemm_run_no_alloc(A, B, D, *, layout: int = LAYOUT_ABT, options=None, stream
     if st != 0:
         raise GemmError(st, "gemm_run_no_alloc")
     return D
+
+
+# The C entry points' names for the FP8 and block-scaled calls (the functions
+# above take torch tensors; these are the same functions under the C names).
+def gemm_fp8_run(A, B, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0, options=None,
+                 stream=None, workspace="auto"):
+    """gemm_fp8_run / gemm_fp8_run_workspace of the C ABI (see gemm_fp8)."""
+    return gemm_fp8(A, B, D, fmt=fmt, out_dtype=out_dtype, alpha=alpha, options=options,
+                    stream=stream, workspace=workspace)
+
+
+def gemm_fp8_abt(A, B, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0, stream=None):
+    """gemm_fp8_abt of the C ABI: gemm_fp8 with the default plan."""
+    return gemm_fp8(A, B, D, fmt=fmt, out_dtype=out_dtype, alpha=alpha, stream=stream)
+
+
+def gemm_mx_run(A, B, SA, SB, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0,
+                options=None, stream=None):
+    """gemm_mx_run of the C ABI (see gemm_mx)."""
+    return gemm_mx(A, B, SA, SB, D, fmt=fmt, out_dtype=out_dtype, alpha=alpha, options=options,
+                   stream=stream)
+
+
+def gemm_mx_abt(A, B, SA, SB, D=None, *, fmt=None, out_dtype=None, alpha: float = 1.0,
+                stream=None):
+    """gemm_mx_abt of the C ABI: gemm_mx with the default plan."""
+    return gemm_mx(A, B, SA, SB, D, fmt=fmt, out_dtype=out_dtype, alpha=alpha, stream=stream)
+
+
+def gemm_run_workspace(A, B, D=None, *, layout: int = LAYOUT_ABT, options=None, stream=None,
+                       workspace="auto"):
+    """gemm_run_workspace of the C ABI: gemm_run, whose `workspace` argument is
+    the caller's buffer (or "auto")."""
+    return gemm_run(A, B, D, layout=layout, options=options, stream=stream, workspace=workspace)
+
+
+gemm_fp8_run_workspace = gemm_fp8_run
+gemm_mx_scales_size = mx_scales_size
+gemm_mx_scales_b_size = mx_scales_b_size
+gemm_mx_pack_scales = mx_pack_scales
+gemm_mx_pack_scales_b = mx_pack_scales_b

@@ -269,3 +269,9 @@ def test_mx_scales_b_size_and_pack_errors(lib):
     assert pack(0, 4, 64, 2, Q, None) == -1
     assert pack(P, 4, 64, 2, Q + 4, None) == -4
     assert pack(P + 4, 4, 64, 2, P, None) == -5
+
+
+def test_binding_offers_every_c_entry_point_by_name():
+    # every function include/gemm.h declares has a Python callable of the same name
+    missing = [name for name in binding.EXPORTS if not callable(getattr(binding, name, None))]
+    assert not missing, missing
