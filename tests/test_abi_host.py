@@ -153,6 +153,23 @@ def test_smem_carve_up_is_disjoint():
         assert spans[-1][1] + (2 * stages + 4) * 8 + 8 + 1024 <= 232448
 
 
+def test_block_scaled_smem_carve_up_is_disjoint_and_aligned():
+    # Block-scaled FP8, 2-CTA 224-wide tiles, 6 stages: A and B rings (128-byte
+    # K rows), A-scale atoms, B-scale blocks, one epilogue buffer per warp
+    # (1 KiB aligned: it is 128-byte swizzled), barriers; within 227 KiB.
+    stages, a, b = 6, 128 * 128, 112 * 128
+    off_sfa = stages * (a + b)
+    off_sfb = off_sfa + stages * 512
+    off_epi = (off_sfb + stages * 4096 + 1023) // 1024 * 1024
+    off_bar = off_epi + 4 * 4096
+    spans = [(0, stages * a), (stages * a, off_sfa), (off_sfa, off_sfb),
+             (off_sfb, off_sfb + stages * 4096), (off_epi, off_bar)]
+    for (s0, e0), (s1, e1) in zip(spans, spans[1:]):
+        assert e0 <= s1 and s0 < e0
+    assert off_sfa % 512 == 0 and off_sfb % 512 == 0 and off_epi % 1024 == 0
+    assert off_bar + (2 * stages + 4 + 4) * 8 + 8 + 1024 <= 232448
+
+
 def test_tile_map_limits_and_large_grids(lib):
     # The scheduler's index arithmetic is 32-bit: 2^31 tiles or more is a shape
     # error; just below the limit the map still covers the far corner.
