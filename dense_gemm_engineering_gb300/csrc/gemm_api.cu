@@ -203,8 +203,8 @@ struct Stages {
     static constexpr int value = stages_for(CG, BN, CONS);
 };
 
-template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int MC = 1, int F8 = 0>
-using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, MC, F8>;
+template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int F8 = 0>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, F8>;
 
 // Block-scaled FP8 (MX) stages: a stage also holds 512 B of A scales and the
 // tile's 4 KiB block of B scales, and the epilogue stages through one 4 KiB
@@ -213,12 +213,11 @@ constexpr int stages_for_mx(int cg, int bn) {
     return (227 * 1024 - 16384 - 1024 - 512) / (128 * 128 + (bn / cg) * 128 + 512 + 4096);
 }
 template <int CG, int BN, bool BF16, int F8>
-using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, 1, F8, true>;
+using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, F8, true>;
 
 struct Plan {
     int cg, bm, bn, stages;
     int cons;  // MMA consumers per CTA
-    int mc;    // CTA pairs per cluster sharing A by multicast
     int clusters;
     int64_t tiles;
     int group;
@@ -265,8 +264,7 @@ void plan_split(Plan* p, int requested, bool have_workspace) {
     p->whole_units = p->tiles;
     p->split = 1;
     const int64_t tail = p->clusters > 0 ? p->tiles % p->clusters : 0;
-    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0 && p->cons == 1 &&
-        p->mc == 1) {
+    if (have_workspace && tail > 0 && requested >= 2 && (p->bn % 64) == 0 && p->cons == 1) {
         int64_t s = requested;
         if (s > kMaxSplit) s = kMaxSplit;
         if (s > p->k_blocks) s = p->k_blocks;
@@ -289,7 +287,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
              int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha,
              void* workspace, cudaStream_t stream, const void* SA, const void* SB) {
     CUtensorMap ma, mb, md;
-    if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_BOX_ROWS))
+    if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_ROWS))
         return GEMM_ERR_CUDA;
     if constexpr (!C::B_MN) {
         if (!encode_2d(&mb, B, in_fmt, uint64_t(K), uint64_t(N), uint64_t(ldb), C::BK, C::B_ROWS))
@@ -309,7 +307,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     args.K = int32_t(K);
     args.k_blocks = int32_t((K + C::BK - 1) / C::BK);
     args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
-    args.grid.n_tiles = int32_t((N + C::BN_CLUSTER - 1) / C::BN_CLUSTER);
+    args.grid.n_tiles = int32_t((N + C::BN - 1) / C::BN);
     args.grid.group = p.group;
     args.whole_units = p.whole_units;
     args.split = p.split;
@@ -340,14 +338,14 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
 // Dispatch on (cta_group, block_n, layout, dtype, FP8 input) to one template
 // instance.  `bf16` is the output type (and the input type when f8 == 0).
 template <template <class> class Fn, class... Ts>
-int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, int f8, Ts&&... ts) {
+int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, Ts&&... ts) {
     if (f8 != 0) {
-        // FP8 inputs: K-major B, one consumer, no multicast; 2-CTA 256 / 224-wide
-        // and 1-CTA 256-wide tiles.
-        if (b_mn || cons != 1 || mc != 1) return GEMM_ERR_OPTION;
+        // FP8 inputs: K-major B, one consumer; 2-CTA 256 / 224-wide and 1-CTA
+        // 256-wide tiles.
+        if (b_mn || cons != 1) return GEMM_ERR_OPTION;
 #define GB300_CASE8(CG_, BN_, F8_, BF_)                                                  \
     if (cg == CG_ && bn == BN_ && f8 == F8_ && bf16 == BF_)                              \
-        return Fn<Cfg<CG_, BN_, false, BF_, 1, 1, F8_>>::call(std::forward<Ts>(ts)...);
+        return Fn<Cfg<CG_, BN_, false, BF_, 1, F8_>>::call(std::forward<Ts>(ts)...);
 #define GB300_CASES8(CG_, BN_) \
     GB300_CASE8(CG_, BN_, 1, false) GB300_CASE8(CG_, BN_, 1, true) \
     GB300_CASE8(CG_, BN_, 2, false) GB300_CASE8(CG_, BN_, 2, true)
@@ -358,15 +356,6 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int mc, int f8, Ts&
 #undef GB300_CASE8
         return GEMM_ERR_OPTION;
     }
-#define GB300_CASEMC(MN_, BF_)                                                           \
-    if (mc == 2 && cons == 1 && cg == 2 && bn == 256 && b_mn == MN_ && bf16 == BF_)      \
-        return Fn<Cfg<2, 256, MN_, BF_, 1, 2>>::call(std::forward<Ts>(ts)...);
-    GB300_CASEMC(false, false)
-    GB300_CASEMC(false, true)
-    GB300_CASEMC(true, false)
-    GB300_CASEMC(true, true)
-#undef GB300_CASEMC
-    if (mc != 1) return GEMM_ERR_OPTION;
 #define GB300_CASE(CG_, BN_, MN_, BF_)                                                   \
     if (cons == 1 && cg == CG_ && bn == BN_ && b_mn == MN_ && bf16 == BF_)               \
         return Fn<Cfg<CG_, BN_, MN_, BF_>>::call(std::forward<Ts>(ts)...);
@@ -461,13 +450,14 @@ int check_options(const gemm_options_t* o) {
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
     if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
     if (o->consumers < 0 || o->consumers > 2) return GEMM_ERR_OPTION;
-    if (o->multicast < 0 || o->multicast > 2) return GEMM_ERR_OPTION;
+    // multicast: kept in the struct for layout stability; 0 or 1 (no multicast) only.
+    if (o->multicast < 0 || o->multicast > 1) return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
 int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
     int n = 0;
-    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, 1, f8_code(dtype), dev,
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, f8_code(dtype), dev,
                           sm_count, &n) != GEMM_OK)
         return 0;
     return n;
@@ -520,9 +510,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
         // Block-scaled FP8: 2-CTA clusters, 224-wide tiles, whole tiles only.
         if (!is_fp8(dtype) || b_layout != 0) return GEMM_ERR_DTYPE;
         if (o && ((o->cta_group && o->cta_group != 2) || (o->block_n && o->block_n != 224) ||
-                  o->consumers > 1 || o->multicast > 1 || o->tail_split > 1))
+                  o->consumers > 1 || o->tail_split > 1))
             return GEMM_ERR_OPTION;
-        p->mc = 1;
         p->cg = 2;
         p->cons = 1;
         p->bm = 256;
@@ -542,18 +531,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
         plan_split(p, 0, false);
         return GEMM_OK;
     }
-    p->mc = (o && o->multicast) ? o->multicast : 1;
-    p->cg = (o && o->cta_group) ? o->cta_group : ((M <= 128 && p->mc == 1) ? 1 : 2);
+    p->cg = (o && o->cta_group) ? o->cta_group : (M <= 128 ? 1 : 2);
     p->cons = (o && o->consumers) ? o->consumers : 1;
-    if (p->mc == 2 && (p->cg != 2 || p->cons != 1 || (o && o->block_n && o->block_n != 256)))
-        return GEMM_ERR_OPTION;
-    if (is_fp8(dtype) && (p->mc != 1 || p->cons != 1)) return GEMM_ERR_OPTION;
+    if (is_fp8(dtype) && p->cons != 1) return GEMM_ERR_OPTION;
     p->bm = 128 * p->cg * p->cons;
     if (p->cons == 2) {
         // Two consumers: 2-CTA clusters, 256-wide tiles only.
         if (p->cg != 2 || (o && o->block_n && o->block_n != 256)) return GEMM_ERR_OPTION;
-        p->bn = 256;
-    } else if (p->mc == 2) {
         p->bn = 256;
     } else if (o && o->block_n) {
         p->bn = o->block_n;
@@ -564,13 +548,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     }
     p->group = (o && o->raster_group) ? o->raster_group : 16;
     const int64_t m_tiles = (M + p->bm - 1) / p->bm;
-    const int64_t n_tiles = (N + p->bn * p->mc - 1) / (p->bn * p->mc);
+    const int64_t n_tiles = (N + p->bn - 1) / p->bn;
     p->tiles = m_tiles * n_tiles;
     if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
     if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
     int max_clusters = 0;
-    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, p->mc,
-                           f8_code(dtype), dev, di.sm_count, &max_clusters);
+    st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, f8_code(dtype),
+                           dev, di.sm_count, &max_clusters);
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
     p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
@@ -663,8 +647,7 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
         return dispatch_mx<RunFn>(p.cg, p.bn, out_dtype == GEMM_BF16, f8_code(in_fmt), p, A, B, D, M,
                                   N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace, stream,
                                   SA, SB);
-    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, p.mc,
-                           f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
                            alpha, workspace, stream, static_cast<const void*>(nullptr),
                            static_cast<const void*>(nullptr));
 }

@@ -77,15 +77,11 @@ enum : uint32_t {
     kRoleSelfTest = 5u
 };
 
-template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int MC_ = 1,
-          int F8_ = 0, bool MX_ = false>
+template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int F8_ = 0,
+          bool MX_ = false>
 struct KernelConfig {
     static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
-    // CTA pairs per cluster: 1, or 2 side by side along N that share A — each
-    // CTA loads half of its A rows and multicasts them to its counterpart in
-    // the other pair, so A's L2 -> SMEM traffic halves.
-    static constexpr int MC = MC_;
-    static constexpr int CLUSTER = CG * MC;   // CTAs per cluster
+    static constexpr int CLUSTER = CG;        // CTAs per cluster: the tile's CTAs
     // MMA consumers per CTA: 1, or 2 ("TIRx GEMM on Blackwell", V9: two MMAs on
     // different A rows share each staged B tile; each CTA holds 256 A rows).
     static constexpr int CONS = CONS_;
@@ -191,15 +187,12 @@ struct KernelConfig {
     static_assert((BN / CG) % 16 == 0, "each CTA's share of B is whole 16-row SW128 groups");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(CONS == 1 || CONS == 2, "one or two MMA consumers");
-    static_assert(MC == 1 || (MC == 2 && CG == 2 && CONS == 1), "A multicast pairs 2-CTA, 1-consumer tiles");
-    static constexpr int A_BOX_ROWS = A_ROWS / MC;  // A rows per TMA issue
-    static constexpr int BN_CLUSTER = BN * MC;      // columns of a cluster's tile
     static_assert(CONS * (FULL_CHUNKS + (HALF_CHUNK ? 1 : 0)) * EPI_BUF_BYTES <=
                       PIECES_PER_WARP * PIECE_BYTES,
                   "the last unit's epilogue chunks fit in each warp's share of the ring");
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
-    static_assert(!MX || (F8 && BN == 224 && CONS == 1 && MC == 1 && !B_MN && ACC_STRIDE == 256 &&
+    static_assert(!MX || (F8 && BN == 224 && CONS == 1 && !B_MN && ACC_STRIDE == 256 &&
                           NUM_ACC == 2 && BK == 128),
                   "MX: FP8 A.Bt, 224-wide tiles (224 accumulator + 32 scale columns per buffer)");
     static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "SW128 atoms are 1 KiB");
@@ -363,10 +356,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
     const uint32_t lane = threadIdx.x % 32u;
-    const uint32_t crank = (C::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;
-    const uint32_t rank = crank & uint32_t(C::CG - 1);         // CTA within its pair
-    const uint32_t pair = crank / uint32_t(C::CG);             // pair within the cluster
-    const uint32_t pair_leader = crank & ~uint32_t(C::CG - 1);  // cluster rank of the pair's leader
+    const uint32_t rank = (C::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;  // CTA within its pair
     const bool leader = (rank == 0u);
     const int64_t cluster_id = blockIdx.x / C::CLUSTER;
     const int64_t num_clusters = gridDim.x / C::CLUSTER;
@@ -386,7 +376,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp == 0 && lane == 0) {
         for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
             ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
-            ptx::mbar_init(empty_bar(s), uint32_t(C::MC));  // one tcgen05.commit per pair
+            ptx::mbar_init(empty_bar(s), 1);  // the pair's one tcgen05.commit
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
@@ -429,7 +419,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int32_t mt, nt;
             tile_of_task(args.grid, w.tile, mt, nt);
             const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
-            const int32_t b_row = nt * C::BN_CLUSTER + int32_t(pair) * C::BN + int32_t(rank) * C::B_ROWS;
+            const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
                     ok = false;
@@ -451,18 +441,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                  b_row + 64 * c, k0);
                         }
                     } else {
-                        const uint32_t fb = ptx::map_to_rank(full_bar(s), pair_leader);
-                        if constexpr (C::MC == 1) {
-                            ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
-                        } else {
-                            // this pair's share of the A rows, to the same CTA rank of every pair
-                            uint16_t mask = 0;
-#pragma unroll
-                            for (int q = 0; q < C::MC; ++q) mask |= uint16_t(1u << (q * C::CG + rank));
-                            ptx::tma_load_2d_pair_multicast(a_dst + pair * (C::A_BOX_ROWS * 128u), &tmap_a,
-                                                            fb, k0, a_row + int32_t(pair) * C::A_BOX_ROWS,
-                                                            mask);
-                        }
+                        const uint32_t fb = ptx::map_to_rank(full_bar(s), 0u);  // the leader's barrier
+                        ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
                         if constexpr (!C::B_MN) {
                             ptx::tma_load_2d_pair(b_dst, &tmap_b, fb, k0, b_row);
                         } else {
@@ -484,7 +464,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             ptx::tma_load_2d(sfa_dst, &tmap_sa, full_bar(s), kb * 128, a_row / 128);
                             ptx::tma_load_2d(sfb_dst, &tmap_sb, full_bar(s), 0, sfb_block * 4);
                         } else {
-                            const uint32_t fb = ptx::map_to_rank(full_bar(s), pair_leader);
+                            const uint32_t fb = ptx::map_to_rank(full_bar(s), 0u);
                             ptx::tma_load_2d_pair(sfa_dst, &tmap_sa, fb, kb * 128, a_row / 128);
                             ptx::tma_load_2d_pair(sfb_dst, &tmap_sb, fb, 0, sfb_block * 4);
                         }
@@ -563,7 +543,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             }
                         }
                         // slot free (in every CTA that received data for it) once these MMAs finish
-                        ptx::mma_commit<C::CG>(empty_bar(s), uint16_t((1u << C::CLUSTER) - 1u));
+                        ptx::mma_commit<C::CG>(empty_bar(s), uint16_t(0x3u));
                     }
                     __syncwarp();
                     sfbuf ^= 1u;
@@ -571,7 +551,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 if (!ok) break;
                 if (ptx::elect_one_sync())
-                    ptx::mma_commit<C::CG>(acc_full_bar(ab), uint16_t(0x3u << pair_leader));  // accumulator ready
+                    ptx::mma_commit<C::CG>(acc_full_bar(ab), uint16_t(0x3u));  // accumulator ready
                 __syncwarp();
                 if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
             }
@@ -605,7 +585,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if constexpr (C::CG == 2)
-                    ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(b), pair_leader));
+                    ptx::mbar_arrive_cluster(ptx::map_to_rank(acc_empty_bar(b), 0u));
                 else
                     ptx::mbar_arrive(acc_empty_bar(b));
             }
@@ -703,7 +683,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_fence_after();
 
             const int32_t row0 = mt * C::BM + int32_t(rank) * C::A_ROWS + int32_t(quarter) * 32;
-            const int32_t col0 = nt * C::BN_CLUSTER + int32_t(pair) * C::BN;
+            const int32_t col0 = nt * C::BN;
             const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + ab * C::SLOT_COLS;
 
             // In the cluster's last unit the accumulator is not handed back: no

@@ -155,19 +155,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Same, multicast: the tile lands at the same offset in the shared memory of
-// every CTA in `cta_mask`, and each destination's completion is signalled on
-// the barrier at `cluster_bar`'s offset in that destination's pair leader.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           uint32_t cluster_bar, int32_t x,
-                                                           int32_t y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // 2-D tile store from shared memory; out-of-bounds elements are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y) {

@@ -115,11 +115,10 @@ const char* gemm_status_string(int status);
  *                 block_n 256 only), operand traffic per FLOP drops by a
  *                 quarter, and the two accumulators fill TMEM, so a tile's
  *                 epilogue no longer overlaps the next tile's MMAs.
- *   multicast     0 or 1 = one CTA pair per cluster.  2 = clusters of two
- *                 pairs side by side along N (a 256 x 512 cluster tile,
- *                 cta_group 2, block_n 256, one consumer) that share A: each
- *                 CTA loads half of its 128 A rows and multicasts them to the
- *                 same rank of the other pair, halving A's L2 -> SMEM traffic.
+ *   multicast     must be 0 or 1 (GEMM_ERR_OPTION otherwise): a cluster is
+ *                 always the CTAs of one tile, and every CTA loads its own
+ *                 operand tiles (no load is multicast to other CTAs).  The
+ *                 field is kept so that the structure's layout does not change.
  */
 typedef struct {
     int cta_group;

@@ -74,6 +74,7 @@ def call(A=P, B=Q, D=R, M=128, N=128, K=64, lda=64, ldb=64, ldd=128, dtype=0, la
     (dict(opts={"cta_group": 0, "block_n": 0, "raster_group": 0, "max_clusters": 0, "tail_split": 17}), -8),
     (dict(opts={"consumers": 3}), -8),
     (dict(opts={"multicast": 3}), -8),
+    (dict(opts={"multicast": 2}), -8),  # no multicast load exists
 ])
 def test_argument_errors(lib, kw, status):
     assert call(**kw) == status

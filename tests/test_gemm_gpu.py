@@ -29,11 +29,9 @@ VARIANTS = [
     {"cta_group": 1, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0,
      "consumers": 2},
-    {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0,
-     "multicast": 2},
 ]
 VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224",
-       "cg2_n256_2cons", "cg2_n256_mc2"]
+       "cg2_n256_2cons"]
 
 
 def k_major_only(variant, layout):
@@ -375,8 +373,7 @@ def _fuzz_cases(n=48, seed=2026):
         if cg == 2 and bn in (0, 256) and rng.random() < 0.4:
             opts["consumers"] = 2
         elif cg in (0, 2) and bn in (0, 256) and rng.random() < 0.4:
-            opts["multicast"] = 2
-            opts["tail_split"] = 0
+            rng.random()  # (a retired option drew here; kept so the case list is unchanged)
         pad = [int(rng.choice([0, 8, 24])) for _ in range(2)]
         cases.append((i, layout, dtype, M, N, K, opts, pad))
     return cases
@@ -408,36 +405,13 @@ def test_two_consumer_option_limits():
         assert e.value.status == -8
 
 
-def test_multicast_many_tiles_per_cluster():
-    # 256 x 512 cluster tiles, few clusters: each cluster walks many tiles, so
-    # the ring's slots are refilled across tile boundaries by both pairs.
-    for layout, dtype in (("abt", "f16"), ("ab", "bf16")):
-        opts = {"multicast": 2, "max_clusters": 3}
-        parity(1300, 1320, 640, layout, dtype, seed=17, options=opts)
-
-
-def test_multicast_n_tail_inside_second_pair():
-    # N ends inside the first pair's half of the last cluster tile: the second
-    # pair's tile lies wholly outside D and must write nothing.
-    M, N, K = 384, 520, 256
-    sentinel = 0x5A5A
-    buf = torch.full((M, 1024), sentinel, dtype=torch.int16, device="cuda")
-    D = buf.view(torch.float16)[:, :N]
-    A, B = inputs.operands(M, N, K, "abt", "f16", "uniform", 23)
-    run(A, B, "abt", "f16", options={"multicast": 2}, D=D)
-    host = buf.cpu().numpy().view(np.uint16)
-    assert (host[:, N:] == sentinel).all()
-    check_close(host[:, :N], oracle.gemm(A, B, layout="abt", dtype="f16"), "f16", "mc2 tail")
-
-
-def test_multicast_option_limits():
+def test_multicast_option_is_rejected():
+    # No TMA load is multicast: the option accepts 0 or 1 only.
     A = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
     B = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
-    for bad in ({"multicast": 2, "cta_group": 1}, {"multicast": 2, "block_n": 128},
-                {"multicast": 2, "consumers": 2}):
-        with pytest.raises(binding.GemmError) as e:
-            binding.gemm_abt(A, B, options=bad)
-        assert e.value.status == -8
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_abt(A, B, options={"multicast": 2})
+    assert e.value.status == -8
 
 
 def test_cuda_graph_capture_and_replay():
