@@ -55,6 +55,18 @@ def parse_args(argv=None):
                    help="skip the context figures (cuBLAS, warm L2, single-core oracle)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per_config leg (every other workload, measured after the "
+                        "headline)")
+    p.add_argument("--options", default=None,
+                   help="plan options (JSON object of gemm_options_t fields) for the measured "
+                        "GEMM, e.g. '{\"raster_group\": 8, \"l2_hints\": 13}'")
+    p.add_argument("--sweep", choices=["raster"], default=None,
+                   help="instead of the benchmark: time the workload under every raster order, "
+                        "group and L2-hint choice (one JSON line each, L2 flushed, CUDA events)")
+    p.add_argument("--soak-seconds", type=float, default=1.5,
+                   help="after the timed region, repeat its steps this long with the clock "
+                        "sampler still on (clock evidence under load; not timed)")
     return p.parse_args(argv)
 
 
@@ -162,6 +174,9 @@ class ClockSampler:
         self.proc = None
         self.out = None
 
+    def mark(self):
+        pass
+
     def start(self):
         try:
             self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -230,6 +245,7 @@ class NvmlSampler:
         fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
         self.reasons_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
         self.samples = []
+        self.mark_at = None
         self.stop_evt = threading.Event()
         self.thread = threading.Thread(target=self._run, daemon=True)
 
@@ -250,6 +266,10 @@ class NvmlSampler:
     def start(self):
         self.thread.start()
 
+    def mark(self):
+        """End of the timed region: later samples belong to the soak."""
+        self.mark_at = len(self.samples)
+
     def stop(self):
         self.stop_evt.set()
         self.thread.join()
@@ -260,10 +280,18 @@ class NvmlSampler:
             for bit, name in self.REASONS.items():
                 if s[3] & bit:
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
-                "sm_max_mhz": max(s[1] for s in self.samples), "samples": len(sm),
-                "power_w_max": max(s[2] for s in self.samples), "reasons": sorted(reasons),
-                "source": "NVML polled every ~2 ms during the timed region"}
+        out = {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+               "sm_max_mhz": max(s[1] for s in self.samples), "samples": len(sm),
+               "power_w_max": max(s[2] for s in self.samples),
+               "power_w_median": statistics.median(s[2] for s in self.samples),
+               "reasons": sorted(reasons),
+               "source": "NVML polled every ~2 ms during the timed region and the soak that "
+                         "repeats its steps right after it"}
+        if self.mark_at is not None:
+            timed = self.samples[:max(1, self.mark_at)]
+            out["timed_region"] = {"samples": len(timed),
+                                   "sm_mhz": statistics.median(s[0] for s in timed)}
+        return out
 
 
 def clock_sampler(uuid: str):
@@ -317,18 +345,20 @@ def operand(t, cfg):
     return t if cfg.is_fp8 else t.view(torch_dtype(cfg.dtype))
 
 
-def gemm_for(cfg):
+def gemm_for(cfg, options=None):
     """gemm(xs, d): one GEMM through the public binding on device inputs xs =
-    [A, B] (block-scaled: [A, B, SA, SB] with the scales in the tiled layout)."""
+    [A, B] (block-scaled: [A, B, SA, SB] with the scales in the tiled layout),
+    with plan `options` (None = the automatic plan)."""
     from dense_gemm_engineering_gb300 import binding
 
     if cfg.mx:
         return lambda xs, d: binding.gemm_mx(xs[0], xs[1], xs[2], xs[3], d, fmt=cfg.dtype,
-                                             alpha=cfg.alpha)
+                                             alpha=cfg.alpha, options=options)
     if cfg.is_fp8:
-        return lambda xs, d: binding.gemm_fp8(xs[0], xs[1], d, fmt=cfg.dtype, alpha=cfg.alpha)
+        return lambda xs, d: binding.gemm_fp8(xs[0], xs[1], d, fmt=cfg.dtype, alpha=cfg.alpha,
+                                              options=options)
     f = binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
-    return lambda xs, d: f(xs[0], xs[1], d)
+    return lambda xs, d: f(xs[0], xs[1], d, options=options)
 
 
 def device_inputs(cfg, dX, packed=None):
@@ -344,14 +374,24 @@ def device_inputs(cfg, dX, packed=None):
     return xs
 
 
-def oracle_rows(orc, cfg, X, rows):
+def oracle_rows(orc, cfg, X, rows, want_f64=False):
     A, B = X[0], X[1]
     if cfg.mx:
         return orc.gemm_mx(A, B, X[2], X[3], fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha,
-                           rows=rows)
+                           rows=rows, want_f64=want_f64)
     if cfg.is_fp8:
-        return orc.gemm_fp8(A, B, fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha, rows=rows)
-    return orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=rows)
+        return orc.gemm_fp8(A, B, fmt=cfg.dtype, out_dtype=cfg.out, alpha=cfg.alpha, rows=rows,
+                            want_f64=want_f64)
+    return orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=rows, want_f64=want_f64)
+
+
+def oracle_sum_abs(orc, cfg, X, rows):
+    """binary64 sums of |A[i,k] B'[j,k]| over k for D's rows (16-bit inputs): the
+    oracle run on |A| and |B| (sign bits cleared)."""
+    import numpy as np
+
+    A, B = (np.asarray(x, dtype=np.uint16) & np.uint16(0x7FFF) for x in X[:2])
+    return orc.gemm(A, B, layout=cfg.layout, dtype=cfg.dtype, rows=rows, want_f64=True)[1]
 
 
 def peak_for(cfg, peaks):
@@ -393,18 +433,21 @@ def oracle_sample(cfg, X, target_s: float):
     t_probe = max(time.perf_counter() - t0, 1e-6)
     rows = max(probe_rows, min(cfg.M, int(target_s / (t_probe / probe_rows))))
     t0 = time.perf_counter()
-    ref = oracle_rows(orc, cfg, X, (0, rows))
+    ref, ref64 = oracle_rows(orc, cfg, X, (0, rows), want_f64=True)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cfg.N * cfg.K
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
             "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"rows 0..{rows} of D ({rows} x {cfg.N} outputs, K={cfg.K}), "
-                      f"{dt:.1f} s"}, rows, dt, ref
+                      f"{dt:.1f} s"}, rows, dt, (ref, ref64)
 
 
-def check_rows(cfg, got_bits, ref_bits) -> dict:
-    """The timed GEMM's D against the oracle's rows from the CPU-baseline leg:
-    |got - ref| <= atol + rtol |ref| (the parity tests' bound)."""
+def check_rows(cfg, got_bits, ref_bits, ref64=None, sum_abs=None) -> dict:
+    """The timed GEMM's D against the oracle's rows: |got - ref| <= atol + rtol
+    |ref| (the parity tests' bound), element by element.  With the oracle's
+    unrounded binary64 sums (ref64), also the largest error in output ulps
+    (max_ulp), and with the sums of |terms| (16-bit inputs) the strict bound
+    |got - ref64| <= 1 ulp + 2^-16 sum|terms| that a lost K = 16 slice fails."""
     import numpy as np
     import torch
 
@@ -415,10 +458,22 @@ def check_rows(cfg, got_bits, ref_bits) -> dict:
     got, ref = dec(got_bits), dec(ref_bits)
     err = np.abs(got - ref)
     bound = cfg.atol + cfg.rtol * np.abs(ref)
-    return {"rows": int(ref.shape[0]), "max_abs_err": float(err.max()),
-            "max_err_over_bound": float((err / bound).max()),
-            "within_tolerance": bool((err <= bound).all()),
-            "bound": f"|D - oracle| <= {cfg.atol} + {cfg.rtol} |oracle|, element by element"}
+    out = {"rows": int(ref.shape[0]), "max_abs_err": float(err.max()),
+           "max_err_over_bound": float((err / bound).max()),
+           "within_tolerance": bool((err <= bound).all()),
+           "bound": f"|D - oracle| <= {cfg.atol} + {cfg.rtol} |oracle|, element by element"}
+    if ref64 is not None:
+        emin, p = (-14, 10) if cfg.out == "f16" else (-126, 7)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref64), 2.0 ** emin))) - p)
+        e64 = np.abs(got - ref64)
+        out["max_ulp"] = float((e64 / ulp).max())
+        if sum_abs is not None:
+            strict = ulp + 2.0 ** -16 * sum_abs
+            out["within_strict"] = bool((e64 <= strict).all())
+            out["max_err_over_strict"] = float((e64 / strict).max())
+            out["strict_bound"] = ("|D - exact| <= 1 ulp(exact) + 2^-16 sum_k |A B'|, exact = the "
+                                   "oracle's unrounded binary64 sum")
+    return out
 
 
 def oracle_single_core(cfg, X, rows: int = 64):
@@ -466,6 +521,210 @@ def time_launches(fn, count, dev, flush=None):
     torch.cuda.synchronize(dev)
     t = [a.elapsed_time(b) for a, b in evs]
     return sum(t) / len(t)
+
+
+def soak(step, dev, seconds: float) -> int:
+    """Repeat `step` back to back for about `seconds` (not timed), so that the
+    clock sampler sees the timed region's load for long enough; returns the
+    number of steps run."""
+    import torch
+
+    n, t_end = 0, time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        n += 20
+        torch.cuda.synchronize(dev)
+    return n
+
+
+def clock_from_probes(rows) -> dict:
+    """SM clock inside the kernel from gemm_run_clock_probe records
+    [clock64 start, globaltimer start, clock64 end, globaltimer end]."""
+    mhz = [(c1 - c0) / (t1 - t0) * 1e3 for c0, t0, c1, t1 in rows if t1 > t0 and c1 > c0]
+    if not mhz:
+        return None
+    return {"launches": len(mhz), "sm_mhz_median": statistics.median(mhz),
+            "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+            "source": "first CTA's %clock64 and %globaltimer at kernel start and end "
+                      "(gemm_run_clock_probe), the soak's launches"}
+
+
+def library_gemm(cfg, xs, dX, dev):
+    """The vendor library's GEMM on the same device tensors (context only):
+    (callable, description)."""
+    import torch
+
+    from dense_gemm_engineering_gb300 import binding
+
+    dA, dB = xs[0], xs[1]
+    if cfg.mx:
+        # cuBLASLt's block-scaled FP8 GEMM through torch: the layout of A's
+        # scales is the one torch._scaled_mm takes for 32-element UE8M0
+        # scales, for both operands
+        f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
+        e8 = getattr(torch, "float8_e8m0fnu", None)
+        a8, b8 = dA.view(f8), dB.view(f8)
+        sa = xs[2][:binding.mx_scales_size(cfg.M, cfg.K)]
+        sb = binding.mx_pack_scales(dX[3], cfg.K)[:binding.mx_scales_size(cfg.N, cfg.K)]
+        mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa.view(e8),  # noqa: E731
+                                      scale_b=sb.view(e8), out_dtype=torch_dtype(cfg.out))
+        return mm, "torch._scaled_mm (cuBLASLt block-scaled FP8, UE8M0 per 32)"
+    if cfg.is_fp8:
+        # cuBLASLt's FP8 GEMM through torch (scales of 1, alpha folded in by A's scale)
+        f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
+        a8, b8 = dA.view(f8), dB.view(f8)
+        one = torch.tensor(1.0, device=dev)
+        sa = torch.tensor(float(cfg.alpha), device=dev)
+        mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=one,  # noqa: E731
+                                      out_dtype=torch_dtype(cfg.out))
+        return mm, "torch._scaled_mm (cuBLASLt FP8)"
+    if cfg.layout == "abt":
+        return (lambda: torch.mm(dA, dB.t())), "torch.mm (cuBLAS)"
+    return (lambda: torch.mm(dA, dB)), "torch.mm (cuBLAS)"
+
+
+# Workloads measured after the headline, one record each under per_config.
+PER_CONFIG = ["single_tile_128x128x64_f16_abt", "kloop_256x256x1024_f16_abt",
+              "rect_8192x17408x5120_bf16_ab", "ragged_3000x5000x4000_f16_abt",
+              "fp8_square_4096x4096x4096_e4m3_abt", "fp8_8192x8192x8192_e4m3_abt",
+              "mx_square_4096x4096x4096_e4m3_abt", "mx_8192x8192x8192_e4m3_abt"]
+
+
+def check_row_ranges(M: int):
+    """Rows of D the per-config check compares with the oracle: the first two,
+    two in the middle and the last two."""
+    cand = [(0, 2), (M // 2, M // 2 + 2), (M - 2, M)]
+    out = []
+    for r0, r1 in cand:
+        r0, r1 = max(0, r0), min(M, r1)
+        if r1 > r0 and all(r1 <= a or r0 >= b for a, b in out):
+            out.append((r0, r1))
+    return out
+
+
+def measure_config(cfg, dev, flush, count, peaks) -> dict:
+    """One workload under the headline's protocol (L2 flushed before every
+    launch, CUDA events around each launch), interleaved with the vendor
+    library's GEMM on the same tensors, and its D checked against the oracle
+    on a few whole rows."""
+    import numpy as np
+    import torch
+
+    import oracle as oracle_pkg
+    from dense_gemm_engineering_gb300 import binding
+
+    X = make_inputs(cfg)
+    dX = [storage_tensor(x).to(dev) for x in X]
+    xs = device_inputs(cfg, dX)
+    dD = torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev)
+    gemm = gemm_for(cfg)
+    mm, mm_what = library_gemm(cfg, xs, dX, dev)
+    ours, lib = [], []
+    for _ in range(2):  # interleaved: ours, library, ours, library
+        ours.append(time_launches(lambda: gemm(xs, dD), count, dev, flush))
+        try:
+            lib.append(time_launches(mm, count, dev, flush))
+        except (RuntimeError, TypeError) as e:
+            lib, mm_what = None, f"{mm_what} unavailable: {str(e).splitlines()[0][:120]}"
+            break
+    gemm(xs, dD)
+    in_kernel = None
+    if not cfg.is_fp8:  # the SM clock inside the kernel, same protocol, not timed
+        probes = torch.zeros((count, 4), dtype=torch.int64, device=dev)
+        for i in range(count):
+            flush.zero_()
+            binding.gemm_run_clock_probe(xs[0], xs[1], dD, probes[i],
+                                         layout=0 if cfg.layout == "abt" else 1)
+        torch.cuda.synchronize(dev)
+        in_kernel = clock_from_probes(probes.cpu().tolist())
+    torch.cuda.synchronize(dev)
+    status = binding.gemm_device_status(clear=True)
+    ms = sum(ours) / len(ours)
+    flops = 2.0 * cfg.M * cfg.N * cfg.K
+    achieved = flops / (ms / 1e3) / 1e12
+    peak, _ = peak_for(cfg, peaks)
+    orc = oracle_pkg.get()
+    got, ref, ref64, sab = [], [], [], []
+    for r0, r1 in check_row_ranges(cfg.M):
+        got.append(dD[r0:r1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+        r, r64 = oracle_rows(orc, cfg, X, (r0, r1), want_f64=True)
+        ref.append(r)
+        ref64.append(r64)
+        if not cfg.is_fp8:
+            sab.append(oracle_sum_abs(orc, cfg, X, (r0, r1)))
+    check = check_rows(cfg, np.concatenate(got), np.concatenate(ref), np.concatenate(ref64),
+                       np.concatenate(sab) if sab else None)
+    check["row_ranges"] = check_row_ranges(cfg.M)
+    if cfg.mx:
+        plan = binding.gemm_mx_plan(cfg.M, cfg.N, cfg.K,
+                                    {"e4m3": binding.GEMM_E4M3, "e5m2": binding.GEMM_E5M2}[cfg.dtype])
+    else:
+        code = {"f16": binding.GEMM_F16, "bf16": binding.GEMM_BF16, "e4m3": binding.GEMM_E4M3,
+                "e5m2": binding.GEMM_E5M2}[cfg.dtype]
+        plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, code, 0 if cfg.layout == "abt" else 1)
+    t_lib = sum(lib) / len(lib) if lib else None
+    out = {"metric": metric_for(cfg), "value": achieved, "unit": UNIT, "ms_per_step": ms,
+           "steps": 2 * count, "dtype": cfg.dtype, "out_dtype": cfg.out,
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                        "frac": achieved / peak},
+           "check": check, "device_status": status, "plan": plan, "clock_in_kernel": in_kernel,
+           "library": {"value": flops / (t_lib / 1e3) / 1e12 if t_lib else None,
+                       "ms_per_step": t_lib, "what": mm_what,
+                       "ratio_ours_over_library": (t_lib / ms) if t_lib else None}}
+    del X, dX, xs, dD
+    torch.cuda.empty_cache()
+    return out
+
+
+RASTER_SWEEP = [(order, group, hints) for order in (1, 2) for group in (4, 8, 12, 16, 24, 32)
+                for hints in (1, 3, 11, 15)]
+
+
+def run_raster_sweep(args, cfg):
+    """Time one workload under each (raster order, group, L2 hints) choice with
+    the benchmark's protocol (L2 flushed before every launch, CUDA events);
+    the automatic plan and the vendor library's GEMM are timed between them
+    for reference.  One JSON line per choice on stdout."""
+    import torch
+
+    from dense_gemm_engineering_gb300 import binding, build
+
+    if cfg.is_fp8 or cfg.mx:
+        raise SystemExit("--sweep raster takes a 16-bit workload")
+    dev = torch.device("cuda", dist_env()[2])
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load()
+    X = make_inputs(cfg)
+    dX = [storage_tensor(x).to(dev) for x in X]
+    xs = device_inputs(cfg, dX)
+    dD = torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    layout = 0 if cfg.layout == "abt" else 1
+    f = binding.gemm_abt if cfg.layout == "abt" else binding.gemm_ab
+    mm, mm_what = library_gemm(cfg, xs, dX, dev)
+    flops = 2.0 * cfg.M * cfg.N * cfg.K
+    count = max(5, min(args.steps, 20))
+    code = binding.GEMM_F16 if cfg.dtype == "f16" else binding.GEMM_BF16
+    auto = binding.gemm_plan(cfg.M, cfg.N, cfg.K, code, layout)
+
+    def emit(kind, opts, ms):
+        print(json.dumps({"sweep": "raster", "workload": cfg.name, "kind": kind, "options": opts,
+                          "ms_per_step": ms, "value": flops / (ms / 1e3) / 1e12, "unit": UNIT}),
+              flush=True)
+
+    for i, (order, group, hints) in enumerate(RASTER_SWEEP):
+        if i % 8 == 0:
+            emit("automatic", {k: auto[k] for k in ("raster_order", "raster_group", "l2_hints")},
+                 time_launches(lambda: f(xs[0], xs[1], dD), count, dev, flush))
+            emit(mm_what, None, time_launches(mm, count, dev, flush))
+        opts = {"raster_order": order, "raster_group": group, "l2_hints": hints}
+        emit("ours", opts, time_launches(lambda: f(xs[0], xs[1], dD, options=opts), count, dev,
+                                         flush))
+    if binding.gemm_device_status(clear=True) != 0:
+        raise RuntimeError("device status word set during the sweep")
+    return 0
 
 
 def run_reference(args, cfg):
@@ -605,7 +864,7 @@ def run_ours(args, cfg):
     import torch
     import torch.distributed as dist
 
-    from dense_gemm_engineering_gb300 import binding, build
+    from dense_gemm_engineering_gb300 import binding, build, configs
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -620,7 +879,8 @@ def run_ours(args, cfg):
     xs = device_inputs(cfg, dX)  # scales packed once, before anything is timed
     dA, dB = xs[0], xs[1]
     dD = torch.empty((cfg.M, cfg.N), dtype=torch_dtype(cfg.out), device=dev)
-    gemm = gemm_for(cfg)
+    options = json.loads(args.options) if args.options else None
+    gemm = gemm_for(cfg, options)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -651,7 +911,41 @@ def run_ours(args, cfg):
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
+    soak_steps = 0
+    in_kernel = None
+    if sampler:
+        # The timed region is short (tens of steps of well under a millisecond):
+        # keep its load (same steps, not timed) for a while so that the clock
+        # record holds enough samples under load.  For 16-bit workloads the
+        # soak's GEMMs also record their first CTA's clock counter and the
+        # global timer (gemm_run_clock_probe): the SM clock inside the kernel.
+        sampler.mark()
+        probes = None
+        if not cfg.is_fp8:
+            probes = torch.zeros((512, 4), dtype=torch.int64, device=dev)
+            layout = 0 if cfg.layout == "abt" else 1
+            k = [0]
+
+            def soak_step():
+                flush.zero_()
+                binding.gemm_run_clock_probe(xs[0], xs[1], dD, probes[k[0] % 512], layout=layout,
+                                             options=options)
+                k[0] += 1
+        else:
+            def soak_step():
+                flush.zero_()
+                gemm(xs, dD)
+        t_soak = time.perf_counter()
+        soak_steps = soak(soak_step, dev, args.soak_seconds)
+        t_soak = time.perf_counter() - t_soak
+        if probes is not None:
+            in_kernel = clock_from_probes(probes[:min(k[0], 512)].cpu().tolist())
     clocks = sampler.stop() if sampler else None
+    if clocks is not None:
+        clocks["soak"] = {"steps": soak_steps, "seconds": t_soak,
+                          "what": "the timed region's step (L2 flush + GEMM) repeated back to "
+                                  "back after it, not timed, sampler still on"}
+        clocks["in_kernel"] = in_kernel
     barrier()
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per_launch_ms) / len(per_launch_ms)
@@ -672,16 +966,19 @@ def run_ours(args, cfg):
     peaks, peak_src = measured_peaks()
     peak, peak_basis = peak_for(cfg, peaks)
     src_hash = kernel_source_hash()
-    traffic = recorded_traffic(cfg.name, src_hash)
+    traffic = None if options else recorded_traffic(cfg.name, src_hash)
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     flop_clk = FLOP_PER_CLK_PER_SM * (2 if cfg.is_fp8 else 1)
     nominal = props.multi_processor_count * flop_clk * sm_max * 1e6 / 1e12
     dtype_code = {"f16": binding.GEMM_F16, "bf16": binding.GEMM_BF16, "e4m3": binding.GEMM_E4M3,
                   "e5m2": binding.GEMM_E5M2}[cfg.dtype]
     if cfg.mx:
-        plan = binding.gemm_mx_plan(cfg.M, cfg.N, cfg.K, dtype_code)
+        plan = binding.gemm_mx_plan(cfg.M, cfg.N, cfg.K, dtype_code, options)
     else:
-        plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, dtype_code, 0 if cfg.layout == "abt" else 1)
+        plan = binding.gemm_plan(cfg.M, cfg.N, cfg.K, dtype_code, 0 if cfg.layout == "abt" else 1,
+                                 options)
+    if options:
+        plan["options"] = options
 
     if rank != 0:
         if world > 1:
@@ -690,10 +987,14 @@ def run_ours(args, cfg):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu, rows, _, ref = oracle_sample(cfg, X, args.cpu_seconds)
-        # the timed launches' D against those oracle rows
+        cpu, rows, _, (ref, ref64) = oracle_sample(cfg, X, args.cpu_seconds)
+        # the timed launches' D against those oracle rows (the |terms| sums for
+        # the strict bound are computed outside the timed oracle sample)
+        import oracle as oracle_pkg
+
+        sum_abs = None if cfg.is_fp8 else oracle_sum_abs(oracle_pkg.get(), cfg, X, (0, rows))
         cpu["check"] = check_rows(cfg, dD[:rows].contiguous().view(torch.int16).cpu().numpy()
-                                  .view(np.uint16), ref)
+                                  .view(np.uint16), ref, ref64, sum_abs)
         # the same oracle on one core over 64 rows, whole-D time extrapolated
         cpu["single_core"] = oracle_single_core(cfg, X)
 
@@ -701,33 +1002,7 @@ def run_ours(args, cfg):
     context = None
     if not args.no_context:
         n_ctx = max(5, min(args.steps, 20))
-        if cfg.mx:
-            # cuBLASLt's block-scaled FP8 GEMM through torch: the layout of A's
-            # scales is the one torch._scaled_mm takes for 32-element UE8M0
-            # scales, for both operands
-            f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
-            e8 = getattr(torch, "float8_e8m0fnu", None)
-            a8, b8 = dA.view(f8), dB.view(f8)
-            sa = xs[2][:binding.mx_scales_size(cfg.M, cfg.K)]
-            sb = binding.mx_pack_scales(dX[3], cfg.K)[:binding.mx_scales_size(cfg.N, cfg.K)]
-            mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa.view(e8),  # noqa: E731
-                                          scale_b=sb.view(e8), out_dtype=torch_dtype(cfg.out))
-            mm_what = "torch._scaled_mm (cuBLASLt block-scaled FP8, UE8M0 per 32)"
-        elif cfg.is_fp8:
-            # cuBLASLt's FP8 GEMM through torch (scales of 1, alpha folded in by D's scale)
-            f8 = torch.float8_e4m3fn if cfg.dtype == "e4m3" else torch.float8_e5m2
-            a8, b8 = dA.view(f8), dB.view(f8)
-            one = torch.tensor(1.0, device=dev)
-            sa = torch.tensor(float(cfg.alpha), device=dev)
-            mm = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=one,  # noqa: E731
-                                          out_dtype=torch_dtype(cfg.out))
-            mm_what = "torch._scaled_mm (cuBLASLt FP8)"
-        elif cfg.layout == "abt":
-            mm = lambda: torch.mm(dA, dB.t())  # noqa: E731
-            mm_what = "torch.mm (cuBLAS)"
-        else:
-            mm = lambda: torch.mm(dA, dB)  # noqa: E731
-            mm_what = "torch.mm (cuBLAS)"
+        mm, mm_what = library_gemm(cfg, xs, dX, dev)
         try:
             t_mm = time_launches(mm, n_ctx, dev, flush)
         except (RuntimeError, TypeError) as e:  # e.g. a format the library does not take
@@ -744,6 +1019,14 @@ def run_ours(args, cfg):
         }
         if binding.gemm_device_status(clear=True) != 0:
             raise RuntimeError("device status word set during the context runs")
+
+    # ---- every other workload, one record each (single GPU, headline runs only) ------
+    per_config = None
+    if world == 1 and not args.no_per_config and cfg.name == configs.HEADLINE.name:
+        per_config = {}
+        for name in PER_CONFIG:
+            per_config[name] = measure_config(configs.BY_NAME[name], dev, flush,
+                                              max(10, min(args.steps, 20)), peaks)
 
     line = {
         "metric": metric_for(cfg), "value": value, "unit": UNIT, "n_gpus": world,
@@ -772,10 +1055,18 @@ def run_ours(args, cfg):
         "per_launch_ms": {"min": min(per_launch_ms), "median": statistics.median(per_launch_ms),
                           "max": max(per_launch_ms)},
         "context": context,
+        "per_config": per_config,
     }
-    if clocks and clocks.get("sm_mhz"):
+    run_mhz, run_src = None, None
+    if clocks and clocks.get("in_kernel"):
+        run_mhz, run_src = clocks["in_kernel"]["sm_mhz_median"], "in-kernel clock probe"
+    elif clocks and clocks.get("sm_mhz"):
+        run_mhz, run_src = clocks["sm_mhz"], "NVML"
+    if run_mhz:
         line["tensor_peak_nominal"]["frac_at_run_clock"] = (
-            achieved / (props.multi_processor_count * flop_clk * clocks["sm_mhz"] / 1e6))
+            achieved / (props.multi_processor_count * flop_clk * run_mhz / 1e6))
+        line["tensor_peak_nominal"]["run_clock_mhz"] = run_mhz
+        line["tensor_peak_nominal"]["run_clock_source"] = run_src
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -790,6 +1081,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.sweep == "raster":
+        return run_raster_sweep(args, cfg)
     return run_ours(args, cfg)
 
 

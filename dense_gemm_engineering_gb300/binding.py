@@ -32,7 +32,9 @@ STATUS_NAMES = {
 # Every symbol include/gemm.h declares.
 EXPORTS = ("gemm_abt", "gemm_ab", "gemm_run", "gemm_run_workspace", "gemm_workspace_size",
            "gemm_run_no_alloc", "gemm_status_string", "gemm_plan", "gemm_tile_origin",
-           "gemm_device_status", "gemm_selftest_wait_timeout", "gemm_fp8_abt", "gemm_fp8_run",
+           "gemm_device_status", "gemm_selftest_wait_timeout", "gemm_selftest_gemm_timeout",
+           "gemm_run_clock_probe",
+           "gemm_fp8_abt", "gemm_fp8_run",
            "gemm_fp8_run_workspace", "gemm_mx_abt", "gemm_mx_run", "gemm_mx_scales_size",
            "gemm_mx_scales_b_size", "gemm_mx_pack_scales", "gemm_mx_pack_scales_b", "gemm_mx_plan")
 
@@ -49,7 +51,8 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
                 ("tail_split", ctypes.c_int), ("consumers", ctypes.c_int),
-                ("multicast", ctypes.c_int)]
+                ("multicast", ctypes.c_int), ("raster_order", ctypes.c_int),
+                ("l2_hints", ctypes.c_int)]
 
 
 _lib = None
@@ -112,20 +115,27 @@ def load(path: str | None = None):
     lib.gemm_mx_pack_scales_b.argtypes = [vp, i64, i64, i64, vp, vp]
     lib.gemm_mx_pack_scales_b.restype = c_int
     lib.gemm_mx_plan.argtypes = [i64, i64, i64, c_int, ctypes.POINTER(GemmOptions), ip, ip, ip,
-                                 ip, ip, ctypes.POINTER(i64)]
+                                 ip, ip, ctypes.POINTER(i64), ip, ip]
     lib.gemm_mx_plan.restype = c_int
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions), ip, ip,
-                              ip, ip, ip, ctypes.POINTER(i64), ip]
+                              ip, ip, ip, ctypes.POINTER(i64), ip, ip, ip, ip]
     lib.gemm_plan.restype = c_int
-    lib.gemm_tile_origin.argtypes = [i64, i64, c_int, c_int, c_int, i64, ctypes.POINTER(i64),
+    lib.gemm_tile_origin.argtypes = [i64, i64, c_int, c_int, c_int, c_int, i64, ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
     lib.gemm_tile_origin.restype = c_int
     lib.gemm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
     lib.gemm_device_status.restype = c_int
     lib.gemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.gemm_selftest_wait_timeout.restype = c_int
+    lib.gemm_selftest_gemm_timeout.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int,
+                                               c_int, ctypes.POINTER(GemmOptions),
+                                               ctypes.c_uint64, vp]
+    lib.gemm_selftest_gemm_timeout.restype = c_int
+    lib.gemm_run_clock_probe.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, c_int,
+                                         ctypes.POINTER(GemmOptions), vp, vp]
+    lib.gemm_run_clock_probe.restype = c_int
     if path is None:
         _lib = lib
     return lib
@@ -457,13 +467,17 @@ def gemm_mx_plan(M: int, N: int, K: int, in_format: int = GEMM_E4M3, options=Non
     """The tile shape and persistent grid gemm_mx would use on the current device."""
     vals = [ctypes.c_int() for _ in range(5)]
     tiles = ctypes.c_int64()
+    group, order = ctypes.c_int(), ctypes.c_int()
     st = load().gemm_mx_plan(M, N, K, in_format, _options(options),
-                             *[ctypes.byref(v) for v in vals], ctypes.byref(tiles))
+                             *[ctypes.byref(v) for v in vals], ctypes.byref(tiles),
+                             ctypes.byref(group), ctypes.byref(order))
     if st != 0:
         raise GemmError(st, "gemm_mx_plan")
     keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
     out = {k: v.value for k, v in zip(keys, vals)}
     out["num_tiles"] = tiles.value
+    out["raster_group"] = group.value
+    out["raster_order"] = order.value
     return out
 
 
@@ -472,24 +486,30 @@ def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOU
     """The tile shape and persistent grid a call would use on the current device."""
     vals = [ctypes.c_int() for _ in range(5)]
     tiles = ctypes.c_int64()
-    split = ctypes.c_int()
+    split, group, order, hints = (ctypes.c_int() for _ in range(4))
     st = load().gemm_plan(M, N, K, dtype, layout, _options(options),
                           *[ctypes.byref(v) for v in vals], ctypes.byref(tiles),
-                          ctypes.byref(split))
+                          ctypes.byref(split), ctypes.byref(group), ctypes.byref(order),
+                          ctypes.byref(hints))
     if st != 0:
         raise GemmError(st, "gemm_plan")
     keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
     out = {k: v.value for k, v in zip(keys, vals)}
     out["num_tiles"] = tiles.value
     out["tail_split"] = split.value
+    out["raster_group"] = group.value
+    out["raster_order"] = order.value
+    out["l2_hints"] = hints.value
     return out
 
 
-def gemm_tile_origin(M: int, N: int, block_m: int, block_n: int, group: int, task: int):
-    """(m0, n0) of the tile the persistent scheduler assigns to `task`."""
+def gemm_tile_origin(M: int, N: int, block_m: int, block_n: int, group: int, task: int,
+                     raster_order: int = 1):
+    """(m0, n0) of the tile the persistent scheduler assigns to `task` (raster
+    groups of `group` M tiles for raster_order 1, N tiles for 2)."""
     m0, n0 = ctypes.c_int64(), ctypes.c_int64()
-    st = load().gemm_tile_origin(M, N, block_m, block_n, group, task, ctypes.byref(m0),
-                                 ctypes.byref(n0))
+    st = load().gemm_tile_origin(M, N, block_m, block_n, group, raster_order, task,
+                                 ctypes.byref(m0), ctypes.byref(n0))
     if st != 0:
         raise GemmError(st, "gemm_tile_origin")
     return m0.value, n0.value
@@ -511,6 +531,42 @@ def gemm_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     st = load().gemm_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, torch.device("cuda")))
     if st != 0:
         raise GemmError(st, "gemm_selftest_wait_timeout")
+
+
+def gemm_selftest_gemm_timeout(A, B, D, wait_limit_ns: int, *, layout: int = LAYOUT_ABT,
+                               options=None, stream=None) -> None:
+    """The GEMM kernel with every barrier wait limited to `wait_limit_ns`: a
+    limit below the operands' arrival time makes a wait give up, which
+    exercises the kernel's abort path (D is left unspecified)."""
+    M, K = A.shape
+    N = B.shape[0] if layout == LAYOUT_ABT else B.shape[1]
+    if tuple(D.shape) != (M, N) or D.dtype != A.dtype or B.dtype != A.dtype:
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    st = load().gemm_selftest_gemm_timeout(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                           _ld(A), _ld(B), _ld(D), _dtype_code(A), int(layout),
+                                           _options(options), int(wait_limit_ns),
+                                           _stream_handle(stream, A.device))
+    if st != 0:
+        raise GemmError(st, "gemm_selftest_gemm_timeout")
+
+
+def gemm_run_clock_probe(A, B, D, probe, *, layout: int = LAYOUT_ABT, options=None,
+                         stream=None):
+    """gemm_run on (A, B, D) that also writes the first CTA's start and end
+    (%clock64, %globaltimer) into `probe`, an int64 CUDA tensor of 4 words."""
+    M, K = A.shape
+    N = B.shape[0] if layout == LAYOUT_ABT else B.shape[1]
+    if tuple(D.shape) != (M, N) or D.dtype != A.dtype or B.dtype != A.dtype:
+        raise GemmError(-3, "D has the wrong dtype or shape")
+    if probe.device.type != "cuda" or probe.numel() < 4 or probe.element_size() != 8:
+        raise GemmError(-1, "probe must be a CUDA tensor of at least four 8-byte words")
+    st = load().gemm_run_clock_probe(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _ld(A),
+                                     _ld(B), _ld(D), _dtype_code(A), int(layout),
+                                     _options(options), probe.data_ptr(),
+                                     _stream_handle(stream, A.device))
+    if st != 0:
+        raise GemmError(st, "gemm_run_clock_probe")
+    return D
 
 
 def gemm_run_no_alloc(A, B, D, *, layout: int = LAYOUT_ABT, options=None, stream=None):

@@ -17,6 +17,7 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "workspace.h"
 
 namespace gb300 {
 namespace {
@@ -41,7 +42,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Row-major 2-D tensor of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row stride `ld` elements; boxes of box_inner x box_outer,
-// 128-byte swizzle, zero fill outside the tensor.
+// 128-byte swizzle (64-byte for boxes of 64-byte rows), zero fill outside the
+// tensor.
 // `fmt`: GEMM_F16 / GEMM_BF16 (2-byte elements) or GEMM_E4M3 / GEMM_E5M2
 // (1-byte elements, moved as raw bytes).
 bool encode_2d(CUtensorMap* map, const void* ptr, int fmt, uint64_t inner, uint64_t outer,
@@ -56,10 +58,11 @@ bool encode_2d(CUtensorMap* map, const void* ptr, int fmt, uint64_t inner, uint6
     const CUtensorMapDataType dt = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : fmt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t row_bytes = box_inner * (byte ? 1u : 2u);
+    const CUtensorMapSwizzle sw = row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     return enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Block scales (MX) of a rows x K FP8 operand, in the tiled layout of
@@ -150,7 +153,7 @@ cudaError_t ensure_smem_attribute() {
 template <class C>
 void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                     const GemmArgs& args, const CUtensorMap& msa, const CUtensorMap& msb,
-                    int clusters, cudaStream_t stream, cudaError_t* err) {
+                    const CUtensorMap& md32, int clusters, cudaStream_t stream, cudaError_t* err) {
     if ((*err = ensure_smem_attribute<C>()) != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(clusters * C::CLUSTER), 1, 1);
@@ -164,7 +167,7 @@ void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args, msa, msb);
+    *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args, msa, msb, md32);
 }
 
 // Co-resident clusters for a variant on the current device (queried once).
@@ -220,7 +223,9 @@ struct Plan {
     int cons;  // MMA consumers per CTA
     int clusters;
     int64_t tiles;
-    int group;
+    int group;            // tiles per raster group
+    int order;            // kOrderM / kOrderN
+    uint32_t hints;       // kHint* bits
     int64_t k_blocks;
     // Split of the last, partial round of tiles along K (1 = none).
     int64_t whole_units;  // tiles computed whole
@@ -285,7 +290,8 @@ std::atomic<uint32_t> g_epoch{0};
 template <class C>
 int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
              int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha,
-             void* workspace, cudaStream_t stream, const void* SA, const void* SB) {
+             void* workspace, cudaStream_t stream, const void* SA, const void* SB,
+             uint64_t wait_limit_ns, unsigned long long* clock_probe) {
     CUtensorMap ma, mb, md;
     if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_ROWS))
         return GEMM_ERR_CUDA;
@@ -298,10 +304,15 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     }
     if (!encode_2d(&md, D, out_dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
         return GEMM_ERR_CUDA;
+    // The last 32 columns of a tile whose width is an odd multiple of 32 (224):
+    // 32 x 32 boxes.  Other variants never use the map.
+    CUtensorMap md32 = md;
+    if constexpr (C::HALF_CHUNK) {
+        if (!encode_2d(&md32, D, out_dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 32, 32))
+            return GEMM_ERR_CUDA;
+    }
     GemmArgs args;
     args.alpha = alpha;
-    args.d = static_cast<uint16_t*>(D);
-    args.ldd = ldd;
     args.M = int32_t(M);
     args.N = int32_t(N);
     args.K = int32_t(K);
@@ -309,11 +320,15 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     args.grid.m_tiles = int32_t((M + C::BM - 1) / C::BM);
     args.grid.n_tiles = int32_t((N + C::BN - 1) / C::BN);
     args.grid.group = p.group;
+    args.grid.order = p.order;
+    args.l2_hints = p.hints;
     args.whole_units = p.whole_units;
     args.split = p.split;
     args.epoch = g_epoch.fetch_add(1u) + 1u;
     args.counters = nullptr;
     args.partials = nullptr;
+    args.wait_limit_ns = wait_limit_ns;
+    args.clock_probe = clock_probe;
     if (p.split > 1) {
         char* ws = static_cast<char*>(workspace);
         args.counters = reinterpret_cast<unsigned long long*>(ws);
@@ -331,7 +346,7 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
         (void)SB;
     }
     cudaError_t err;
-    launch_variant<C>(ma, mb, md, args, msa, msb, p.clusters, stream, &err);
+    launch_variant<C>(ma, mb, md, args, msa, msb, md32, p.clusters, stream, &err);
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -421,9 +436,9 @@ struct RunFn {
     static int call(const Plan& p, const void* A, const void* B, void* D, int64_t M, int64_t N,
                     int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype,
                     float alpha, void* workspace, cudaStream_t stream, const void* SA,
-                    const void* SB) {
+                    const void* SB, uint64_t wait_limit_ns, unsigned long long* clock_probe) {
         return run_with<C>(p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace,
-                           stream, SA, SB);
+                           stream, SA, SB, wait_limit_ns, clock_probe);
     }
 };
 
@@ -452,6 +467,10 @@ int check_options(const gemm_options_t* o) {
     if (o->consumers < 0 || o->consumers > 2) return GEMM_ERR_OPTION;
     // multicast: kept in the struct for layout stability; 0 or 1 (no multicast) only.
     if (o->multicast < 0 || o->multicast > 1) return GEMM_ERR_OPTION;
+    if (o->raster_order < 0 || o->raster_order > 2) return GEMM_ERR_OPTION;
+    // l2_hints: 0 = automatic, else an odd value (bit 0 marks the explicit choice)
+    if (o->l2_hints < 0 || o->l2_hints > 15 || (o->l2_hints != 0 && !(o->l2_hints & 1)))
+        return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
@@ -497,6 +516,94 @@ int choose_block_n(int64_t M, int64_t N, int bm, int b_layout, int cg, int dtype
     return best;
 }
 
+// L2 bytes a raster group's resident band may take: the band must stay in L2
+// while the group walks the other dimension, next to the streamed operand's
+// panels and the output tiles in flight.  Measured on 8192 x 17408 x 5120
+// BF16 A.B (256 x 256 tiles): bands of 21 and 31 MB (8, 12 M tiles) stay
+// resident (DRAM reads within 1.3x of the model below), a 42 MB band (16)
+// mostly does, an 84 MB band (32) does not (2.1 GB read instead of 0.26 GB).
+constexpr double kBandBudgetBytes = 48.0 * (1 << 20);
+constexpr int kGroups[] = {16, 12, 8, 4, 2, 1};
+
+// Raster order and group from the reuse-window argument ("Choosing schedules
+// and instructions for a backend", section 2, memory report: the operand whose
+// reuse window exceeds L2 is re-read; section 3: grouping M tiles keeps a band
+// of A resident while B streams).  With M groups of G tiles, A is read once
+// and B once per group: A + B * ceil(m_tiles / G) bytes, if A's band (G x
+// block_m rows x K) fits the budget; with N groups the roles swap.  Take the
+// order and the largest group with the least predicted traffic (ties: M
+// groups, larger groups).  Operands that fit in L2 together are read once
+// whatever the order: then the tutorial's G = 16 M groups.  Options override
+// any part of the choice; L2 hints are never automatic (measured: they move
+// DRAM bytes, not time, and an evict_last band could outlive the call).
+void plan_raster(Plan* p, int64_t M, int64_t N, int64_t K, int esize, const gemm_options_t* o) {
+    const int64_t m_tiles = (M + p->bm - 1) / p->bm;
+    const int64_t n_tiles = (N + p->bn - 1) / p->bn;
+    const double a_bytes = double(M) * K * esize, b_bytes = double(N) * K * esize;
+    int order = kOrderM, group = 16;
+    if (a_bytes + b_bytes > kBandBudgetBytes) {
+        double best = 0;
+        for (int ord = kOrderM; ord <= kOrderN; ++ord) {
+            if (o && o->raster_order && o->raster_order - 1 != ord) continue;
+            const int64_t along = ord == kOrderM ? m_tiles : n_tiles;
+            const double band_per_tile = double(ord == kOrderM ? p->bm : p->bn) * K * esize;
+            const double kept = ord == kOrderM ? a_bytes : b_bytes;
+            const double streamed = ord == kOrderM ? b_bytes : a_bytes;
+            for (int g : kGroups) {
+                if (o && o->raster_group && o->raster_group != g) continue;
+                if (g > 1 && g * band_per_tile > kBandBudgetBytes) continue;
+                const int64_t gg = g < along ? g : (along > 0 ? along : 1);
+                const double traffic = kept + streamed * double((along + gg - 1) / gg);
+                if (best == 0 || traffic < best * (1 - 1e-9)) {
+                    best = traffic;
+                    order = ord;
+                    group = g;
+                }
+            }
+        }
+    }
+    p->order = (o && o->raster_order) ? o->raster_order - 1 : order;
+    p->group = (o && o->raster_group) ? o->raster_group : group;
+    p->hints = (o && o->l2_hints) ? uint32_t(o->l2_hints) : 0u;
+    const int64_t along = p->order == kOrderN ? n_tiles : m_tiles;
+    if (p->group > along) p->group = int(along > 0 ? along : 1);
+}
+
+// Small problems: when the chosen tiles fit in one round of the persistent
+// grid, the time is one tile's latency, which shrinks with the tile's width
+// (each SM computes 128 rows x BN whether the tile is one CTA's or a pair's).
+// Take the narrowest tile (128 wide, one or two CTAs) that still fits in one
+// round, if it is narrower than the choice so far.  Measured on 256 x 256 x
+// 1024: 11 us with four 1-CTA 128 x 128 tiles against 12.7 us with two
+// 256 x 192 tiles and 14.5 us with one 256 x 256 tile.  Large problems (more
+// than one round) keep the wide tiles, which move fewer bytes per FLOP.
+void spread_small(int64_t M, int64_t N, int b_layout, int dtype, int dev, int sm_count, bool cg_free,
+                  Plan* p) {
+    const int C = max_clusters_for(p->cg, p->bn, b_layout, dtype, dev, sm_count);
+    if (C <= 0 || M <= 0 || N <= 0) return;
+    const int64_t tiles = ((M + p->bm - 1) / p->bm) * ((N + p->bn - 1) / p->bn);
+    if (tiles > C || p->bn <= 128) return;  // more than one round: keep the wide tiles
+    // 128-wide tiles of one or two CTAs: the one with the most tiles that still
+    // fits in one round (ties keep the current CTA count).
+    int best_cg = 0;
+    int64_t best_t = 0;
+    const int cgs[2] = {p->cg, 3 - p->cg};
+    for (int cg : cgs) {
+        if (!cg_free && cg != p->cg) continue;
+        const int Cn = max_clusters_for(cg, 128, b_layout, dtype, dev, sm_count);
+        const int64_t t = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 127) / 128);
+        if (Cn > 0 && t <= Cn && t >= tiles && t > best_t) {
+            best_cg = cg;
+            best_t = t;
+        }
+    }
+    if (best_cg) {
+        p->cg = best_cg;
+        p->bm = 128 * best_cg;
+        p->bn = 128;
+    }
+}
+
 // Choose the tile shape and grid.  Needs the current device (for its SM count
 // and cluster occupancy).
 int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const gemm_options_t* o,
@@ -516,11 +623,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
         p->cons = 1;
         p->bm = 256;
         p->bn = 224;
-        p->group = (o && o->raster_group) ? o->raster_group : 16;
         const int64_t m_tiles = (M + p->bm - 1) / p->bm;
         p->tiles = m_tiles * ((N + p->bn - 1) / p->bn);
         if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
-        if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
+        plan_raster(p, M, N, K, 1, o);
         int max_clusters = 0;
         st = dispatch_mx<QueryFn>(p->cg, p->bn, false, f8_code(dtype), dev, di.sm_count, &max_clusters);
         if (st != GEMM_OK) return st;
@@ -545,13 +651,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
         if (b_layout == 1 && (p->bn % 128) != 0) return GEMM_ERR_OPTION;
     } else {
         p->bn = choose_block_n(M, N, p->bm, b_layout, p->cg, dtype, dev, di.sm_count);
+        const bool cg_free = !(o && o->cta_group);
+        if (p->cons == 1 && !is_fp8(dtype)) spread_small(M, N, b_layout, dtype, dev, di.sm_count, cg_free, p);
     }
-    p->group = (o && o->raster_group) ? o->raster_group : 16;
     const int64_t m_tiles = (M + p->bm - 1) / p->bm;
     const int64_t n_tiles = (N + p->bn - 1) / p->bn;
     p->tiles = m_tiles * n_tiles;
     if (p->tiles >= kMaxTiles) return GEMM_ERR_SHAPE;
-    if (p->group > m_tiles) p->group = int(m_tiles > 0 ? m_tiles : 1);
+    plan_raster(p, M, N, K, is_fp8(dtype) ? 1 : 2, o);
     int max_clusters = 0;
     st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, f8_code(dtype),
                            dev, di.sm_count, &max_clusters);
@@ -597,7 +704,8 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
              int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha, int b_layout,
              const gemm_options_t* opts, void* workspace, size_t workspace_bytes,
              cudaStream_t stream, const void* SA = nullptr, const void* SB = nullptr,
-             bool mx = false) {
+             bool mx = false, uint64_t wait_limit_ns = kWaitLimitNs,
+             unsigned long long* clock_probe = nullptr) {
     int st = check_sizes(M, N, K, in_fmt, b_layout);
     if (st != GEMM_OK) return st;
     if (out_dtype != GEMM_F16 && out_dtype != GEMM_BF16) return GEMM_ERR_DTYPE;
@@ -646,10 +754,10 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
     if (mx)
         return dispatch_mx<RunFn>(p.cg, p.bn, out_dtype == GEMM_BF16, f8_code(in_fmt), p, A, B, D, M,
                                   N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace, stream,
-                                  SA, SB);
+                                  SA, SB, wait_limit_ns, clock_probe);
     return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
                            alpha, workspace, stream, static_cast<const void*>(nullptr),
-                           static_cast<const void*>(nullptr));
+                           static_cast<const void*>(nullptr), wait_limit_ns, clock_probe);
 }
 
 }  // namespace
@@ -764,7 +872,8 @@ extern "C" int gemm_mx_scales_b_size(int64_t N, int64_t K, size_t* bytes) {
 
 extern "C" int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,
                             int* cta_group, int* block_m, int* block_n, int* stages,
-                            int* num_clusters, int64_t* num_tiles) {
+                            int* num_clusters, int64_t* num_tiles, int* raster_group,
+                            int* raster_order) {
     if (!is_fp8(in_format)) return GEMM_ERR_DTYPE;
     int st = check_sizes(M, N, K, in_format, 0);
     if (st != GEMM_OK) return st;
@@ -777,6 +886,8 @@ extern "C" int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, cons
     if (stages) *stages = p.stages;
     if (num_clusters) *num_clusters = p.clusters;
     if (num_tiles) *num_tiles = p.tiles;
+    if (raster_group) *raster_group = p.group;
+    if (raster_order) *raster_order = p.order + 1;
     return GEMM_OK;
 }
 
@@ -801,6 +912,22 @@ extern "C" int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, i
     return GEMM_OK;
 }
 
+int gb300::split_workspace_layout(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
+                                  const gemm_options_t* opts, size_t* counter_bytes,
+                                  size_t* total_bytes) {
+    int st = check_sizes(M, N, K, dtype, b_layout);
+    if (st != GEMM_OK) return st;
+    if ((st = check_options(opts)) != GEMM_OK) return st;
+    if (!counter_bytes || !total_bytes) return GEMM_ERR_NULL;
+    *counter_bytes = *total_bytes = 0;
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    Plan p;
+    if ((st = make_plan(M, N, K, dtype, b_layout, opts, true, &p)) != GEMM_OK) return st;
+    *total_bytes = workspace_bytes_needed(p);
+    *counter_bytes = p.split > 1 ? p.ws_counter_bytes : 0;
+    return GEMM_OK;
+}
+
 extern "C" int gemm_abt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                         int64_t lda, int64_t ldb, int64_t ldd, int dtype, cudaStream_t stream) {
     return gemm_run(A, B, D, M, N, K, lda, ldb, ldd, dtype, 0, nullptr, stream);
@@ -813,7 +940,8 @@ extern "C" int gemm_ab(const void* A, const void* B, void* D, int64_t M, int64_t
 
 extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
                          const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
-                         int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split) {
+                         int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split,
+                         int* raster_group, int* raster_order, int* l2_hints) {
     int st = check_sizes(M, N, K, dtype, b_layout);
     if (st != GEMM_OK) return st;
     if ((st = check_options(opts)) != GEMM_OK) return st;
@@ -826,18 +954,23 @@ extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layou
     if (num_clusters) *num_clusters = p.clusters;
     if (num_tiles) *num_tiles = p.tiles;
     if (tail_split) *tail_split = p.split;
+    if (raster_group) *raster_group = p.group;
+    if (raster_order) *raster_order = p.order + 1;
+    if (l2_hints) *l2_hints = int(p.hints | 1u);
     return GEMM_OK;
 }
 
 extern "C" int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
-                                int64_t task, int64_t* m0, int64_t* n0) {
+                                int raster_order, int64_t task, int64_t* m0, int64_t* n0) {
     if (M <= 0 || N <= 0 || block_m <= 0 || block_n <= 0 || group <= 0 || M > INT32_MAX ||
         N > INT32_MAX)
         return GEMM_ERR_SHAPE;
+    if (raster_order != 1 && raster_order != 2) return GEMM_ERR_OPTION;
     TileGrid g;
     g.m_tiles = int32_t((M + block_m - 1) / block_m);
     g.n_tiles = int32_t((N + block_n - 1) / block_n);
     g.group = group;
+    g.order = raster_order - 1;
     if (tile_count(g) >= kMaxTiles || task < 0 || task >= tile_count(g)) return GEMM_ERR_SHAPE;
     int32_t mt, nt;
     tile_of_task(g, task, mt, nt);
@@ -864,6 +997,27 @@ extern "C" int gemm_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream
     if (st != GEMM_OK) return st;
     wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+extern "C" int gemm_selftest_gemm_timeout(const void* A, const void* B, void* D, int64_t M,
+                                          int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                          int64_t ldd, int dtype, int b_layout,
+                                          const gemm_options_t* opts, uint64_t wait_limit_ns,
+                                          cudaStream_t stream) {
+    if (is_fp8(dtype)) return GEMM_ERR_DTYPE;
+    return run_impl(A, B, D, M, N, K, lda, ldb, ldd, dtype, dtype, 1.0f, b_layout, opts, nullptr, 0,
+                    stream, nullptr, nullptr, false, wait_limit_ns);
+}
+
+extern "C" int gemm_run_clock_probe(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                                    int b_layout, const gemm_options_t* opts,
+                                    unsigned long long* probe, cudaStream_t stream) {
+    if (is_fp8(dtype)) return GEMM_ERR_DTYPE;
+    if (!probe) return GEMM_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(probe) & 7u) return GEMM_ERR_ALIGN;
+    return run_impl(A, B, D, M, N, K, lda, ldb, ldd, dtype, dtype, 1.0f, b_layout, opts, nullptr, 0,
+                    stream, nullptr, nullptr, false, kWaitLimitNs, probe);
 }
 
 extern "C" const char* gemm_status_string(int status) {

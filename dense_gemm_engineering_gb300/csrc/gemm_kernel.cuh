@@ -42,10 +42,13 @@
 //     TMA store, which clips rows/columns outside D (TileFoundry section 5).
 //     D is never cleared: every tile is written exactly once (section 6).
 //
-// Every barrier wait is bounded (kWaitLimitNs).  A wait that runs out records
-// the reason in the device status word, raises a CTA-local abort flag that
-// the other roles poll, and all roles leave their loops; the CTA still frees
-// TMEM and takes part in the final cluster barrier, so the context survives.
+// Every barrier wait is bounded (kWaitLimitNs, or a shorter limit a self-test
+// passes in GemmArgs).  A wait that runs out records the reason in the device
+// status word and raises the abort flag of its CTA and of the other CTA of the
+// pair, which every role polls; all roles leave their loops, and each warp
+// that sees the flag waits 1 ms (for copies, MMAs and arrivals already in
+// flight to land) before it joins the final cluster barrier; the CTA still
+// frees TMEM, so the context survives.
 #pragma once
 
 #include <cstdint>
@@ -66,6 +69,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 // Pause between an epilogue warp's 64-column chunk stores (see the epilogue).
 constexpr uint32_t kStorePaceNs = 1000;
 constexpr int kStorePaceMinKBlocks = 32;
+
+// L2 eviction priorities of the operand loads and the output stores
+// (GemmArgs::l2_hints; bit 0 only marks an explicit choice).
+enum : uint32_t { kHintALast = 2u, kHintBFirst = 4u, kHintDFirst = 8u };
 
 // Status word layout: bits 0..7 = reason, bits 8..15 = role.
 enum : uint32_t { kReasonTimeout = 1u, kReasonCounter = 2u };
@@ -204,8 +211,6 @@ struct GemmArgs {
     int32_t M, N, K;
     int32_t k_blocks;   // ceil(K / BK)
     float alpha;        // FP8 inputs: D = alpha * (A . Bt) (unused for 16-bit inputs)
-    uint16_t* d;        // D, for the direct stores of a 32-column tail chunk
-    int64_t ldd;        // row stride of D in elements
     TileGrid grid;
     // Work units.  Units [0, whole_units) are whole tiles (unit u = tile u).
     // The remaining tiles ("tail" tiles, the last partial round of the
@@ -216,6 +221,11 @@ struct GemmArgs {
     uint32_t epoch;     // tag of this launch for the tail counters
     float* partials;    // split > 1: FP32 partial of each (tail tile, range, CTA, warp quarter)
     unsigned long long* counters;  // split > 1: one per (tail tile, CTA, warp quarter)
+    uint64_t wait_limit_ns;        // limit of every barrier wait (kWaitLimitNs unless a self-test)
+    uint32_t l2_hints;             // kHint* bits: L2 eviction priorities (0 = none)
+    // Diagnostic (null normally): CTA 0 writes its SM clock counter and the
+    // global nanosecond timer at its start ([0], [1]) and end ([2], [3]).
+    unsigned long long* clock_probe;
 };
 
 struct WorkUnit {
@@ -283,24 +293,36 @@ __device__ __forceinline__ uint64_t noswizzle_desc(uint32_t addr, uint32_t lbo, 
     return d;
 }
 
-__device__ __forceinline__ void raise_abort(volatile uint32_t* abort_flag, uint32_t role) {
-    *abort_flag = 1u;
+// A CTA's abort state: its flag (in its shared memory, polled by every role),
+// the shared::cluster address of the same flag in the other CTA of its pair
+// (0 for a CTA alone), and the limit of every wait.
+struct AbortCtl {
+    volatile uint32_t* flag;
+    uint32_t peer_flag;
+    uint64_t limit_ns;
+};
+
+// Record the reason and raise the flag in both CTAs of the pair: a role of
+// the other CTA may be the one that would wait for this CTA's work, and every
+// warp that sees the flag settles before it leaves (see the teardown).
+__device__ __forceinline__ void raise_abort(const AbortCtl& ac, uint32_t role) {
+    *ac.flag = 1u;
+    if (ac.peer_flag) ptx::st_cluster_u32(ac.peer_flag, 1u);
     atomicCAS(&g_gemm_status, 0u, kReasonTimeout | (role << 8));
 }
 
-// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs or when another
-// role of this CTA has aborted.  Returns false on give-up.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile uint32_t* abort_flag, uint32_t role,
-                                             uint64_t limit_ns = kWaitLimitNs) {
+// Wait for phase `parity` of `bar`, giving up after ac.limit_ns or when a role
+// of this CTA or of its pair has aborted.  Returns false on give-up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortCtl& ac,
+                                             uint32_t role) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((i & 7u) == 0u) {
-            if (*abort_flag) return false;
-            if (ptx::global_timer_ns() - t0 > limit_ns) {
-                raise_abort(abort_flag, role);
+            if (*ac.flag) return false;
+            if (ptx::global_timer_ns() - t0 > ac.limit_ns) {
+                raise_abort(ac, role);
                 return false;
             }
         }
@@ -309,17 +331,26 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 
 // wait_bounded for a whole converged warp: every lane waits (and acquires), and
 // all lanes return the same result.
-__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
-                                                  volatile uint32_t* abort_flag, uint32_t role) {
-    const bool ok = wait_bounded(bar, parity, abort_flag, role);
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, const AbortCtl& ac,
+                                                  uint32_t role) {
+    const bool ok = wait_bounded(bar, parity, ac, role);
     return __all_sync(0xffffffffu, ok);
 }
 
-// After an abort: give in-flight asynchronous copies and MMAs (which complete
-// in microseconds) time to land before shared memory and TMEM are released.
+// After an abort: give in-flight asynchronous copies, MMAs and their barrier
+// arrivals (which complete in microseconds) time to land before shared memory
+// and TMEM are released.
 __device__ __forceinline__ void settle_after_abort() {
     const uint64_t t0 = ptx::global_timer_ns();
     while (ptx::global_timer_ns() - t0 < 1000000ull) __nanosleep(10000);
+}
+
+// For a converged warp at the end of its role: if this CTA's abort flag is
+// up, settle (the whole warp takes one decision, read by lane 0).
+__device__ __forceinline__ void settle_if_aborted(const AbortCtl& ac) {
+    const uint32_t up = __shfl_sync(0xffffffffu, *ac.flag, 0);
+    if (up) settle_after_abort();
+    __syncwarp();
 }
 
 // Count one finished K-range of a tail tile.  The counter word holds
@@ -348,8 +379,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_d, const GemmArgs args,
                         const __grid_constant__ CUtensorMap tmap_sa,
-                        const __grid_constant__ CUtensorMap tmap_sb) {
+                        const __grid_constant__ CUtensorMap tmap_sb,
+                        const __grid_constant__ CUtensorMap tmap_d32) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (args.clock_probe && blockIdx.x == 0 && threadIdx.x == 0) {
+        args.clock_probe[0] = clock64();
+        args.clock_probe[1] = ptx::global_timer_ns();
+    }
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
@@ -371,6 +407,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
+    const AbortCtl ac{abort_flag,
+                      (C::CLUSTER > 1) ? ptx::map_to_rank(base + C::OFF_ABORT, rank ^ 1u) : 0u,
+                      args.wait_limit_ns};
 
     // ---- one-time setup -------------------------------------------------
     if (warp == 0 && lane == 0) {
@@ -388,19 +427,38 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_d);
+        if constexpr (C::HALF_CHUNK) ptx::prefetch_tensormap(&tmap_d32);
         if constexpr (C::MX) {
             ptx::prefetch_tensormap(&tmap_sa);
             ptx::prefetch_tensormap(&tmap_sb);
         }
     }
+    if (warp == 0) __syncwarp();  // lane 0's barrier set-up, for the whole producer warp
     if (warp == 1) {
         ptx::tmem_alloc<C::CG>(base + C::OFF_TMEM_SLOT, C::TMEM_COLS);
         ptx::tmem_relinquish<C::CG>();
     }
+    // Prologue barrier, split in two: every thread arrives once this CTA's
+    // barriers are initialised and its TMEM is allocated, and waits before it
+    // uses either.  The producer of a CTA whose loads complete on its own
+    // barriers (a CTA alone, or the leader of a pair) needs neither TMEM nor
+    // the other CTA, so it does not wait: its first loads leave while TMEM is
+    // allocated and the pair meets.  (With a pair it completes its wait at the
+    // end of its role: a thread waits once for each cluster barrier phase
+    // before it arrives on the next.)
+    const bool early_producer = (warp == 0) && (C::CLUSTER == 1 || leader);
     ptx::tc_fence_before();
-    if constexpr (C::CLUSTER > 1) ptx::cluster_sync(); else __syncthreads();
+    if constexpr (C::CLUSTER > 1) {
+        ptx::cluster_arrive();
+        if (!early_producer) ptx::cluster_wait();
+    } else {
+        if (early_producer) ptx::named_bar_arrive(1, kNumThreads);
+        else ptx::named_bar_sync(1, kNumThreads);
+    }
     ptx::tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
+    // (the producer never touches TMEM)
+    const uint32_t tmem_base =
+        (warp == 0) ? 0u : *reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_TMEM_SLOT);
 
     // The producer and the MMA issuer are warp roles whose loops run on the whole
     // warp, with one elected lane issuing each TMA copy, MMA and commit ("TIRx: A
@@ -412,6 +470,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // k-block.
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------
+        // Optional L2 eviction priorities: A evict_last keeps the band of A
+        // rows that a raster group reuses; B evict_first lets the streamed
+        // operand leave L2 first.
+        const bool hinted = (args.l2_hints & (kHintALast | kHintBFirst)) != 0u;
+        uint64_t pol_a = 0, pol_b = 0;
+        if (hinted) {
+            pol_a = (args.l2_hints & kHintALast) ? ptx::l2_policy_evict_last() : ptx::l2_policy_evict_normal();
+            pol_b = (args.l2_hints & kHintBFirst) ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
+        }
+        // One operand box into this CTA's shared memory; with CG == 2 the
+        // completion goes to the leader's full barrier.
+        auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y,
+                        uint64_t pol) {
+            if constexpr (C::CG == 1) {
+                if (hinted) ptx::tma_load_2d_hint(dst, map, bar, x, y, pol);
+                else ptx::tma_load_2d(dst, map, bar, x, y);
+            } else {
+                if (hinted) ptx::tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                else ptx::tma_load_2d_pair(dst, map, bar, x, y);
+            }
+        };
         uint32_t s = 0, ph = 0;
         bool ok = true;
         for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
@@ -421,7 +500,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
             const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleProducer)) {
+                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, ac, kRoleProducer)) {
                     ok = false;
                     break;
                 }
@@ -430,27 +509,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
                     const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
                     const int32_t k0 = kb * C::BK;
-                    if constexpr (C::CG == 1) {
-                        ptx::tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, a_row);
-                        if constexpr (!C::B_MN) {
-                            ptx::tma_load_2d(b_dst, &tmap_b, full_bar(s), k0, b_row);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < C::B_ROWS / 64; ++c)
-                                ptx::tma_load_2d(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, full_bar(s),
-                                                 b_row + 64 * c, k0);
-                        }
+                    // the leader's barrier (a shared::cluster address) for a pair
+                    const uint32_t fb = (C::CG == 1) ? full_bar(s) : ptx::map_to_rank(full_bar(s), 0u);
+                    load(a_dst, &tmap_a, fb, k0, a_row, pol_a);
+                    if constexpr (!C::B_MN) {
+                        load(b_dst, &tmap_b, fb, k0, b_row, pol_b);
                     } else {
-                        const uint32_t fb = ptx::map_to_rank(full_bar(s), 0u);  // the leader's barrier
-                        ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, k0, a_row);
-                        if constexpr (!C::B_MN) {
-                            ptx::tma_load_2d_pair(b_dst, &tmap_b, fb, k0, b_row);
-                        } else {
 #pragma unroll
-                            for (int c = 0; c < C::B_ROWS / 64; ++c)
-                                ptx::tma_load_2d_pair(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, fb,
-                                                      b_row + 64 * c, k0);
-                        }
+                        for (int c = 0; c < C::B_ROWS / 64; ++c)
+                            load(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, fb, b_row + 64 * c, k0, pol_b);
                     }
                     if constexpr (C::MX) {
                         // The scales of k-block kb, into this CTA's shared memory,
@@ -478,31 +545,111 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // Drain: every slot must have been released by the MMA, so no
             // tcgen05.commit arrives on this CTA's barriers after it exits.
             for (int i = 0; i < C::STAGES; ++i) {
-                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, abort_flag, kRoleDrain)) {
+                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, ac, kRoleDrain)) {
                     ok = false;
                     break;
                 }
                 if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
             }
         }
-        if (!ok) settle_after_abort();
         __syncwarp();
     } else if (warp == 1) {
         // ---- MMA issuer (leader CTA) ------------------------------------------
-        if (leader) {
+        if constexpr (C::CONS == 2) {
+          if (leader) {
+            // Two consumers ("TIRx GEMM on Blackwell", V9): their accumulators
+            // fill TMEM, so the next tile's MMAs can only start once the
+            // epilogue has drained them.  It drains consumer 0 first and hands
+            // each consumer back on its own barrier (acc_empty[h]); consumer 0
+            // then runs alone over the tile's first k-blocks (up to one ring),
+            // keeping their stages, while consumer 1 is still being drained;
+            // consumer 1 catches up on those stages, and the rest of the tile
+            // issues both consumers per k-block as one B tile serves both.
+            uint32_t s = 0, ph = 0, aph = 0;
+            bool ok = true;
+            auto issue = [&](uint32_t st, int h, bool first_kb) {
+                const uint32_t a_addr = base + C::OFF_A + st * C::A_BYTES + 16384u * uint32_t(h);
+                const uint32_t b_addr = base + C::OFF_B + st * C::B_BYTES;
+#pragma unroll
+                for (int k = 0; k < C::BK / C::MMA_K; ++k) {
+                    const uint64_t bd = C::B_MN ? sw128_desc(b_addr + 2048u * k, C::MN_ATOM_BYTES, 1024u)
+                                                : sw128_desc(b_addr + 32u * k, 16u, 1024u);
+                    const uint64_t ad = sw128_desc(a_addr + 32u * k, 16u, 1024u);
+                    ptx::mma_f16<C::CG>(tmem_base + uint32_t(h) * C::ACC_STRIDE, ad, bd, C::IDESC,
+                                        uint32_t(!first_kb || k != 0));
+                }
+            };
+            for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
+                const WorkUnit w = unit_of(args, u);
+                const int nkb = w.kb1 - w.kb0;
+                const int lead = nkb < C::STAGES ? nkb : C::STAGES;
+                const uint32_t s0 = s;
+                if (!wait_bounded_warp(acc_empty_bar(0), aph ^ 1u, ac, kRoleMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int i = 0; i < lead; ++i) {  // consumer 0 alone; stages kept
+                    if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (ptx::elect_one_sync()) issue(s, 0, i == 0);
+                    __syncwarp();
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                if (!wait_bounded_warp(acc_empty_bar(1), aph ^ 1u, ac, kRoleMma)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                for (int i = 0; i < lead; ++i) {  // consumer 1 catches up, stages released
+                    const uint32_t st = (s0 + uint32_t(i)) % uint32_t(C::STAGES);
+                    if (ptx::elect_one_sync()) {
+                        issue(st, 1, i == 0);
+                        ptx::mma_commit<C::CG>(empty_bar(st), uint16_t(0x3u));
+                    }
+                    __syncwarp();
+                }
+                for (int i = lead; i < nkb; ++i) {  // both consumers share each B tile
+                    if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (ptx::elect_one_sync()) {
+                        issue(s, 0, false);
+                        issue(s, 1, false);
+                        ptx::mma_commit<C::CG>(empty_bar(s), uint16_t(0x3u));
+                    }
+                    __syncwarp();
+                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                if (ptx::elect_one_sync())
+                    ptx::mma_commit<C::CG>(acc_full_bar(0), uint16_t(0x3u));  // both accumulators ready
+                __syncwarp();
+                aph ^= 1u;
+            }
+            // No drain: the epilogue hands back every accumulator but those of
+            // the cluster's last unit, and this loop waited for each hand-back.
+          }
+        } else if (leader) {
             uint32_t s = 0, ph = 0, ab = 0, aph = 0;
             uint32_t sfbuf = 0;  // MX: TMEM scale buffer of the next k-block
             bool ok = true;
             for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
                 const WorkUnit w = unit_of(args, u);
-                if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleMma)) {
+                if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, ac, kRoleMma)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * C::SLOT_COLS;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded_warp(full_bar(s), ph, abort_flag, kRoleMma)) {
+                    if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
                         ok = false;
                         break;
                     }
@@ -561,14 +708,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // except the slot of the cluster's last unit, which the epilogue
                 // keeps (its release would be the last arrival of the launch).
                 for (uint32_t i = 0; i + 1 < C::NUM_ACC; ++i) {
-                    if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, abort_flag, kRoleDrain)) {
+                    if (!wait_bounded_warp(acc_empty_bar(ab), aph ^ 1u, ac, kRoleDrain)) {
                         ok = false;
                         break;
                     }
                     if (++ab == C::NUM_ACC) { ab = 0; aph ^= 1u; }
                 }
             }
-            if (!ok) settle_after_abort();
         }
         __syncwarp();
     } else {
@@ -590,19 +736,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ptx::mbar_arrive(acc_empty_bar(b));
             }
         };
-        // 64 FP32 values of this lane's row -> 16-bit -> swizzled staging -> TMA
-        // store of the warp's 32 x 64 box at (col, row0).  Staging alternates
-        // between the warp's two buffers, or (in a cluster's last unit, when the
-        // ring is idle) takes a fresh 4 KiB slice of the ring per chunk, which
-        // never waits for an earlier store.
+        // W = 64 (or 32, the last chunk of a 224-wide tile) FP32 values of this
+        // lane's row -> 16-bit -> swizzled staging -> TMA store of the warp's
+        // 32 x W box at (col, row0), which clips rows and columns outside D.
+        // Staging alternates between the warp's buffers, or (in a cluster's last
+        // unit, when the ring is idle) takes a fresh 4 KiB slice of the ring per
+        // chunk, which never waits for an earlier store.
         // FP8 inputs: D = alpha * (A . Bt), applied to the FP32 sum before the
         // one rounding to 16 bits.
         const float alpha = args.alpha;
+        const bool hint_d = (args.l2_hints & kHintDFirst) != 0u;
+        const uint64_t pol_d = hint_d ? ptx::l2_policy_evict_first() : 0ull;
         auto scaled = [&](float x) -> float {
             if constexpr (C::F8) return x * alpha; else return x;
         };
-        auto store_chunk = [&](const uint32_t (&bits)[64], int32_t col, int32_t row0,
-                               int32_t ring_slot = -1) {
+        auto store_chunk = [&](const auto& bits, int32_t col, int32_t row0, int32_t ring_slot = -1) {
+            constexpr int W = int(sizeof(bits) / sizeof(bits[0]));
+            static_assert(W == 64 || W == 32, "a chunk is 64 or 32 columns");
             uint32_t buf;
             if (ring_slot >= 0) {
                 buf = my_ring + uint32_t(ring_slot) * C::EPI_BUF_BYTES;
@@ -612,51 +762,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (lane == 0) ptx::bulk_wait_group_read<int(C::EPI_BUFS) - 1>();
             }
             __syncwarp();
-            // Row `lane` of the 32 x 64 staging tile, 128-byte swizzled: the
-            // 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
-            const uint32_t row_addr = buf + lane * 128u;
+            // Row `lane` of the 32 x W staging tile.  W = 64: 128-byte rows,
+            // 128-byte swizzle (16-byte chunk c of row r at chunk position
+            // c ^ (r % 8)).  W = 32: 64-byte rows, 64-byte swizzle (chunk c of
+            // row r at c ^ ((r / 2) % 4)).  Either way the 8 lanes of each
+            // quarter-warp phase of a 16-byte store cover all 32 banks.
+            const uint32_t row_addr = buf + lane * uint32_t(2 * W);
+            const uint32_t sw = (W == 64) ? (lane & 7u) : ((lane >> 1) & 3u);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < W / 8; ++c) {
                 auto f = [&](int i) { return scaled(__uint_as_float(bits[8 * c + i])); };
                 const uint32_t p0 = ptx::pack2<C::BF16>(f(0), f(1));
                 const uint32_t p1 = ptx::pack2<C::BF16>(f(2), f(3));
                 const uint32_t p2 = ptx::pack2<C::BF16>(f(4), f(5));
                 const uint32_t p3 = ptx::pack2<C::BF16>(f(6), f(7));
-                ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ (lane & 7u)) << 4), p0, p1, p2, p3);
+                ptx::st_shared_v4(row_addr + ((uint32_t(c) ^ sw) << 4), p0, p1, p2, p3);
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (row0 < args.M && col < args.N) ptx::tma_store_2d(&tmap_d, buf, col, row0);
+                if (row0 < args.M && col < args.N) {
+                    const CUtensorMap* map = (W == 64) ? &tmap_d : &tmap_d32;
+                    if (hint_d) ptx::tma_store_2d_hint(map, buf, col, row0, pol_d);
+                    else ptx::tma_store_2d(map, buf, col, row0);
+                }
                 ptx::bulk_commit_group();  // one group per chunk, even if empty
             }
             ++chunk;
-        };
-        // 32 FP32 values (bit patterns) of row `row` -> 16-bit -> D[row][col..col+31],
-        // masked at the edges of D.
-        auto store_half_chunk = [&](const uint32_t (&r)[32], int32_t col, int32_t row) {
-            auto pk = [&](uint32_t lo, uint32_t hi) {
-                return ptx::pack2<C::BF16>(scaled(__uint_as_float(lo)), scaled(__uint_as_float(hi)));
-            };
-            if (row >= args.M || col >= args.N) return;
-            uint16_t* dst = args.d + int64_t(row) * args.ldd + col;
-            if (col + 32 <= args.N) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 q = make_uint4(
-                        pk(r[8 * c + 0], r[8 * c + 1]), pk(r[8 * c + 2], r[8 * c + 3]),
-                        pk(r[8 * c + 4], r[8 * c + 5]), pk(r[8 * c + 6], r[8 * c + 7]));
-                    reinterpret_cast<uint4*>(dst)[c] = q;
-                }
-            } else {
-                const int32_t n = args.N - col;
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const uint32_t p = pk(r[c], r[c + 1]);
-                    if (c < n) dst[c] = uint16_t(p & 0xFFFFu);
-                    if (c + 1 < n) dst[c + 1] = uint16_t(p >> 16);
-                }
-            }
         };
         auto load_acc = [&](uint32_t taddr, float (&v)[64]) {
             uint32_t lo[32], hi[32];
@@ -675,7 +807,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int32_t mt, nt;
             tile_of_task(args.grid, w.tile, mt, nt);
             uint32_t ok = 1u;
-            if (lane == 0) ok = wait_bounded(acc_full_bar(ab), aph, abort_flag, kRoleEpilogue);
+            if (lane == 0) ok = wait_bounded(acc_full_bar(ab), aph, ac, kRoleEpilogue);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             while (!ptx::mbar_try_wait(acc_full_bar(ab), aph)) {
@@ -718,17 +850,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_ld_32x32b_x32(th + 64u * j + 32u,
                                                 *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
                         ptx::tmem_wait_ld();
-                        if (last_h && j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) release(ab);
+                        if (j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) {
+                            // two consumers: each goes back on its own barrier
+                            if (C::CONS == 2) release(uint32_t(h));
+                            else if (last_h) release(ab);
+                        }
                         if (pace && j > 0) __nanosleep(kStorePaceNs);
                         store_chunk(bits, col0 + 64 * j, rh, last_unit ? h * C::FULL_CHUNKS + j : -1);
                     }
                     if constexpr (C::HALF_CHUNK) {
-                        // Last 32 columns: this lane's row, 64 bytes, stored directly.
+                        // Last 32 columns: a 32 x 32 box through the second D map.
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(th + 64u * C::FULL_CHUNKS, r);
                         ptx::tmem_wait_ld();
                         if (last_h) release(ab);
-                        store_half_chunk(r, col0 + 64 * C::FULL_CHUNKS, rh + int32_t(lane));
+                        if (pace) __nanosleep(kStorePaceNs);
+                        store_chunk(r, col0 + 64 * C::FULL_CHUNKS, rh,
+                                    last_unit ? h * (C::FULL_CHUNKS + 1) + C::FULL_CHUNKS : -1);
                     }
                 }
             } else {
@@ -788,7 +926,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                        C::PIECE_BYTES, my_epi_bar);
                                     ++piece;
                                 }
-                            ok2 = wait_bounded(my_epi_bar, eph, abort_flag, kRoleEpilogue);
+                            ok2 = wait_bounded(my_epi_bar, eph, ac, kRoleEpilogue);
                         }
                         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
                         if (ok2) {
@@ -876,6 +1014,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // Done with TMEM and with the cluster's shared state: arrive on the
         // final cluster barrier now, so that its latency and the skew between
         // the cluster's CTAs overlap the drain of this warp's bulk stores.
+        settle_if_aborted(ac);
         ptx::tc_fence_before();
         if constexpr (C::CLUSTER > 1) ptx::cluster_arrive();
         if (lane == 0) ptx::bulk_wait_all();
@@ -885,8 +1024,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ---- teardown ---------------------------------------------------------
     // Every CTA of the cluster stays until all are done (the peer reads this
     // CTA's shared memory and arrives on its barriers); TMEM is freed after
-    // every warp's last TMEM read.
+    // every warp's last TMEM read.  Without an abort every copy, MMA and
+    // arrival aimed at a CTA has been waited for by one of its roles before
+    // that role gets here.  After an abort (the flag is raised in both CTAs of
+    // the pair), each warp that sees the flag settles before it arrives: an
+    // operation still in flight was issued either before its issuer arrived
+    // (and an issuer that saw the flag settled after it) or before the abort
+    // (and the warp that raised it settles after it), and the barrier cannot
+    // complete before those warps arrive.
+    if (warp < 2) settle_if_aborted(ac);  // the epilogue warps settled already
     if constexpr (C::CLUSTER > 1) {
+        if (early_producer) ptx::cluster_wait();  // the prologue phase, long complete
         if (warp < 2) {  // the epilogue warps arrived already
             ptx::tc_fence_before();
             ptx::cluster_arrive();
@@ -900,6 +1048,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
     }
+    if (args.clock_probe && blockIdx.x == 0 && threadIdx.x == 0) {
+        args.clock_probe[2] = clock64();
+        args.clock_probe[3] = ptx::global_timer_ns();
+    }
 }
 
 // Failure-path self-test: one thread waits, through wait_bounded, on a
@@ -912,7 +1064,8 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
         abort_flag = 0u;
         ptx::mbar_init(ptx::smem_addr(&bar), 1);
         ptx::fence_mbar_init();
-        wait_bounded(ptx::smem_addr(&bar), 0u, &abort_flag, kRoleSelfTest, limit_ns);
+        const AbortCtl ac{&abort_flag, 0u, limit_ns};
+        wait_bounded(ptx::smem_addr(&bar), 0u, ac, kRoleSelfTest);
     }
 }
 

@@ -9,8 +9,17 @@
 // consecutive tiles; tasks walk the groups in order and, inside a group, walk
 // the N tiles with the group's M tiles innermost.  Tasks that run at the same
 // time then touch few distinct B column panels (reused through L2) and a
-// bounded band of A rows.  Unlike the tutorial's order, the last group may be
-// shorter than `group`, so any M works; every tile is visited exactly once.
+// bounded band of A rows, which stays in L2 while the group walks all of N:
+// A is read from DRAM about once and B once per group.  Unlike the tutorial's
+// order, the last group may be shorter than `group`, so any M works; every
+// tile is visited exactly once.
+//
+// The same walk with the roles of M and N exchanged (order = kOrderN: groups
+// of `group` N tiles, the M tiles walked inside a group with the group's N
+// tiles innermost) keeps a band of B columns in L2 instead and reads A once
+// per group: the better choice when B's band is the one that fits (the
+// tutorial's memory report: the operand whose reuse window exceeds L2 is the
+// one that must stream).
 #pragma once
 
 #include <cstdint>
@@ -23,10 +32,13 @@
 
 namespace gb300 {
 
+enum : int32_t { kOrderM = 0, kOrderN = 1 };
+
 struct TileGrid {
     int32_t m_tiles;  // ceil(M / block_m)
     int32_t n_tiles;  // ceil(N / block_n)
-    int32_t group;    // M tiles per raster group (>= 1)
+    int32_t group;    // tiles per raster group along the grouped dimension (>= 1)
+    int32_t order;    // kOrderM: groups of M tiles; kOrderN: groups of N tiles
 };
 
 GB300_HD int64_t tile_count(const TileGrid& g) {
@@ -40,17 +52,21 @@ constexpr int64_t kMaxTiles = int64_t(1) << 31;
 
 // Task -> (m tile, n tile).  Requires 0 <= task < tile_count(g) < kMaxTiles.
 GB300_HD void tile_of_task(const TileGrid& g, int64_t task, int32_t& mt, int32_t& nt) {
+    const bool by_n = (g.order == kOrderN);
+    const uint32_t grouped = static_cast<uint32_t>(by_n ? g.n_tiles : g.m_tiles);
+    const uint32_t other = static_cast<uint32_t>(by_n ? g.m_tiles : g.n_tiles);
     const uint32_t t = static_cast<uint32_t>(task);
     const uint32_t group = static_cast<uint32_t>(g.group);
-    const uint32_t per_group = group * static_cast<uint32_t>(g.n_tiles);  // <= tile count
+    const uint32_t per_group = group * other;  // <= tile count
     const uint32_t grp = t / per_group;
-    const uint32_t first_m = grp * group;
-    const uint32_t left = static_cast<uint32_t>(g.m_tiles) - first_m;
-    const uint32_t rows_in_group = left < group ? left : group;
+    const uint32_t first = grp * group;
+    const uint32_t left = grouped - first;
+    const uint32_t in_group = left < group ? left : group;
     const uint32_t r = t - grp * per_group;
-    const uint32_t q = r / rows_in_group;
-    nt = static_cast<int32_t>(q);
-    mt = static_cast<int32_t>(first_m + (r - q * rows_in_group));
+    const uint32_t q = r / in_group;                       // position along the other dimension
+    const uint32_t g_idx = first + (r - q * in_group);     // position along the grouped one
+    mt = static_cast<int32_t>(by_n ? q : g_idx);
+    nt = static_cast<int32_t>(by_n ? g_idx : q);
 }
 
 }  // namespace gb300

@@ -95,9 +95,17 @@ const char* gemm_status_string(int status);
  *                 cta_group::1), 2 = a 2-CTA cluster per 256-row tile
  *                 (cta_group::2, the two CTAs' tensor cores act as one).
  *   block_n       0 = automatic, else the N extent of a tile: 128 or 256.
- *   raster_group  0 = automatic, else the number of M tiles per raster group
- *                 of the persistent scheduler (tiles are visited group by
- *                 group, N-major inside a group, so consecutive tiles share B).
+ *   raster_group  0 = automatic, else the number of tiles per raster group
+ *                 of the persistent scheduler, counted along the grouped
+ *                 dimension (see raster_order).
+ *   raster_order  0 = automatic.  1 = groups of raster_group M tiles: tiles
+ *                 are visited group by group, and inside a group the N tiles
+ *                 in order with the group's M tiles innermost, so tiles that
+ *                 run at the same time share B's column panel and the band
+ *                 of A rows stays in L2 while the group walks N ("Choosing
+ *                 schedules and instructions for a backend", section 3).
+ *                 2 = the same with M and N exchanged: groups of N tiles, a
+ *                 band of B columns stays in L2 while the group walks M.
  *   max_clusters  0 = as many co-resident clusters as fit, else an upper bound
  *                 on the persistent grid (in clusters).
  *   tail_split    0 or 1 = balanced grid: the persistent schedule's rounds
@@ -117,8 +125,12 @@ const char* gemm_status_string(int status);
  *                 epilogue no longer overlaps the next tile's MMAs.
  *   multicast     must be 0 or 1 (GEMM_ERR_OPTION otherwise): a cluster is
  *                 always the CTAs of one tile, and every CTA loads its own
- *                 operand tiles (no load is multicast to other CTAs).  The
- *                 field is kept so that the structure's layout does not change.
+ *                 operand tiles (no load is multicast to other CTAs).
+ *   l2_hints      0 = automatic.  Otherwise an odd value (bit 0 marks the
+ *                 choice as explicit; an even non-zero value is
+ *                 GEMM_ERR_OPTION) whose other bits set L2 eviction
+ *                 priorities: 2 = A's loads evict_last, 4 = B's loads
+ *                 evict_first, 8 = D's stores evict_first (1 = no hints).
  */
 typedef struct {
     int cta_group;
@@ -128,6 +140,8 @@ typedef struct {
     int tail_split;
     int consumers;
     int multicast;
+    int raster_order;
+    int l2_hints;
 } gemm_options_t;
 
 /* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */
@@ -271,7 +285,7 @@ int gemm_mx_pack_scales_b(const void* src, int64_t N, int64_t K, int64_t ld, voi
 /* The plan gemm_mx_run would use (outputs as gemm_plan; may be NULL). */
 int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int in_format, const gemm_options_t* opts,
                  int* cta_group, int* block_m, int* block_n, int* stages, int* num_clusters,
-                 int64_t* num_tiles);
+                 int64_t* num_tiles, int* raster_group, int* raster_order);
 
 /*
  * Bytes of workspace gemm_run_workspace needs for these sizes and options on
@@ -282,50 +296,57 @@ int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout
                         const gemm_options_t* opts, size_t* bytes);
 
 /*
- * gemm_run_workspace for callers that cannot allocate device memory (code
- * captured into a CUDA graph or running under a fixed memory budget, plugins
- * whose host framework owns every allocation, loops where an allocation may
- * block or fail).  The pages describe no counterpart: it is an addition of
- * this library.
+ * gemm_run_workspace for callers that cannot allocate device memory: a plugin
+ * inside a host framework whose memory manager owns all device memory and
+ * must account for every byte; a latency-critical loop, where cudaMalloc or
+ * cudaFree can synchronise the device and stall every stream; a process whose
+ * device-memory budget is fixed at start-up.  The pages describe no
+ * counterpart: it is an addition of this library.
  *
  * The split tail's workspace is a fixed 20 MiB scratch array compiled into
- * the library; every GPU that loads the library holds one until the process
- * exits.  The caller passes A, B and D as for gemm_run; nothing is allocated
- * and no allocating routine is called.  A plan that needs more than 20 MiB
- * (a tail_split s with (T mod C) x s larger than the cluster count C)
- * returns GEMM_ERR_WORKSPACE; s <= C / (T mod C) always fits on a 152-SM
- * GB300.
+ * the library (a file-scope __device__ array); every GPU that loads the
+ * library holds one until the process exits.  The caller passes A, B and D
+ * as for gemm_run; no memory is allocated and no allocating routine is
+ * called.  A plan that needs more than 20 MiB (a tail_split s with
+ * (T mod C) x s larger than the cluster count C) returns GEMM_ERR_WORKSPACE;
+ * s <= C / (T mod C) always fits on a 152-SM GB300.
  *
- * The first call on each device looks up the scratch's device address and
- * zeroes it (a synchronous cudaMemset), so make that first call before any
- * stream capture.  All calls on a device share the one scratch array, which
- * keeps the last call's contents: calls that overlap on the GPU (different
- * streams, concurrent graphs) race on it and must be serialised by the caller.
+ * The first call on each device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one scratch
+ * array, which keeps the last call's contents: a call whose plan splits
+ * clears the split tail's counter words first (cudaMemsetAsync on `stream`),
+ * and calls that overlap on the GPU (different streams) race on the array
+ * and must be serialised by the caller.
  */
 int gemm_run_no_alloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
                       const gemm_options_t* opts, cudaStream_t stream);
 
 /*
- * Plan of a call, without launching: the tile shape, grid, stage count and
- * tail split gemm_run_workspace (with a large enough workspace) would use for
- * these sizes on the current device.  Any out pointer may be NULL.  Returns
- * the same argument errors as gemm_run (pointers are not checked).
+ * Plan of a call, without launching: the tile shape, grid, stage count, tail
+ * split, raster group and order (1 = M groups, 2 = N groups, as the
+ * options) and L2 hints (an explicit, odd l2_hints value) that
+ * gemm_run_workspace (with a large enough workspace) would use for these
+ * sizes on the current device.  Any out pointer may be NULL.  Returns the
+ * same argument errors as gemm_run (pointers are not checked).
  */
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
               const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
-              int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split);
+              int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split,
+              int* raster_group, int* raster_order, int* l2_hints);
 
 /*
  * The persistent scheduler's task -> tile map (the same function the kernel
  * runs), for host-side checks.  Tiles of block_m x block_n cover the M x N
- * output; `group` M tiles form a raster group.  Writes the tile's first row
- * and column.  Returns GEMM_ERR_SHAPE if task is outside [0, tiles) or if
- * there are 2^31 tiles or more (the scheduler's index arithmetic is 32-bit;
- * gemm_run rejects such sizes with the same error).
+ * output; `group` tiles along M (raster_order 1) or along N (raster_order 2)
+ * form a raster group.  Writes the tile's first row and column.  Returns
+ * GEMM_ERR_SHAPE if task is outside [0, tiles) or if there are 2^31 tiles or
+ * more (the scheduler's index arithmetic is 32-bit; gemm_run rejects such
+ * sizes with the same error), GEMM_ERR_OPTION for another raster_order.
  */
 int gemm_tile_origin(int64_t M, int64_t N, int block_m, int block_n, int group,
-                     int64_t task, int64_t* m0, int64_t* n0);
+                     int raster_order, int64_t task, int64_t* m0, int64_t* n0);
 
 /*
  * Device-side error word of the current device.  Every wait inside the kernel
@@ -349,6 +370,39 @@ int gemm_device_status(uint32_t* status, int clear);
  * Returns GEMM_OK once launched, GEMM_ERR_DEVICE or GEMM_ERR_CUDA otherwise.
  */
 int gemm_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/*
+ * Self-test of the GEMM kernel's own abort path: gemm_run(A, B, D, ...) with
+ * every barrier wait of the kernel limited to `wait_limit_ns` nanoseconds
+ * instead of about 2 s.  With a limit far below the time the first operands
+ * take to arrive (e.g. 100 ns), a wait gives up: the kernel records
+ * reason 1 (timeout) and the role that gave up in the device status word,
+ * raises the abort flag in both CTAs of every pair that sees it, leaves all
+ * loops, waits 1 ms for work already in flight, frees Tensor Memory and
+ * returns; the CUDA context stays usable and later calls run normally.  D's
+ * contents are unspecified afterwards (tiles may be partly written).
+ * Arguments and errors as gemm_run (16-bit types only).
+ */
+int gemm_selftest_gemm_timeout(const void* A, const void* B, void* D, int64_t M, int64_t N,
+                               int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int dtype,
+                               int b_layout, const gemm_options_t* opts, uint64_t wait_limit_ns,
+                               cudaStream_t stream);
+
+/*
+ * Diagnostic: gemm_run(A, B, D, ...) whose first CTA also records, in
+ * `probe` (a device buffer of four 8-byte words, 8-byte aligned), the SM's
+ * clock counter (%clock64) and the global nanosecond timer (%globaltimer) at
+ * its start (probe[0], probe[1]) and at its end (probe[2], probe[3]).
+ * (probe[2] - probe[0]) / (probe[3] - probe[1]) is the SM clock, in GHz,
+ * that the kernel ran at, which a driver query sampled from the host may not
+ * show.  Nothing else differs from gemm_run; 16-bit types only.  Errors as
+ * gemm_run, plus GEMM_ERR_NULL / GEMM_ERR_ALIGN for the probe buffer.  The
+ * operation has no counterpart on the pages: it is a measurement aid.
+ */
+int gemm_run_clock_probe(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldd, int dtype, int b_layout,
+                         const gemm_options_t* opts, unsigned long long* probe,
+                         cudaStream_t stream);
 
 #ifdef __cplusplus
 }

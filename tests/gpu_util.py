@@ -64,6 +64,63 @@ def check_close(got_bits, ref_bits, dtype, what="", ref_f64=None):
     return out
 
 
+def ulp_of(x64: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of the 16-bit output format at |x| (IEEE binary16, or bfloat16)."""
+    emin, p = (-14, 10) if dtype == "f16" else (-126, 7)
+    mag = np.maximum(np.abs(x64), 2.0 ** emin)
+    return 2.0 ** (np.floor(np.log2(mag)) - p)
+
+
+STRICT_REL = 2.0 ** -16
+
+
+def check_strict(got_bits, ref_f64, sum_abs_f64, dtype, what=""):
+    """|got - ref64| <= ulp(ref64) + 2^-16 * sum_k |A[i,k] B'[j,k]|, element by
+    element, against the oracle's unrounded binary64 sums.
+
+    The method's arithmetic is fixed ("TIRx GEMM on Blackwell", Take away 1:
+    FP32 accumulation, only the order of additions changes) and the output is
+    rounded once: FP32 sums of any order stay within a few 2^-24 of
+    sum |terms| of the exact sum, and the rounding adds at most half an ulp.
+    A K = 16 slice lost or counted twice moves an output by about
+    sqrt(16) * E|term|, far outside the bound.  Returns the largest error in
+    output ulps and the worst ratio to the bound.
+    """
+    got = decode(got_bits, dtype)
+    ref = np.asarray(ref_f64, dtype=np.float64)
+    ulp = ulp_of(ref, dtype)
+    bound = ulp + STRICT_REL * np.asarray(sum_abs_f64, dtype=np.float64)
+    err = np.abs(got - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)
+        i, j = idx[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} outside 1 ulp + 2^-16 sum|terms|; first at "
+            f"{tuple(idx[0])}: got {got[i, j]!r} exact {ref[i, j]!r} bound {bound[i, j]!r}")
+    if not err.size:
+        return {"max_ulp": 0.0, "worst_strict_ratio": 0.0}
+    return {"max_ulp": float((err / ulp).max()), "worst_strict_ratio": float((err / bound).max())}
+
+
+def abs_bits(bits: np.ndarray) -> np.ndarray:
+    """16-bit patterns with the sign bit cleared (|x| for FP16 and BF16)."""
+    return np.asarray(bits, dtype=np.uint16) & np.uint16(0x7FFF)
+
+
+def oracle_with_bound(orc, A, B, layout, dtype, rows=None, cols=None):
+    """The oracle's rounded D, its unrounded binary64 sums, and the binary64
+    sums of |terms| (the oracle run on |A| and |B|) for the strict check."""
+    kw = {"layout": layout, "dtype": dtype, "want_f64": True}
+    if rows is not None:
+        kw["rows"] = rows
+    if cols is not None:
+        kw["cols"] = cols
+    ref, ref64 = orc.gemm(A, B, **kw)
+    _, sum_abs = orc.gemm(abs_bits(A), abs_bits(B), **kw)
+    return ref, ref64, sum_abs
+
+
 def sample_tiles(M, N, K, block_m, block_n, group, num_clusters, stages, tile_origin,
                  seed=0, extra_random=16, block_k=64):
     """Seeded sample of whole output tiles that covers every value of

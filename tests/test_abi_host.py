@@ -92,25 +92,44 @@ def test_k_zero_needs_no_inputs_but_validates_output(lib):
 
 # ---- the persistent scheduler's task -> tile map ---------------------------
 
-def cover(M, N, bm, bn, group):
+def cover(M, N, bm, bn, group, order=1):
     tiles = -(-M // bm) * -(-N // bn)
-    seen = [binding.gemm_tile_origin(M, N, bm, bn, group, t) for t in range(tiles)]
+    seen = [binding.gemm_tile_origin(M, N, bm, bn, group, t, order) for t in range(tiles)]
     return tiles, seen
 
 
+@pytest.mark.parametrize("order", [1, 2], ids=["m_groups", "n_groups"])
 @pytest.mark.parametrize("M,N,bm,bn,group", [
     (4096, 4096, 128, 128, 16),   # "TIRx GEMM on Blackwell", V3: 32 x 32 = 1,024 tiles
     (4096, 4096, 256, 256, 16),
     (3000, 5000, 256, 256, 16),   # ragged: last group and last tiles partial
     (3000, 5000, 128, 256, 7),
     (8192, 17408, 256, 256, 16),
+    (8192, 17408, 256, 256, 5),   # N groups: 68 N tiles = 13 groups of 5 and one of 3
     (300, 100, 128, 128, 1),
 ])
-def test_every_tile_exactly_once(lib, M, N, bm, bn, group):
-    tiles, seen = cover(M, N, bm, bn, group)
+def test_every_tile_exactly_once(lib, M, N, bm, bn, group, order):
+    tiles, seen = cover(M, N, bm, bn, group, order)
     expect = {(m, n) for m in range(0, M, bm) for n in range(0, N, bn)}
     assert len(seen) == tiles == len(expect)
     assert set(seen) == expect
+
+
+def test_n_group_order_is_the_m_order_transposed(lib):
+    # Groups of N tiles walk M with the group's N tiles innermost: the map of
+    # an M x N grid in N order is the map of the N x M grid in M order with
+    # the two coordinates exchanged (and it differs from the M order).
+    M, N, bm, bn, group = 3000, 5000, 256, 128, 6
+    _, by_n = cover(M, N, bm, bn, group, 2)
+    _, by_m_t = cover(N, M, bn, bm, group, 1)
+    assert by_n == [(m, n) for (n, m) in by_m_t]
+    _, by_m = cover(M, N, bm, bn, group, 1)
+    assert by_n != by_m
+    # the first tasks of an N group: the group's N tiles for M tile 0, then M tile 1
+    assert by_n[:group + 1] == [(0, k * bn) for k in range(group)] + [(bm, 0)]
+    with pytest.raises(binding.GemmError) as e:
+        binding.gemm_tile_origin(M, N, bm, bn, group, 0, 3)
+    assert e.value.status == -8
 
 
 def test_v3_tile_count(lib):

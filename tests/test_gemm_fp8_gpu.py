@@ -111,10 +111,11 @@ def test_large_sampled_tiles():
     A, B = inputs.operands(M, N, K, "abt", "e4m3", "normal", 7)
     D = from_device(run8(A, B, "e4m3", "bf16", alpha=0.5))
     plan = binding.gemm_plan(M, N, K, binding.GEMM_E4M3, binding.LAYOUT_ABT)
-    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], 16,
+    g, o = plan["raster_group"], plan["raster_order"]
+    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], g,
                          plan["num_clusters"], plan["stages"],
                          lambda t: binding.gemm_tile_origin(M, N, plan["block_m"], plan["block_n"],
-                                                            16, t), seed=3, block_k=128)
+                                                            g, t, o), seed=3, block_k=128)
     for (m0, n0) in tiles:
         m1, n1 = min(m0 + plan["block_m"], M), min(n0 + plan["block_n"], N)
         ref, ref64 = oracle.gemm_fp8(A, B, fmt="e4m3", out_dtype="bf16", alpha=0.5,

@@ -197,10 +197,11 @@ def test_large_sampled_tiles():
     A, B, SA, SB = inputs.mx_operands(M, N, K, "e4m3", "normal", 7)
     D = from_device(run_mx(A, B, SA, SB, K, "e4m3", "bf16", alpha=0.5))
     plan = binding.gemm_mx_plan(M, N, K, binding.GEMM_E4M3)
-    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], 16, plan["num_clusters"],
+    g, o = plan["raster_group"], plan["raster_order"]
+    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], g, plan["num_clusters"],
                          plan["stages"],
                          lambda t: binding.gemm_tile_origin(M, N, plan["block_m"],
-                                                            plan["block_n"], 16, t),
+                                                            plan["block_n"], g, t, o),
                          seed=3, extra_random=8, block_k=128)
     for (m0, n0) in tiles:
         m1, n1 = min(m0 + plan["block_m"], M), min(n0 + plan["block_n"], N)
@@ -218,10 +219,11 @@ def test_mlp_shapes_sampled_tiles(shape):
     A, B, SA, SB = inputs.mx_operands(M, N, K, "e4m3", "normal", 8)
     D = from_device(run_mx(A, B, SA, SB, K, "e4m3", "bf16"))
     plan = binding.gemm_mx_plan(M, N, K, binding.GEMM_E4M3)
-    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], 16, plan["num_clusters"],
+    g, o = plan["raster_group"], plan["raster_order"]
+    tiles = sample_tiles(M, N, K, plan["block_m"], plan["block_n"], g, plan["num_clusters"],
                          plan["stages"],
                          lambda t: binding.gemm_tile_origin(M, N, plan["block_m"],
-                                                            plan["block_n"], 16, t),
+                                                            plan["block_n"], g, t, o),
                          seed=4, extra_random=4, block_k=128)
     for (m0, n0) in tiles:
         m1, n1 = min(m0 + plan["block_m"], M), min(n0 + plan["block_n"], N)
