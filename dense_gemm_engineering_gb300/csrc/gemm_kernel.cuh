@@ -752,6 +752,50 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         auto scaled = [&](float x) -> float {
             if constexpr (C::F8) return x * alpha; else return x;
         };
+        // The whole-tile epilogue's steps, 32 columns at a time (see there):
+        // pick the staging buffer of the next chunk (waiting until the store
+        // EPI_BUFS chunks ago has read it, unless the ring slice is used) ...
+        auto stage_buffer = [&](int32_t ring_slot) -> uint32_t {
+            uint32_t b;
+            if (ring_slot >= 0) {
+                b = my_ring + uint32_t(ring_slot) * C::EPI_BUF_BYTES;
+            } else {
+                b = buf0 + (chunk % C::EPI_BUFS) * C::EPI_BUF_BYTES;
+                if (lane == 0) ptx::bulk_wait_group_read<int(C::EPI_BUFS) - 1>();
+            }
+            __syncwarp();
+            return b;
+        };
+        // ... convert 32 FP32 values of this lane's row and store them as half
+        // `half` of its row in the staging tile (W = 64: 128-byte rows, 128-byte
+        // swizzle; W = 32: 64-byte rows, 64-byte swizzle, half 0 only) ...
+        auto stage_half = [&](const uint32_t (&v)[32], uint32_t b, int W, int half) {
+            const uint32_t row_addr = b + lane * uint32_t(2 * W);
+            const uint32_t sw = (W == 64) ? (lane & 7u) : ((lane >> 1) & 3u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                auto f = [&](int i) { return scaled(__uint_as_float(v[8 * q + i])); };
+                const uint32_t p0 = ptx::pack2<C::BF16>(f(0), f(1));
+                const uint32_t p1 = ptx::pack2<C::BF16>(f(2), f(3));
+                const uint32_t p2 = ptx::pack2<C::BF16>(f(4), f(5));
+                const uint32_t p3 = ptx::pack2<C::BF16>(f(6), f(7));
+                ptx::st_shared_v4(row_addr + ((uint32_t(4 * half + q) ^ sw) << 4), p0, p1, p2, p3);
+            }
+        };
+        // ... and send the staged 32 x W box to D.
+        auto issue_store = [&](uint32_t b, int32_t col, int32_t row0, int W) {
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < args.M && col < args.N) {
+                    const CUtensorMap* map = (W == 64) ? &tmap_d : &tmap_d32;
+                    if (hint_d) ptx::tma_store_2d_hint(map, b, col, row0, pol_d);
+                    else ptx::tma_store_2d(map, b, col, row0);
+                }
+                ptx::bulk_commit_group();  // one group per chunk, even if empty
+            }
+            ++chunk;
+        };
         auto store_chunk = [&](const auto& bits, int32_t col, int32_t row0, int32_t ring_slot = -1) {
             constexpr int W = int(sizeof(bits) / sizeof(bits[0]));
             static_assert(W == 64 || W == 32, "a chunk is 64 or 32 columns");
@@ -839,36 +883,44 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const bool pace = (C::NUM_ACC == 2) && !last_unit && w.kb1 - w.kb0 >= kStorePaceMinKBlocks;
             if (w.range < 0) {
                 // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
-                // the CTA's A rows 128h..128h+127).
+                // the CTA's A rows 128h..128h+127), 32 columns at a time: the
+                // TMEM load of the next 32 columns is in flight while the
+                // current ones are converted and staged, and each 64-column
+                // chunk (or the last 32 columns of a 224-wide tile) leaves as
+                // one TMA store once both of its halves are staged.
 #pragma unroll 1
                 for (int h = 0; h < C::CONS; ++h) {
                     const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
                     const int32_t rh = row0 + 128 * h;
                     const bool last_h = (h == C::CONS - 1);
-#pragma unroll 1
-                    for (int j = 0; j < C::FULL_CHUNKS; ++j) {
-                        uint32_t bits[64];
-                        ptx::tmem_ld_32x32b_x32(th + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&bits[0]));
-                        ptx::tmem_ld_32x32b_x32(th + 64u * j + 32u,
-                                                *reinterpret_cast<uint32_t(*)[32]>(&bits[32]));
-                        ptx::tmem_wait_ld();
-                        if (j == C::FULL_CHUNKS - 1 && !C::HALF_CHUNK) {
-                            // two consumers: each goes back on its own barrier
+                    constexpr int U = C::BN / 32;  // 32-column units
+                    constexpr int CHUNKS = C::FULL_CHUNKS + (C::HALF_CHUNK ? 1 : 0);
+                    uint32_t ra[32], rb[32];
+                    uint32_t buf = 0;
+                    ptx::tmem_ld_32x32b_x32(th, ra);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        uint32_t(&cur)[32] = (u % 2 == 0) ? ra : rb;
+                        uint32_t(&nxt)[32] = (u % 2 == 0) ? rb : ra;
+                        if (u + 1 < U) {
+                            ptx::tmem_ld_32x32b_x32(th + 32u * uint32_t(u + 1), nxt);
+                        } else {
+                            // every TMEM read of this accumulator is done; two
+                            // consumers go back each on its own barrier
                             if (C::CONS == 2) release(uint32_t(h));
                             else if (last_h) release(ab);
                         }
-                        if (pace && j > 0) __nanosleep(kStorePaceNs);
-                        store_chunk(bits, col0 + 64 * j, rh, last_unit ? h * C::FULL_CHUNKS + j : -1);
-                    }
-                    if constexpr (C::HALF_CHUNK) {
-                        // Last 32 columns: a 32 x 32 box through the second D map.
-                        uint32_t r[32];
-                        ptx::tmem_ld_32x32b_x32(th + 64u * C::FULL_CHUNKS, r);
-                        ptx::tmem_wait_ld();
-                        if (last_h) release(ab);
-                        if (pace) __nanosleep(kStorePaceNs);
-                        store_chunk(r, col0 + 64 * C::FULL_CHUNKS, rh,
-                                    last_unit ? h * (C::FULL_CHUNKS + 1) + C::FULL_CHUNKS : -1);
+                        const int c = u / 2;
+                        const bool first_half = (u % 2 == 0);
+                        const bool narrow = C::HALF_CHUNK && (c == C::FULL_CHUNKS);  // 32 columns
+                        if (first_half) {
+                            if (pace && c > 0) __nanosleep(kStorePaceNs);
+                            buf = stage_buffer(last_unit ? h * CHUNKS + c : -1);
+                        }
+                        stage_half(cur, buf, narrow ? 32 : 64, first_half ? 0 : 1);
+                        if (!first_half || narrow) issue_store(buf, col0 + 64 * c, rh, narrow ? 32 : 64);
+                        if (u + 1 < U) ptx::tmem_wait_ld();
                     }
                 }
             } else {
