@@ -594,11 +594,11 @@ PER_CONFIG = ["single_tile_128x128x64_f16_abt", "kloop_256x256x1024_f16_abt",
 def check_row_ranges(M: int):
     """Rows of D the per-config check compares with the oracle: the first two,
     two in the middle and the last two."""
-    cand = [(0, 2), (M // 2, M // 2 + 2), (M - 2, M)]
     out = []
-    for r0, r1 in cand:
-        r0, r1 = max(0, r0), min(M, r1)
-        if r1 > r0 and all(r1 <= a or r0 >= b for a, b in out):
+    for r0, r1 in [(0, 2), (M // 2, M // 2 + 2), (M - 2, M)]:
+        r0 = max(r0, out[-1][1] if out else 0)  # disjoint, in order
+        r1 = min(M, r1)
+        if r1 > r0:
             out.append((r0, r1))
     return out
 

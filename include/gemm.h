@@ -164,6 +164,11 @@ int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
  *                  for these sizes).  Zero it once before its first use;
  *                  afterwards it may be reused by any number of calls, because
  *                  every launch tags its counters with a fresh launch number.
+ *                  A launch replayed from a CUDA graph repeats its number, so
+ *                  after a launch that ended with a non-zero
+ *                  gemm_device_status() (a wait that gave up may leave its
+ *                  counters half-counted) zero the workspace again before the
+ *                  graph is replayed.
  *                  Calls that share a workspace must not run concurrently
  *                  (different streams): they would race on it.
  * workspace = NULL runs the plain persistent schedule (as gemm_run).

@@ -171,3 +171,50 @@ def test_check_rows_against_the_oracle():
     bad = ref.copy()
     bad[3, 5] ^= np.uint16(0x4000)  # flip a high exponent bit
     assert not bench.check_rows(cfg, bad, ref)["within_tolerance"]
+
+
+# ---- this build's additions: strict row check, in-kernel clock, row sampling -------
+
+def _f16_bits(x):
+    return np.asarray(x, dtype=np.float16).view(np.uint16)
+
+
+def test_check_rows_strict_bound_accepts_rounding_and_rejects_a_lost_slice():
+    from dense_gemm_engineering_gb300 import configs
+
+    cfg = configs.HEADLINE
+    exact = np.array([[1.0 + 2 ** -12, -3.25, 0.0, 100.0 + 2 ** -5]])
+    sum_abs = np.array([[1024.0, 1024.0, 1024.0, 1024.0]])
+    ref = _f16_bits(exact)                        # the one rounding
+    ok = bench.check_rows(cfg, ref, ref, exact, sum_abs)
+    assert ok["within_tolerance"] and ok["within_strict"] and ok["max_ulp"] <= 0.5
+    # a K = 16 slice of U[-1,1) products (|sum| ~ sqrt(16)/3 ~ 1.3) moves one output
+    bad = _f16_bits(exact + np.array([[0.0, 0.0, 1.3, 0.0]]))
+    chk = bench.check_rows(cfg, bad, ref, exact, sum_abs)
+    assert not chk["within_strict"] and chk["max_err_over_strict"] > 1
+
+
+def test_clock_from_probes():
+    rows = [[1000, 10, 1000 + 1800 * 50, 10 + 50_000],   # 1800 MHz over 50 us
+            [0, 0, 1700 * 40, 40_000],                   # 1700 MHz
+            [5, 5, 5, 5]]                                # no time elapsed: ignored
+    c = bench.clock_from_probes(rows)
+    assert c["launches"] == 2
+    assert c["sm_mhz_min"] == pytest.approx(1700) and c["sm_mhz_max"] == pytest.approx(1800)
+    assert bench.clock_from_probes([[1, 1, 1, 1]]) is None
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 128, 3000, 8192])
+def test_check_row_ranges_are_disjoint_and_inside(M):
+    r = bench.check_row_ranges(M)
+    assert r and all(0 <= a < b <= M for a, b in r)
+    assert all(r[i][1] <= r[i + 1][0] for i in range(len(r) - 1))
+    assert r[0][0] == 0 and r[-1][1] == M
+
+
+def test_options_and_sweep_flags_parse():
+    a = bench.parse_args(["--options", '{"raster_group": 8}', "--sweep", "raster",
+                          "--no-per-config", "--soak-seconds", "0.5"])
+    assert json.loads(a.options) == {"raster_group": 8}
+    assert a.sweep == "raster" and a.no_per_config and a.soak_seconds == 0.5
+    assert all(o in (1, 2) and g >= 1 and h % 2 == 1 for o, g, h in bench.RASTER_SWEEP)
