@@ -108,13 +108,18 @@ const char* gemm_status_string(int status);
  *                 band of B columns stays in L2 while the group walks M.
  *   max_clusters  0 = as many co-resident clusters as fit, else an upper bound
  *                 on the persistent grid (in clusters).
- *   tail_split    0 or 1 = balanced grid: the persistent schedule's rounds
- *                 are spread over the fewest clusters that keep the same round
- *                 count, so no cluster idles in a partial last round.
- *                 s in [2, 16], only with a workspace (gemm_run_workspace):
- *                 keep every cluster and split each tile of the last, partial
- *                 round into s K-ranges (capped by the number of 64-wide
- *                 k-blocks).
+ *   tail_split    0 = automatic: a balanced grid (the persistent schedule's
+ *                 rounds spread over the fewest clusters that keep the same
+ *                 round count, so no cluster idles in a partial last round);
+ *                 with a workspace (gemm_run_workspace), a problem whose
+ *                 tiles all fit in one round with clusters to spare also
+ *                 splits every tile's K loop into s ranges over the idle
+ *                 clusters (s <= clusters / tiles, at least 64 k-blocks per
+ *                 range: the partials' fix-up costs a few microseconds).  1 = never split.  s in [2, 16], only with a
+ *                 workspace: split each tile of the last, partial round (of
+ *                 a single-round problem: every tile) into s K-ranges
+ *                 (capped by the number of k-blocks and, for a single
+ *                 round, by clusters / tiles).
  *   consumers     0 or 1 = one MMA accumulator per CTA and tile, two TMEM
  *                 accumulator slots so the epilogue of one tile overlaps the
  *                 next tile's MMAs.  2 = two accumulators per CTA that share
@@ -151,10 +156,12 @@ int gemm_run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
 
 /*
  * The same GEMM with a caller-owned device workspace, which lets the kernel
- * split the last, partial round of its persistent schedule (requested with
- * gemm_options_t.tail_split = s >= 2): with C co-resident clusters and T
- * tiles, the T mod C tiles of that round are each split into s K-ranges so
- * the clusters that would idle share the work.  Each range writes an FP32
+ * split the K loop of tiles that would leave clusters idle.  A problem whose
+ * T tiles fit in one round of C co-resident clusters with clusters to spare
+ * is split automatically: each tile into s <= C / T K-ranges.  The last,
+ * partial round of a longer schedule is split on request
+ * (gemm_options_t.tail_split = s >= 2): its T mod C tiles are each split into
+ * s K-ranges so the clusters that would idle share the work.  Each range writes an FP32
  * partial to the workspace; the range that finishes last (found with an
  * atomic counter, nobody waits) adds the partials in range order and writes D.
  * Results are deterministic for a given plan.
@@ -314,7 +321,8 @@ int gemm_workspace_size(int64_t M, int64_t N, int64_t K, int dtype, int b_layout
  * as for gemm_run; no memory is allocated and no allocating routine is
  * called.  A plan that needs more than 20 MiB (a tail_split s with
  * (T mod C) x s larger than the cluster count C) returns GEMM_ERR_WORKSPACE;
- * s <= C / (T mod C) always fits on a 152-SM GB300.
+ * s <= C / (T mod C), and every automatic split, always fits on a 152-SM
+ * GB300.
  *
  * The first call on each device looks up the scratch's device address
  * (cudaGetSymbolAddress, with that device current); make that first call

@@ -365,6 +365,30 @@ def test_split_tail(case, layout, dtype):
            options=opts)
 
 
+def test_automatic_k_split_of_single_round_problems():
+    # Tiles that fit one round with clusters to spare share their K loop over the
+    # idle clusters when a workspace is given: at least 64 k-blocks per range.
+    p = binding.gemm_plan(512, 512, 16384, 0, 0)       # 16 1-CTA tiles, 256 k-blocks
+    assert p["num_tiles"] == 16 and p["tail_split"] == 4 and p["num_clusters"] == 64
+    assert binding.gemm_workspace_size(512, 512, 16384, 0, 0) > 0
+    q = binding.gemm_plan(256, 256, 1024, 0, 0)        # 16 k-blocks: never split
+    assert q["tail_split"] == 1
+    r = binding.gemm_plan(512, 512, 16384, 0, 0, {"tail_split": 1})
+    assert r["tail_split"] == 1 and r["num_clusters"] == 16
+
+
+@pytest.mark.parametrize("shape,layout,dtype", [
+    ((512, 512, 16384), "abt", "f16"),    # 4 ranges of 64 k-blocks
+    ((384, 640, 12000), "ab", "bf16"),    # ragged tiles, K tail of 32
+    ((256, 512, 32768), "abt", "f16"),    # 8 ranges: the fix-up reads partials from L2
+])
+def test_automatic_k_split_parity(shape, layout, dtype):
+    M, N, K = shape
+    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1)
+    assert plan["tail_split"] >= 2
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + 7)
+
+
 def test_split_tail_deterministic_and_workspace_reused():
     M, N, K = 1024, 1024, 2048
     opts = {"cta_group": 2, "block_n": 256, "max_clusters": 7, "tail_split": 3}
