@@ -166,7 +166,7 @@ void launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = C::CLUSTER > 1 ? 1 : 0;  // a lone CTA is launched as a plain grid
     *err = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, ma, mb, md, args, msa, msb, md32);
 }
 
