@@ -52,7 +52,7 @@ class GemmOptions(ctypes.Structure):
                 ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
                 ("tail_split", ctypes.c_int), ("consumers", ctypes.c_int),
                 ("multicast", ctypes.c_int), ("raster_order", ctypes.c_int),
-                ("l2_hints", ctypes.c_int)]
+                ("l2_hints", ctypes.c_int), ("cluster_ksplit", ctypes.c_int)]
 
 
 _lib = None
@@ -120,7 +120,7 @@ def load(path: str | None = None):
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, ctypes.POINTER(GemmOptions), ip, ip,
-                              ip, ip, ip, ctypes.POINTER(i64), ip, ip, ip, ip]
+                              ip, ip, ip, ctypes.POINTER(i64), ip, ip, ip, ip, ip]
     lib.gemm_plan.restype = c_int
     lib.gemm_tile_origin.argtypes = [i64, i64, c_int, c_int, c_int, c_int, i64, ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -486,11 +486,11 @@ def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOU
     """The tile shape and persistent grid a call would use on the current device."""
     vals = [ctypes.c_int() for _ in range(5)]
     tiles = ctypes.c_int64()
-    split, group, order, hints = (ctypes.c_int() for _ in range(4))
+    split, group, order, hints, ks = (ctypes.c_int() for _ in range(5))
     st = load().gemm_plan(M, N, K, dtype, layout, _options(options),
                           *[ctypes.byref(v) for v in vals], ctypes.byref(tiles),
                           ctypes.byref(split), ctypes.byref(group), ctypes.byref(order),
-                          ctypes.byref(hints))
+                          ctypes.byref(hints), ctypes.byref(ks))
     if st != 0:
         raise GemmError(st, "gemm_plan")
     keys = ("cta_group", "block_m", "block_n", "stages", "num_clusters")
@@ -500,6 +500,7 @@ def gemm_plan(M: int, N: int, K: int, dtype: int = GEMM_F16, layout: int = LAYOU
     out["raster_group"] = group.value
     out["raster_order"] = order.value
     out["l2_hints"] = hints.value
+    out["cluster_ksplit"] = ks.value
     return out
 
 

@@ -206,8 +206,8 @@ struct Stages {
     static constexpr int value = stages_for(CG, BN, CONS);
 };
 
-template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int F8 = 0>
-using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, F8>;
+template <int CG, int BN, bool B_MN, bool BF16, int CONS = 1, int F8 = 0, int KS = 1>
+using Cfg = KernelConfig<CG, BN, Stages<CG, BN, CONS>::value, B_MN, BF16, CONS, F8, false, KS>;
 
 // Block-scaled FP8 (MX) stages: a stage also holds 512 B of A scales and the
 // tile's 4 KiB block of B scales, and the epilogue stages through one 4 KiB
@@ -221,6 +221,7 @@ using CfgMX = KernelConfig<CG, BN, stages_for_mx(CG, BN), false, BF16, 1, F8, tr
 struct Plan {
     int cg, bm, bn, stages;
     int cons;  // MMA consumers per CTA
+    int ks;    // K-ranges per tile inside a cluster (1 = none)
     int clusters;
     int64_t tiles;
     int group;            // tiles per raster group
@@ -318,6 +319,9 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
              int64_t lda, int64_t ldb, int64_t ldd, int in_fmt, int out_dtype, float alpha,
              void* workspace, cudaStream_t stream, const void* SA, const void* SB,
              uint64_t wait_limit_ns, unsigned long long* clock_probe) {
+    // An in-cluster K split reuses the operand ring of each CTA for the
+    // partials once its own MMAs are done: exactly one tile per cluster.
+    if (C::KS > 1 && (p.split != 1 || p.tiles != int64_t(p.clusters))) return GEMM_ERR_OPTION;
     CUtensorMap ma, mb, md;
     if (!encode_2d(&ma, A, in_fmt, uint64_t(K), uint64_t(M), uint64_t(lda), C::BK, C::A_ROWS))
         return GEMM_ERR_CUDA;
@@ -330,10 +334,11 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
     }
     if (!encode_2d(&md, D, out_dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 64, 32))
         return GEMM_ERR_CUDA;
-    // The last 32 columns of a tile whose width is an odd multiple of 32 (224):
-    // 32 x 32 boxes.  Other variants never use the map.
+    // The last 32 columns of a tile whose width is an odd multiple of 32 (224),
+    // and a CTA's 32 columns of a 128-wide tile split 4 ways inside its
+    // cluster: 32 x 32 boxes.  Other variants never use the map.
     CUtensorMap md32 = md;
-    if constexpr (C::HALF_CHUNK) {
+    if constexpr (C::D32) {
         if (!encode_2d(&md32, D, out_dtype, uint64_t(N), uint64_t(M), uint64_t(ldd), 32, 32))
             return GEMM_ERR_CUDA;
     }
@@ -379,7 +384,24 @@ int run_with(const Plan& p, const void* A, const void* B, void* D, int64_t M, in
 // Dispatch on (cta_group, block_n, layout, dtype, FP8 input) to one template
 // instance.  `bf16` is the output type (and the input type when f8 == 0).
 template <template <class> class Fn, class... Ts>
-int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, Ts&&... ts) {
+int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, int ks, Ts&&... ts) {
+    if (ks != 1) {
+        // In-cluster K split: 16-bit, 1-CTA tiles, 128 wide (2 or 4 ranges)
+        // or 256 wide (2 ranges).
+        if (f8 != 0 || cons != 1 || cg != 1) return GEMM_ERR_OPTION;
+#define GB300_CASEKS(BN_, KS_, MN_, BF_)                                                 \
+    if (bn == BN_ && ks == KS_ && b_mn == MN_ && bf16 == BF_)                            \
+        return Fn<Cfg<1, BN_, MN_, BF_, 1, 0, KS_>>::call(std::forward<Ts>(ts)...);
+#define GB300_CASESKS(BN_, KS_) \
+    GB300_CASEKS(BN_, KS_, false, false) GB300_CASEKS(BN_, KS_, false, true) \
+    GB300_CASEKS(BN_, KS_, true, false) GB300_CASEKS(BN_, KS_, true, true)
+        GB300_CASESKS(128, 2)
+        GB300_CASESKS(128, 4)
+        GB300_CASESKS(256, 2)
+#undef GB300_CASESKS
+#undef GB300_CASEKS
+        return GEMM_ERR_OPTION;
+    }
     if (f8 != 0) {
         // FP8 inputs: K-major B, one consumer; 2-CTA 256 / 224-wide and 1-CTA
         // 256-wide tiles.
@@ -497,12 +519,15 @@ int check_options(const gemm_options_t* o) {
     // l2_hints: 0 = automatic, else an odd value (bit 0 marks the explicit choice)
     if (o->l2_hints < 0 || o->l2_hints > 15 || (o->l2_hints != 0 && !(o->l2_hints & 1)))
         return GEMM_ERR_OPTION;
+    if (o->cluster_ksplit != 0 && o->cluster_ksplit != 1 && o->cluster_ksplit != 2 &&
+        o->cluster_ksplit != 4)
+        return GEMM_ERR_OPTION;
     return GEMM_OK;
 }
 
-int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count) {
+int max_clusters_for(int cg, int bn, int b_layout, int dtype, int dev, int sm_count, int ks = 1) {
     int n = 0;
-    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, f8_code(dtype), dev,
+    if (dispatch<QueryFn>(cg, bn, b_layout == 1, dtype == GEMM_BF16, 1, f8_code(dtype), ks, dev,
                           sm_count, &n) != GEMM_OK)
         return 0;
     return n;
@@ -630,6 +655,47 @@ void spread_small(int64_t M, int64_t N, int b_layout, int dtype, int dev, int sm
     }
 }
 
+// In-cluster K split (cluster_ksplit: 0 = automatic, 1 = never, 2 / 4 =
+// ranges): a problem whose 1-CTA tiles all fit in one round of KS-CTA clusters
+// has each tile computed by a cluster of KS CTAs, one K-range each; each CTA
+// owns BN / KS of the tile's columns and the partials are exchanged over
+// distributed shared memory (no workspace).  The exchange and the cluster
+// launch cost a few microseconds (measured: ~3 us with 2 ranges, ~4 us with
+// 4), so the automatic choice is the most ranges (4 for 128-wide tiles, 2
+// for 256-wide) that keep at least kMinClusterRangeKBlocks k-blocks per
+// range, and none when the workspace split (plan_split) would run more
+// ranges per tile.
+constexpr int64_t kMinClusterRangeKBlocks = 16;
+
+void plan_cluster_split(int b_layout, int dtype, int dev, int sm_count, const gemm_options_t* o,
+                        bool have_workspace, int max_clusters, Plan* p) {
+    p->ks = 1;
+    const int req = o ? o->cluster_ksplit : 0;
+    if (req == 1 || is_fp8(dtype) || p->cons != 1 || p->cg != 1) return;
+    if (p->bn != 128 && p->bn != 256) return;
+    // ranges per tile of the automatic workspace split, for comparison
+    int64_t ws_ranges = 1;
+    if (req == 0 && have_workspace && (o ? o->tail_split : 0) != 1 && p->tiles > 0 &&
+        p->tiles < max_clusters) {
+        ws_ranges = p->k_blocks / kMinRangeKBlocks;
+        if (ws_ranges > kMaxSplit) ws_ranges = kMaxSplit;
+        if (ws_ranges > max_clusters / p->tiles) ws_ranges = max_clusters / p->tiles;
+    }
+    const int cands[2] = {4, 2};
+    for (int ks : cands) {
+        if (req >= 2 && ks != req) continue;
+        if (ks == 4 && p->bn != 128) continue;
+        if (req == 0 && (p->k_blocks < ks * kMinClusterRangeKBlocks || ws_ranges > ks)) continue;
+        if (p->k_blocks < ks) continue;
+        int C = max_clusters_for(1, p->bn, b_layout, dtype, dev, sm_count, ks);
+        if (o && o->max_clusters && o->max_clusters < C) C = o->max_clusters;
+        if (C <= 0 || p->tiles > C) continue;
+        p->ks = ks;
+        p->clusters = int(p->tiles);
+        return;
+    }
+}
+
 // Choose the tile shape and grid.  Needs the current device (for its SM count
 // and cluster occupancy).
 int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const gemm_options_t* o,
@@ -647,6 +713,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
             return GEMM_ERR_OPTION;
         p->cg = 2;
         p->cons = 1;
+        p->ks = 1;
         p->bm = 256;
         p->bn = 224;
         const int64_t m_tiles = (M + p->bm - 1) / p->bm;
@@ -687,13 +754,21 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     plan_raster(p, M, N, K, is_fp8(dtype) ? 1 : 2, o);
     int max_clusters = 0;
     st = dispatch<QueryFn>(p->cg, p->bn, b_layout == 1, dtype == GEMM_BF16, p->cons, f8_code(dtype),
-                           dev, di.sm_count, &max_clusters);
+                           1, dev, di.sm_count, &max_clusters);
     if (st != GEMM_OK) return st;
     if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
     p->clusters = int(p->tiles < max_clusters ? p->tiles : max_clusters);
     p->stages = stages_for(p->cg, p->bn, p->cons);
     const int bk = is_fp8(dtype) ? kBlockK8 : kBlockK;
     p->k_blocks = (K + bk - 1) / bk;
+    plan_cluster_split(b_layout, dtype, dev, di.sm_count, o, have_workspace, max_clusters, p);
+    if (p->ks > 1) {
+        // one cluster per tile; no workspace split on top
+        p->whole_units = p->tiles;
+        p->split = 1;
+        size_split(p);
+        return GEMM_OK;
+    }
     plan_split(p, o ? o->tail_split : 0, have_workspace, max_clusters);
     return GEMM_OK;
 }
@@ -781,7 +856,7 @@ int run_impl(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_
         return dispatch_mx<RunFn>(p.cg, p.bn, out_dtype == GEMM_BF16, f8_code(in_fmt), p, A, B, D, M,
                                   N, K, lda, ldb, ldd, in_fmt, out_dtype, alpha, workspace, stream,
                                   SA, SB, wait_limit_ns, clock_probe);
-    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, f8_code(in_fmt), p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
+    return dispatch<RunFn>(p.cg, p.bn, b_layout == 1, out_dtype == GEMM_BF16, p.cons, f8_code(in_fmt), p.ks, p, A, B, D, M, N, K, lda, ldb, ldd, in_fmt, out_dtype,
                            alpha, workspace, stream, static_cast<const void*>(nullptr),
                            static_cast<const void*>(nullptr), wait_limit_ns, clock_probe);
 }
@@ -967,7 +1042,7 @@ extern "C" int gemm_ab(const void* A, const void* B, void* D, int64_t M, int64_t
 extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
                          const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
                          int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split,
-                         int* raster_group, int* raster_order, int* l2_hints) {
+                         int* raster_group, int* raster_order, int* l2_hints, int* cluster_ksplit) {
     int st = check_sizes(M, N, K, dtype, b_layout);
     if (st != GEMM_OK) return st;
     if ((st = check_options(opts)) != GEMM_OK) return st;
@@ -983,6 +1058,7 @@ extern "C" int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layou
     if (raster_group) *raster_group = p.group;
     if (raster_order) *raster_order = p.order + 1;
     if (l2_hints) *l2_hints = int(p.hints | 1u);
+    if (cluster_ksplit) *cluster_ksplit = p.ks;
     return GEMM_OK;
 }
 

@@ -85,10 +85,16 @@ enum : uint32_t {
 };
 
 template <int CG_, int BN_, int STAGES_, bool B_MN_, bool BF16_, int CONS_ = 1, int F8_ = 0,
-          bool MX_ = false>
+          bool MX_ = false, int KS_ = 1>
 struct KernelConfig {
-    static constexpr int CG = CG_;            // CTAs per tile (tcgen05 cta_group)
-    static constexpr int CLUSTER = CG;        // CTAs per cluster: the tile's CTAs
+    static constexpr int CG = CG_;            // CTAs per MMA (tcgen05 cta_group)
+    // K-ranges of one tile computed by the CTAs of a cluster (1-CTA tiles
+    // only): CTA k of the cluster multiplies the k-th of KS K-ranges into its
+    // own TMEM and owns BN / KS of the tile's columns; the CTAs exchange the
+    // FP32 partials of each other's columns through their idle operand rings
+    // over distributed shared memory, and each sums and stores its own.
+    static constexpr int KS = KS_;
+    static constexpr int CLUSTER = CG * KS;   // CTAs per cluster
     // MMA consumers per CTA: 1, or 2 ("TIRx GEMM on Blackwell", V9: two MMAs on
     // different A rows share each staged B tile; each CTA holds 256 A rows).
     static constexpr int CONS = CONS_;
@@ -145,8 +151,10 @@ struct KernelConfig {
     // (the epilogue staging is 128-byte swizzled: 1 KiB aligned)
     static constexpr uint32_t OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023u) & ~1023u;
     static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * EPI_BUFS * EPI_BUF_BYTES;
-    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue warp
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps;
+    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue
+    // warp; with KS > 1 also go[4] (every other CTA's ring may receive) and
+    // done[4] (every other CTA's piece has arrived), one per lane quarter
+    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + (KS > 1 ? 8u : 0u);
     // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
     // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
     // (32 rows x 64 FP32 columns).
@@ -199,6 +207,17 @@ struct KernelConfig {
                   "the last unit's epilogue chunks fit in each warp's share of the ring");
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
+    // In-cluster K split: each other CTA's piece of a lane quarter (32 rows x
+    // BN / KS FP32 columns) lands in a slice of its own in the owner's ring.
+    static constexpr uint32_t RECV_SLICE_BYTES = 32u * uint32_t(BN / KS) * 4u;
+    static_assert(KS == 1 || KS == 2 || KS == 4, "1, 2 or 4 K-ranges per cluster");
+    static_assert(KS == 1 || (CG == 1 && CONS == 1 && !MX), "in-cluster K split: 1-CTA, 1-consumer tiles");
+    static_assert(uint32_t(KS - 1) * 4u * RECV_SLICE_BYTES <= RING_BYTES,
+                  "the other CTAs' pieces fit in the owner's ring");
+    static_assert(KS == 1 || (BN / KS) % 32 == 0, "each CTA owns whole 32-column units");
+    // the epilogue stores 32-column boxes (the last chunk of a 224-wide tile,
+    // or a CTA's share of a 128-wide tile split 4 ways)
+    static constexpr bool D32 = HALF_CHUNK || (KS > 1 && BN / KS == 32);
     static_assert(!MX || (F8 && BN == 224 && CONS == 1 && !B_MN && ACC_STRIDE == 256 &&
                           NUM_ACC == 2 && BK == 128),
                   "MX: FP8 A.Bt, 224-wide tiles (224 accumulator + 32 scale columns per buffer)");
@@ -261,6 +280,20 @@ __host__ __device__ __forceinline__ WorkUnit unit_of(const GemmArgs& a, int64_t 
     return w;
 }
 
+// The k-blocks of unit w that CTA `krank` of a cluster computes: all of them,
+// or with an in-cluster K split (KS > 1) the krank-th of KS ranges.
+template <int KS>
+__device__ __forceinline__ void kb_range(const WorkUnit& w, uint32_t krank, int& kb0, int& kb1) {
+    if constexpr (KS == 1) {
+        kb0 = w.kb0;
+        kb1 = w.kb1;
+    } else {
+        const int n = w.kb1 - w.kb0;
+        kb0 = w.kb0 + int(krank) * n / KS;
+        kb1 = w.kb0 + int(krank + 1u) * n / KS;
+    }
+}
+
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
 // start address >> 4 (bits 0-13), leading-dimension byte offset >> 4 (16-29),
 // stride-dimension byte offset >> 4 (32-45), the fixed version value 1 at bits
@@ -293,21 +326,25 @@ __device__ __forceinline__ uint64_t noswizzle_desc(uint32_t addr, uint32_t lbo, 
     return d;
 }
 
-// A CTA's abort state: its flag (in its shared memory, polled by every role),
-// the shared::cluster address of the same flag in the other CTA of its pair
-// (0 for a CTA alone), and the limit of every wait.
+// A CTA's abort state: its flag (in its shared memory, polled by every role;
+// `flag_addr` is its shared::cta address, the same offset in every CTA of the
+// cluster), the cluster's size and this CTA's rank in it, and the limit of
+// every wait.
 struct AbortCtl {
     volatile uint32_t* flag;
-    uint32_t peer_flag;
+    uint32_t flag_addr;
+    uint32_t cluster_size;
+    uint32_t my_rank;
     uint64_t limit_ns;
 };
 
-// Record the reason and raise the flag in both CTAs of the pair: a role of
-// the other CTA may be the one that would wait for this CTA's work, and every
+// Record the reason and raise the flag in every CTA of the cluster: a role of
+// another CTA may be the one that would wait for this CTA's work, and every
 // warp that sees the flag settles before it leaves (see the teardown).
 __device__ __forceinline__ void raise_abort(const AbortCtl& ac, uint32_t role) {
     *ac.flag = 1u;
-    if (ac.peer_flag) ptx::st_cluster_u32(ac.peer_flag, 1u);
+    for (uint32_t r = 0; r < ac.cluster_size; ++r)
+        if (r != ac.my_rank) ptx::st_cluster_u32(ptx::map_to_rank(ac.flag_addr, r), 1u);
     atomicCAS(&g_gemm_status, 0u, kReasonTimeout | (role << 8));
 }
 
@@ -392,7 +429,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x / 32u, 0);
     const uint32_t lane = threadIdx.x % 32u;
-    const uint32_t rank = (C::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;  // CTA within its pair
+    const uint32_t crank = (C::CLUSTER > 1) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t rank = crank % uint32_t(C::CG);   // CTA within its MMA pair
+    const uint32_t krank = crank / uint32_t(C::CG);  // K-range of the tile (KS > 1)
     const bool leader = (rank == 0u);
     const int64_t cluster_id = blockIdx.x / C::CLUSTER;
     const int64_t num_clusters = gridDim.x / C::CLUSTER;
@@ -405,10 +444,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
     };
     auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
+    auto go_bar = [&](uint32_t q) {
+        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + q);
+    };
+    auto done_bar = [&](uint32_t q) {
+        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 8u + kEpilogueWarps + q);
+    };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
-    const AbortCtl ac{abort_flag,
-                      (C::CLUSTER > 1) ? ptx::map_to_rank(base + C::OFF_ABORT, rank ^ 1u) : 0u,
+    const AbortCtl ac{abort_flag, base + C::OFF_ABORT, uint32_t(C::CLUSTER), crank,
                       args.wait_limit_ns};
 
     // ---- one-time setup -------------------------------------------------
@@ -422,12 +466,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(acc_empty_bar(b), uint32_t(C::CG * kEpilogueWarps));  // all epilogue warps
         }
         for (uint32_t e = 0; e < uint32_t(kEpilogueWarps); ++e) ptx::mbar_init(epi_bar(e), 1);
+        if constexpr (C::KS > 1) {
+            for (uint32_t q = 0; q < 4u; ++q) {
+                ptx::mbar_init(go_bar(q), uint32_t(C::KS - 1));     // each other CTA's warp q
+                ptx::mbar_init(done_bar(q), uint32_t(C::KS - 1));
+            }
+        }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_d);
-        if constexpr (C::HALF_CHUNK) ptx::prefetch_tensormap(&tmap_d32);
+        if constexpr (C::D32) ptx::prefetch_tensormap(&tmap_d32);
         if constexpr (C::MX) {
             ptx::prefetch_tensormap(&tmap_sa);
             ptx::prefetch_tensormap(&tmap_sb);
@@ -499,7 +549,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tile_of_task(args.grid, w.tile, mt, nt);
             const int32_t a_row = mt * C::BM + int32_t(rank) * C::A_ROWS;
             const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            int kr0, kr1;
+            kb_range<C::KS>(w, krank, kr0, kr1);
+            for (int kb = kr0; kb < kr1; ++kb) {
                 if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, ac, kRoleProducer)) {
                     ok = false;
                     break;
@@ -687,13 +739,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // either way (448 tensor cycles), which fits the shared-memory
                 // traffic it needs per SM (44 KiB of MMA operand reads and 30 KiB
                 // of TMA writes) better than the issue loop's cost.
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                int kr0, kr1;
+                kb_range<C::KS>(w, krank, kr0, kr1);
+                for (int kb = kr0; kb < kr1; ++kb) {
                     if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    if (ptx::elect_one_sync()) issue_kblock(s, sfbuf, kb == w.kb0);
+                    if (ptx::elect_one_sync()) issue_kblock(s, sfbuf, kb == kr0);
                     __syncwarp();
                     sfbuf ^= 1u;
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
@@ -726,6 +780,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t my_epi_bar = epi_bar(warp - 2u);
         const uint32_t my_ring = base + C::OFF_A + (warp - 2u) * C::PIECES_PER_WARP * C::PIECE_BYTES;
         uint32_t ab = 0, aph = 0, chunk = 0, eph = 0;
+        uint32_t gph = 0, dph = 0;  // in-cluster K split: go / done phases
 
         // Hand accumulator `b` back to the MMA issuer (all TMEM reads done).
         auto release_acc = [&](uint32_t b) {
@@ -882,48 +937,161 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // MMAs (>= 32 k-blocks) outlast them and a second accumulator exists.
             const bool pace = (C::NUM_ACC == 2) && !last_unit && w.kb1 - w.kb0 >= kStorePaceMinKBlocks;
             if (w.range < 0) {
-                // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
-                // the CTA's A rows 128h..128h+127), 32 columns at a time: the
-                // TMEM load of the next 32 columns is in flight while the
-                // current ones are converted and staged, and each 64-column
-                // chunk (or the last 32 columns of a 224-wide tile) leaves as
-                // one TMA store once both of its halves are staged.
-#pragma unroll 1
-                for (int h = 0; h < C::CONS; ++h) {
-                    const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
-                    const int32_t rh = row0 + 128 * h;
-                    const bool last_h = (h == C::CONS - 1);
-                    constexpr int U = C::BN / 32;  // 32-column units
-                    constexpr int CHUNKS = C::FULL_CHUNKS + (C::HALF_CHUNK ? 1 : 0);
-                    uint32_t ra[32], rb[32];
-                    uint32_t buf = 0;
-                    ptx::tmem_ld_32x32b_x32(th, ra);
-                    ptx::tmem_wait_ld();
+                if constexpr (C::KS > 1) {
+                    // In-cluster K split, summed as a reduce-scatter: CTA k owns
+                    // columns [k W, (k+1) W) of the tile (W = BN / KS).  Once its
+                    // own MMAs are done its ring is idle (one unit per cluster):
+                    // it tells every other CTA so (their go[quarter]), waits
+                    // until every other CTA has said the same, writes its FP32
+                    // partial of each other CTA's columns for these 32 rows into
+                    // that CTA's ring over distributed shared memory and arrives
+                    // on that CTA's done[quarter].  Then it adds the others'
+                    // partials of its own columns to its own in CTA order (the
+                    // same sum, term for term, whichever CTA owns the columns)
+                    // and stores them.
+                    constexpr int W = C::BN / C::KS;
+                    constexpr int UW = W / 32;             // 32-column units it owns
+                    constexpr int T = (C::KS - 1) * UW;    // units it sends
+                    // where CTA `src`'s piece of this quarter lands in CTA `dst`
+                    auto recv_slice = [&](uint32_t dst, uint32_t src) -> uint32_t {
+                        const uint32_t slot = src - (src > dst ? 1u : 0u);
+                        return base + C::OFF_A + (slot * 4u + quarter) * C::RECV_SLICE_BYTES;
+                    };
+                    auto send_dst = [&](int t) -> uint32_t {
+                        const uint32_t r = uint32_t(t / UW);
+                        return r + (r >= krank ? 1u : 0u);
+                    };
+                    if (lane == 0)
+                        for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
+                            if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(go_bar(quarter), r));
+                    uint32_t okg = 1u;
+                    if (lane == 0) okg = wait_bounded(go_bar(quarter), gph, ac, kRoleEpilogue);
+                    okg = __shfl_sync(0xffffffffu, okg, 0);
+                    if (!okg) break;
+                    while (!ptx::mbar_try_wait(go_bar(quarter), gph)) {
+                    }  // completed already: every lane's own acquire
+                    gph ^= 1u;
+                    {
+                        uint32_t ra[32], rb[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + send_dst(0) * W, ra);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        uint32_t(&cur)[32] = (u % 2 == 0) ? ra : rb;
-                        uint32_t(&nxt)[32] = (u % 2 == 0) ? rb : ra;
-                        if (u + 1 < U) {
-                            ptx::tmem_ld_32x32b_x32(th + 32u * uint32_t(u + 1), nxt);
-                        } else {
-                            // every TMEM read of this accumulator is done; two
-                            // consumers go back each on its own barrier
-                            if (C::CONS == 2) release(uint32_t(h));
-                            else if (last_h) release(ab);
+                        for (int t = 0; t < T; ++t) {
+                            uint32_t(&cur)[32] = (t % 2 == 0) ? ra : rb;
+                            uint32_t(&nxt)[32] = (t % 2 == 0) ? rb : ra;
+                            if (t + 1 < T)
+                                ptx::tmem_ld_32x32b_x32(taddr + send_dst(t + 1) * W + 32u * uint32_t((t + 1) % UW),
+                                                        nxt);
+                            const uint32_t dst = send_dst(t);
+                            const uint32_t sl = ptx::map_to_rank(recv_slice(dst, krank), dst);
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                ptx::st_cluster_v4(sl + ((uint32_t(t % UW) * 8u + uint32_t(g)) * 32u + lane) * 16u,
+                                                   cur[4 * g], cur[4 * g + 1], cur[4 * g + 2], cur[4 * g + 3]);
+                            if (t + 1 < T) ptx::tmem_wait_ld();
                         }
-                        const int c = u / 2;
-                        const bool first_half = (u % 2 == 0);
-                        const bool narrow = C::HALF_CHUNK && (c == C::FULL_CHUNKS);  // 32 columns
-                        if (first_half) {
-                            if (pace && c > 0) __nanosleep(kStorePaceNs);
-                            buf = stage_buffer(last_unit ? h * CHUNKS + c : -1);
+                    }
+                    ptx::fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0)
+                        for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
+                            if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(done_bar(quarter), r));
+                    // this CTA's own columns: its partial from TMEM (the first
+                    // load in flight while the others' pieces arrive)
+                    const uint32_t town = taddr + krank * uint32_t(W);
+                    uint32_t ra[32], rb[32];
+                    ptx::tmem_ld_32x32b_x32(town, ra);
+                    uint32_t okd = 1u;
+                    if (lane == 0) okd = wait_bounded(done_bar(quarter), dph, ac, kRoleEpilogue);
+                    okd = __shfl_sync(0xffffffffu, okd, 0);
+                    ptx::tmem_wait_ld();
+                    if (!okd) break;
+                    while (!ptx::mbar_try_wait(done_bar(quarter), dph)) {
+                    }  // completed already: every lane's own acquire
+                    dph ^= 1u;
+                    uint32_t buf = 0;
+#pragma unroll
+                    for (int v = 0; v < UW; ++v) {
+                        uint32_t(&cur)[32] = (v % 2 == 0) ? ra : rb;
+                        uint32_t(&nxt)[32] = (v % 2 == 0) ? rb : ra;
+                        if (v + 1 < UW) ptx::tmem_ld_32x32b_x32(town + 32u * uint32_t(v + 1), nxt);
+                        else release(ab);  // every TMEM read of this accumulator is done
+                        // sum = p_0 + p_1 + ... in CTA order (p_krank from TMEM)
+                        float acc[32];
+#pragma unroll 1
+                        for (uint32_t r = 0; r < uint32_t(C::KS); ++r) {
+                            if (r == krank) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const float x = __uint_as_float(cur[i]);
+                                    acc[i] = (r == 0) ? x : acc[i] + x;
+                                }
+                                continue;
+                            }
+                            const uint32_t sl = recv_slice(krank, r);
+#pragma unroll
+                            for (int g = 0; g < 8; ++g) {
+                                float x[4];
+                                ptx::ld_shared_v4(sl + ((uint32_t(v) * 8u + uint32_t(g)) * 32u + lane) * 16u,
+                                                  x[0], x[1], x[2], x[3]);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    acc[4 * g + i] = (r == 0) ? x[i] : acc[4 * g + i] + x[i];
+                            }
                         }
-                        stage_half(cur, buf, narrow ? 32 : 64, first_half ? 0 : 1);
-                        if (!first_half || narrow) issue_store(buf, col0 + 64 * c, rh, narrow ? 32 : 64);
-                        if (u + 1 < U) ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) cur[i] = __float_as_uint(acc[i]);
+                        const bool first_half = (v % 2 == 0);
+                        if (first_half) buf = stage_buffer(-1);  // (the ring holds the pieces)
+                        stage_half(cur, buf, W == 32 ? 32 : 64, first_half ? 0 : 1);
+                        if (!first_half || W == 32)
+                            issue_store(buf, col0 + int32_t(krank) * W + 64 * (v / 2), row0, W == 32 ? 32 : 64);
+                        if (v + 1 < UW) ptx::tmem_wait_ld();
+                    }
+                } else {
+                    // Whole tile: TMEM -> D, consumer by consumer (consumer h holds
+                    // the CTA's A rows 128h..128h+127), 32 columns at a time: the
+                    // TMEM load of the next 32 columns is in flight while the
+                    // current ones are converted and staged, and each 64-column
+                    // chunk (or the last 32 columns of a 224-wide tile) leaves as
+                    // one TMA store once both of its halves are staged.
+#pragma unroll 1
+                    for (int h = 0; h < C::CONS; ++h) {
+                        const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
+                        const int32_t rh = row0 + 128 * h;
+                        const bool last_h = (h == C::CONS - 1);
+                        constexpr int U = C::BN / 32;  // 32-column units
+                        constexpr int CHUNKS = C::FULL_CHUNKS + (C::HALF_CHUNK ? 1 : 0);
+                        uint32_t ra[32], rb[32];
+                        uint32_t buf = 0;
+                        ptx::tmem_ld_32x32b_x32(th, ra);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            uint32_t(&cur)[32] = (u % 2 == 0) ? ra : rb;
+                            uint32_t(&nxt)[32] = (u % 2 == 0) ? rb : ra;
+                            if (u + 1 < U) {
+                                ptx::tmem_ld_32x32b_x32(th + 32u * uint32_t(u + 1), nxt);
+                            } else {
+                                // every TMEM read of this accumulator is done; two
+                                // consumers go back each on its own barrier
+                                if (C::CONS == 2) release(uint32_t(h));
+                                else if (last_h) release(ab);
+                            }
+                            const int c = u / 2;
+                            const bool first_half = (u % 2 == 0);
+                            const bool narrow = C::HALF_CHUNK && (c == C::FULL_CHUNKS);  // 32 columns
+                            if (first_half) {
+                                if (pace && c > 0) __nanosleep(kStorePaceNs);
+                                buf = stage_buffer(last_unit ? h * CHUNKS + c : -1);
+                            }
+                            stage_half(cur, buf, narrow ? 32 : 64, first_half ? 0 : 1);
+                            if (!first_half || narrow) issue_store(buf, col0 + 64 * c, rh, narrow ? 32 : 64);
+                            if (u + 1 < U) ptx::tmem_wait_ld();
+                        }
                     }
                 }
-            } else {
+            } else if constexpr (C::KS == 1) {  // (no tail split with an in-cluster split)
                 // K-range of a tail tile.  Pass 1: write this range's FP32 partial
                 // for the warp's 32 rows to its workspace slot, laid out so that
                 // consecutive lanes touch consecutive 16-byte words.
@@ -1118,7 +1286,7 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
         abort_flag = 0u;
         ptx::mbar_init(ptx::smem_addr(&bar), 1);
         ptx::fence_mbar_init();
-        const AbortCtl ac{&abort_flag, 0u, limit_ns};
+        const AbortCtl ac{&abort_flag, 0u, 1u, 0u, limit_ns};
         wait_bounded(ptx::smem_addr(&bar), 0u, ac, kRoleSelfTest);
     }
 }

@@ -136,6 +136,17 @@ const char* gemm_status_string(int status);
  *                 GEMM_ERR_OPTION) whose other bits set L2 eviction
  *                 priorities: 2 = A's loads evict_last, 4 = B's loads
  *                 evict_first, 8 = D's stores evict_first (1 = no hints).
+ *   cluster_ksplit  0 = automatic, 1 = never, 2 or 4 = that many K-ranges per
+ *                 tile inside a cluster: a problem whose 1-CTA tiles (128
+ *                 wide; 256 wide with 2 ranges) all fit in one round of such
+ *                 clusters has each tile computed by a cluster of that many
+ *                 CTAs, one K-range each; each CTA owns an equal share of the
+ *                 tile's columns, receives the others' FP32 partials of them
+ *                 through distributed shared memory and stores their sum,
+ *                 taken in CTA order (no workspace).  Automatic: the most
+ *                 ranges that keep at least 16 of K's 64-wide blocks per
+ *                 range, unless the workspace split (tail_split) would run
+ *                 more ranges per tile.  16-bit inputs only.
  */
 typedef struct {
     int cta_group;
@@ -147,6 +158,7 @@ typedef struct {
     int multicast;
     int raster_order;
     int l2_hints;
+    int cluster_ksplit;
 } gemm_options_t;
 
 /* b_layout: 0 = B is N x K (D = A.B^T), 1 = B is K x N (D = A.B). */
@@ -339,7 +351,8 @@ int gemm_run_no_alloc(const void* A, const void* B, void* D, int64_t M, int64_t 
 /*
  * Plan of a call, without launching: the tile shape, grid, stage count, tail
  * split, raster group and order (1 = M groups, 2 = N groups, as the
- * options) and L2 hints (an explicit, odd l2_hints value) that
+ * options), L2 hints (an explicit, odd l2_hints value) and in-cluster K
+ * ranges per tile (1 = none) that
  * gemm_run_workspace (with a large enough workspace) would use for these
  * sizes on the current device.  Any out pointer may be NULL.  Returns the
  * same argument errors as gemm_run (pointers are not checked).
@@ -347,7 +360,7 @@ int gemm_run_no_alloc(const void* A, const void* B, void* D, int64_t M, int64_t 
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout,
               const gemm_options_t* opts, int* cta_group, int* block_m, int* block_n,
               int* stages, int* num_clusters, int64_t* num_tiles, int* tail_split,
-              int* raster_group, int* raster_order, int* l2_hints);
+              int* raster_group, int* raster_order, int* l2_hints, int* cluster_ksplit);
 
 /*
  * The persistent scheduler's task -> tile map (the same function the kernel

@@ -30,9 +30,11 @@ VARIANTS = [
     {"cta_group": 1, "block_n": 224, "raster_group": 0, "max_clusters": 0, "tail_split": 0},
     {"cta_group": 2, "block_n": 256, "raster_group": 0, "max_clusters": 0, "tail_split": 0,
      "consumers": 2},
+    {"cta_group": 1, "block_n": 128, "cluster_ksplit": 4},
+    {"cta_group": 1, "block_n": 256, "cluster_ksplit": 2},
 ]
 VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224",
-       "cg2_n256_2cons"]
+       "cg2_n256_2cons", "cg1_n128_ks4", "cg1_n256_ks2"]
 
 
 def k_major_only(variant, layout):
@@ -318,8 +320,9 @@ def test_wait_timeout_is_reported_and_context_survives():
 
 
 @pytest.mark.parametrize("opts", [None, {"cta_group": 1}, {"cta_group": 2, "max_clusters": 3},
-                                  {"cta_group": 2, "consumers": 2}],
-                         ids=["default", "cg1", "cg2_3clusters", "cg2_2cons"])
+                                  {"cta_group": 2, "consumers": 2},
+                                  {"cta_group": 1, "block_n": 128, "cluster_ksplit": 4}],
+                         ids=["default", "cg1", "cg2_3clusters", "cg2_2cons", "cg1_ks4"])
 def test_gemm_kernel_abort_path(opts):
     # The GEMM kernel itself with a 100 ns limit on every barrier wait: the
     # first operands take microseconds to arrive, so a wait gives up.  The
@@ -328,6 +331,9 @@ def test_gemm_kernel_abort_path(opts):
     # normal GEMM must be correct.
     assert binding.gemm_device_status(clear=True) == 0
     M, N, K = 1024, 1024, 1024
+    if opts and opts.get("cluster_ksplit"):
+        M, N, K = 256, 512, 2048  # 8 tiles: one 4-CTA cluster each
+        assert binding.gemm_plan(M, N, K, 0, 0, opts)["cluster_ksplit"] == 4
     A, B = inputs.operands(M, N, K, "abt", "f16", "uniform", 31)
     dA, dB = to_device(A, "f16"), to_device(B, "f16")
     D = torch.empty((M, N), dtype=torch.float16, device="cuda")
@@ -365,15 +371,19 @@ def test_split_tail(case, layout, dtype):
            options=opts)
 
 
+NO_CLUSTER_SPLIT = {"cluster_ksplit": 1}
+
+
 def test_automatic_k_split_of_single_round_problems():
     # Tiles that fit one round with clusters to spare share their K loop over the
-    # idle clusters when a workspace is given: at least 64 k-blocks per range.
-    p = binding.gemm_plan(512, 512, 16384, 0, 0)       # 16 1-CTA tiles, 256 k-blocks
+    # idle clusters when a workspace is given: at least 64 k-blocks per range
+    # (here with the in-cluster split turned off, which takes precedence).
+    p = binding.gemm_plan(512, 512, 16384, 0, 0, NO_CLUSTER_SPLIT)  # 16 1-CTA tiles, 256 k-blocks
     assert p["num_tiles"] == 16 and p["tail_split"] == 4 and p["num_clusters"] == 64
-    assert binding.gemm_workspace_size(512, 512, 16384, 0, 0) > 0
-    q = binding.gemm_plan(256, 256, 1024, 0, 0)        # 16 k-blocks: never split
+    assert binding.gemm_workspace_size(512, 512, 16384, 0, 0, NO_CLUSTER_SPLIT) > 0
+    q = binding.gemm_plan(256, 256, 1024, 0, 0, NO_CLUSTER_SPLIT)  # 16 k-blocks: never split
     assert q["tail_split"] == 1
-    r = binding.gemm_plan(512, 512, 16384, 0, 0, {"tail_split": 1})
+    r = binding.gemm_plan(512, 512, 16384, 0, 0, {"tail_split": 1, "cluster_ksplit": 1})
     assert r["tail_split"] == 1 and r["num_clusters"] == 16
 
 
@@ -384,9 +394,72 @@ def test_automatic_k_split_of_single_round_problems():
 ])
 def test_automatic_k_split_parity(shape, layout, dtype):
     M, N, K = shape
-    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1)
+    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1,
+                             NO_CLUSTER_SPLIT)
     assert plan["tail_split"] >= 2
-    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + 7)
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + 7,
+           options=NO_CLUSTER_SPLIT)
+
+
+def test_in_cluster_k_split_plans():
+    # Problems whose 1-CTA tiles fit one round of clusters of 4 (or 2) CTAs
+    # split each tile's K loop inside its cluster, keeping >= 16 k-blocks per
+    # range, unless the workspace split would run more ranges per tile.
+    p = binding.gemm_plan(256, 256, 4096, 0, 0)        # 4 tiles x 64 k-blocks
+    assert (p["cta_group"], p["block_n"], p["cluster_ksplit"]) == (1, 128, 4)
+    assert p["num_clusters"] == p["num_tiles"] == 4 and p["tail_split"] == 1
+    q = binding.gemm_plan(256, 4096, 4096, 0, 0)       # clusters of 4 do not fit
+    assert q["cluster_ksplit"] == 2
+    assert binding.gemm_plan(1024, 1024, 8192, 0, 0)["cluster_ksplit"] == 2
+    assert binding.gemm_plan(512, 512, 16384, 0, 0)["cluster_ksplit"] == 4
+    # 16 k-blocks: 8 per range would not pay for the exchange
+    assert binding.gemm_plan(256, 256, 1024, 0, 0)["cluster_ksplit"] == 1
+    # the workspace split runs 8 ranges per tile here, more than 4
+    r = binding.gemm_plan(256, 512, 32768, 0, 0)
+    assert r["cluster_ksplit"] == 1 and r["tail_split"] == 8
+    assert binding.gemm_plan(128, 128, 64, 0, 0)["cluster_ksplit"] == 1  # one k-block
+    assert binding.gemm_plan(128, 128, 64, 0, 0, {"cluster_ksplit": 2})["cluster_ksplit"] == 1
+    assert binding.gemm_plan(4096, 4096, 4096, 0, 0)["cluster_ksplit"] == 1
+    assert binding.gemm_plan(256, 256, 1024, 0, 0, {"cluster_ksplit": 2})["cluster_ksplit"] == 2
+    assert binding.gemm_plan(256, 256, 4096, 0, 0, NO_CLUSTER_SPLIT)["cluster_ksplit"] == 1
+    # needs no workspace
+    assert binding.gemm_workspace_size(256, 256, 4096, 0, 0) == 0
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+@pytest.mark.parametrize("shape,layout,dtype", [
+    ((256, 256, 1024), "abt", "f16"),     # the 16-k-block case
+    ((300, 520, 2000), "abt", "bf16"),    # ragged tiles, K not a multiple of 64
+    ((384, 640, 4096), "ab", "f16"),      # MN-major B
+    ((128, 1024, 1040), "ab", "bf16"),    # odd k-blocks per range
+    ((200, 136, 5000), "abt", "f16"),     # CTAs whose columns lie wholly past N
+])
+def test_in_cluster_k_split_parity(ks, shape, layout, dtype):
+    M, N, K = shape
+    opts = {"cta_group": 1, "block_n": 128, "cluster_ksplit": ks}
+    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1,
+                             opts)
+    assert plan["cluster_ksplit"] == ks
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + ks,
+           options=opts)
+
+
+def test_in_cluster_k_split_exact_and_deterministic():
+    # Small integers: every partial and the CTA-order sum are exact in FP32.
+    M, N, K = 256, 512, 2048
+    A, B = small_int_operands(M, N, K, "abt", "f16", seed=9, lim=1)
+    for opts in ({"cta_group": 1, "block_n": 128, "cluster_ksplit": 4},
+                 {"cta_group": 1, "block_n": 256, "cluster_ksplit": 2}):
+        assert binding.gemm_plan(M, N, K, 0, 0, opts)["cluster_ksplit"] == opts["cluster_ksplit"]
+        got = from_device(run(A, B, "abt", "f16", opts))
+        assert np.array_equal(got, oracle.gemm(A, B, layout="abt", dtype="f16"))
+    Af, Bf = inputs.operands(M, N, K, "abt", "f16", "uniform", 10)
+    dA, dB = to_device(Af, "f16"), to_device(Bf, "f16")
+    opts = {"cta_group": 1, "block_n": 128, "cluster_ksplit": 4}
+    d1 = binding.gemm_abt(dA, dB, options=opts)
+    d2 = binding.gemm_abt(dA, dB, options=opts)
+    torch.cuda.synchronize()
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
 
 
 def test_split_tail_deterministic_and_workspace_reused():
