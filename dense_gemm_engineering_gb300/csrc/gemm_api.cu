@@ -195,7 +195,9 @@ int query_max_clusters(int dev, int sm_count) {
 // Stage counts: as many 128-byte-swizzled K slices as fit next to the
 // 32 KiB epilogue staging in 227 KiB.
 constexpr int stages_for(int cg, int bn, int cons) {
-    return (227 * 1024 - 32768 - 1024 - 512) / (128 * cons * 64 * 2 + (bn / cg) * 64 * 2);
+    // (1-CTA tiles of at most 128 columns pair their stages: an even count)
+    return ((227 * 1024 - 32768 - 1024 - 512) / (128 * cons * 64 * 2 + (bn / cg) * 64 * 2)) &
+           ((cg == 1 && cons == 1 && bn <= 128) ? ~1 : ~0);
 }
 template <int CG, int BN, int CONS = 1>
 struct Stages {
@@ -387,7 +389,7 @@ template <template <class> class Fn, class... Ts>
 int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, int ks, Ts&&... ts) {
     if (ks != 1) {
         // In-cluster K split: 16-bit, 1-CTA tiles, 128 wide (2 or 4 ranges)
-        // or 256 wide (2 ranges).
+        // or 64 / 256 wide (2 ranges).
         if (f8 != 0 || cons != 1 || cg != 1) return GEMM_ERR_OPTION;
 #define GB300_CASEKS(BN_, KS_, MN_, BF_)                                                 \
     if (bn == BN_ && ks == KS_ && b_mn == MN_ && bf16 == BF_)                            \
@@ -398,6 +400,7 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, int ks, Ts&
         GB300_CASESKS(128, 2)
         GB300_CASESKS(128, 4)
         GB300_CASESKS(256, 2)
+        GB300_CASESKS(64, 2)
 #undef GB300_CASESKS
 #undef GB300_CASEKS
         return GEMM_ERR_OPTION;
@@ -434,6 +437,8 @@ int dispatch(int cg, int bn, bool b_mn, bool bf16, int cons, int f8, int ks, Ts&
     GB300_CASES(1, 256)
     GB300_CASES(2, 128)
     GB300_CASES(1, 128)
+    GB300_CASES(1, 64)
+    GB300_KMAJOR_CASES(1, 32)
     GB300_KMAJOR_CASES(2, 224)
     GB300_KMAJOR_CASES(2, 192)
     GB300_KMAJOR_CASES(1, 224)
@@ -507,8 +512,8 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int dtype, int b_layout) {
 int check_options(const gemm_options_t* o) {
     if (!o) return GEMM_OK;
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_OPTION;
-    if (o->block_n != 0 && o->block_n != 128 && o->block_n != 192 && o->block_n != 224 &&
-        o->block_n != 256)
+    if (o->block_n != 0 && o->block_n != 32 && o->block_n != 64 && o->block_n != 128 &&
+        o->block_n != 192 && o->block_n != 224 && o->block_n != 256)
         return GEMM_ERR_OPTION;
     if (o->raster_group < 0 || o->max_clusters < 0) return GEMM_ERR_OPTION;
     if (o->tail_split < 0 || o->tail_split > kMaxSplit) return GEMM_ERR_OPTION;
@@ -664,8 +669,14 @@ void spread_small(int64_t M, int64_t N, int b_layout, int dtype, int dev, int sm
 // 4), so the automatic choice is the most ranges (4 for 128-wide tiles, 2
 // for 256-wide) that keep at least kMinClusterRangeKBlocks k-blocks per
 // range, and none when the workspace split (plan_split) would run more
-// ranges per tile.
+// ranges per tile or when K has fewer than kNarrowMaxKBlocks k-blocks.
 constexpr int64_t kMinClusterRangeKBlocks = 16;
+// Below kNarrowMaxKBlocks k-blocks (and from kNarrowMinKBlocks) a single-round
+// problem takes narrow tiles instead (plan_narrow), which measured faster than
+// splitting K in the cluster there (1024 x 1024 x 2048: 14.8 us on 64-wide
+// tiles, 16.8 us with 2 ranges per 128-wide tile).
+constexpr int64_t kNarrowMinKBlocks = 8;
+constexpr int64_t kNarrowMaxKBlocks = 64;
 
 void plan_cluster_split(int b_layout, int dtype, int dev, int sm_count, const gemm_options_t* o,
                         bool have_workspace, int max_clusters, Plan* p) {
@@ -685,13 +696,45 @@ void plan_cluster_split(int b_layout, int dtype, int dev, int sm_count, const ge
     for (int ks : cands) {
         if (req >= 2 && ks != req) continue;
         if (ks == 4 && p->bn != 128) continue;
-        if (req == 0 && (p->k_blocks < ks * kMinClusterRangeKBlocks || ws_ranges > ks)) continue;
+        if (req == 0 && (p->k_blocks < ks * kMinClusterRangeKBlocks || ws_ranges > ks ||
+                         p->k_blocks < kNarrowMaxKBlocks))
+            continue;
         if (p->k_blocks < ks) continue;
         int C = max_clusters_for(1, p->bn, b_layout, dtype, dev, sm_count, ks);
         if (o && o->max_clusters && o->max_clusters < C) C = o->max_clusters;
         if (C <= 0 || p->tiles > C) continue;
         p->ks = ks;
         p->clusters = int(p->tiles);
+        return;
+    }
+}
+
+// Narrow tiles for shallow single-round problems: a 1-CTA tile's k-block costs
+// the MMA warp ~400 cycles of issue whatever its width up to 128 columns
+// (paired stages), and a 128-wide one is bound at ~515 cycles by the 32 KiB
+// each SM must take in per k-block, so a problem whose 128-wide tiles fit one
+// round with SMs to spare finishes sooner on 32- (B N x K only) or 64-wide
+// tiles if those still fit one round.  Measured (L2 flushed): 256 x 256 x 1024
+// 12.5 -> 10.5 us on 32-wide tiles, 1024 x 1024 x 2048 16.8 -> 14.8 us on
+// 64-wide.  Only below kNarrowMaxKBlocks k-blocks: deeper problems gain more
+// from splitting K (in the cluster or over the workspace), which needs 64- or
+// 128-wide tiles.
+
+void plan_narrow(int64_t M, int64_t N, int b_layout, int dtype, int dev, int sm_count, Plan* p) {
+    if (is_fp8(dtype) || p->cg != 1 || p->cons != 1 || p->bn != 128 || p->ks != 1) return;
+    if (p->k_blocks < kNarrowMinKBlocks || p->k_blocks >= kNarrowMaxKBlocks) return;
+    const int C128 = max_clusters_for(1, 128, b_layout, dtype, dev, sm_count);
+    if (C128 <= 0 || p->tiles > C128) return;  // 128-wide tiles take more than one round
+    const int cands[2] = {32, 64};
+    for (int bn : cands) {
+        if (bn == 32 && b_layout != 0) continue;
+        const int C = max_clusters_for(1, bn, b_layout, dtype, dev, sm_count);
+        const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+        if (C <= 0 || tiles > C) continue;
+        p->bn = bn;
+        p->tiles = tiles;
+        p->clusters = int(tiles);
+        p->stages = stages_for(1, bn, 1);
         return;
     }
 }
@@ -740,8 +783,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
         p->bn = 256;
     } else if (o && o->block_n) {
         p->bn = o->block_n;
-        // 192 / 224 are K-major only: an MN-major B tile is loaded in 64-column atoms.
-        if (b_layout == 1 && (p->bn % 128) != 0) return GEMM_ERR_OPTION;
+        // 32- and 64-wide tiles are 1-CTA tiles (an explicit cta_group 2 is an
+        // error; an automatic one becomes 1).
+        if (p->bn < 128) {
+            if (o->cta_group == 2) return GEMM_ERR_OPTION;
+            p->cg = 1;
+            p->bm = 128;
+        }
+        // An MN-major B tile is loaded in 64-column atoms: 64- (1-CTA), 128-
+        // and 256-wide tiles only.
+        if (b_layout == 1 && (p->bn % 128) != 0 && p->bn != 64) return GEMM_ERR_OPTION;
     } else {
         p->bn = choose_block_n(M, N, p->bm, b_layout, p->cg, dtype, dev, di.sm_count);
         const bool cg_free = !(o && o->cta_group);
@@ -762,6 +813,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dtype, int b_layout, const ge
     const int bk = is_fp8(dtype) ? kBlockK8 : kBlockK;
     p->k_blocks = (K + bk - 1) / bk;
     plan_cluster_split(b_layout, dtype, dev, di.sm_count, o, have_workspace, max_clusters, p);
+    if (!(o && o->block_n)) {
+        const int bn0 = p->bn;
+        plan_narrow(M, N, b_layout, dtype, dev, di.sm_count, p);
+        if (p->bn != bn0) {
+            plan_raster(p, M, N, K, 2, o);
+            max_clusters = max_clusters_for(1, p->bn, b_layout, dtype, dev, di.sm_count);
+            if (o && o->max_clusters && o->max_clusters < max_clusters) max_clusters = o->max_clusters;
+            if (p->clusters > max_clusters) p->clusters = max_clusters;
+        }
+    }
     if (p->ks > 1) {
         // one cluster per tile; no workspace split on top
         p->whole_units = p->tiles;

@@ -143,6 +143,15 @@ struct KernelConfig {
     // previous one's reads; the stores of a tile are paced 1 us apart anyway).
     static constexpr uint32_t EPI_BUFS = MX ? 1u : 2u;
     static constexpr uint32_t MN_ATOM_BYTES = 64u * 128u;              // MN-major: 64 K x 64 N
+    // K-blocks per ring barrier.  The MMA warp pays a fixed cost per pass
+    // (~200 cycles for the barrier wait, vote and fence, ~50 for the commit)
+    // on top of ~70 cycles per MMA issued; a 1-CTA tile of at most 128
+    // columns has only 256 tensor cycles per k-block to hide it in, so its
+    // stages go in pairs: one full and one empty barrier per pair, one wait
+    // and one commit per two k-blocks.  2-CTA and wider tiles are tensor-bound
+    // with one k-block per pass.
+    static constexpr int G = (CG == 1 && CONS == 1 && !MX && BN <= 128) ? 2 : 1;
+    static constexpr int GROUPS = STAGES / G;  // ring barrier pairs (full, empty)
 
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
@@ -151,10 +160,10 @@ struct KernelConfig {
     // (the epilogue staging is 128-byte swizzled: 1 KiB aligned)
     static constexpr uint32_t OFF_EPI = (OFF_SFB + STAGES * SFB_BYTES + 1023u) & ~1023u;
     static constexpr uint32_t OFF_BAR = OFF_EPI + kEpilogueWarps * EPI_BUFS * EPI_BUF_BYTES;
-    // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], one per epilogue
+    // full[GROUPS], empty[GROUPS], acc_full[2], acc_empty[2], one per epilogue
     // warp; with KS > 1 also go[4] (every other CTA's ring may receive) and
     // done[4] (every other CTA's piece has arrived), one per lane quarter
-    static constexpr uint32_t NUM_BARS = 2u * STAGES + 4u + kEpilogueWarps + (KS > 1 ? 8u : 0u);
+    static constexpr uint32_t NUM_BARS = 2u * GROUPS + 4u + kEpilogueWarps + (KS > 1 ? 8u : 0u);
     // Split-tail fix-up: in a cluster's last unit the ring is idle, and each
     // epilogue warp may use RING_BYTES / 4 of it for partial pieces of 8 KiB
     // (32 rows x 64 FP32 columns).
@@ -198,10 +207,13 @@ struct KernelConfig {
                   "instruction descriptor fields in range");
 
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
-    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile N is a multiple of 32 in [128, 256]");
+    static_assert(BN == 32 || BN == 64 || (BN % 32 == 0 && BN >= 128 && BN <= 256),
+                  "tile N is 32, 64 or a multiple of 32 in [128, 256]");
+    static_assert(BN >= 128 || (CG == 1 && CONS == 1 && !MX), "32- and 64-wide tiles: 1 CTA, 1 consumer");
     static_assert((BN / CG) % 16 == 0, "each CTA's share of B is whole 16-row SW128 groups");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(CONS == 1 || CONS == 2, "one or two MMA consumers");
+    static_assert(STAGES % G == 0 && GROUPS >= 2, "whole groups of stages, at least two");
     static_assert(CONS * (FULL_CHUNKS + (HALF_CHUNK ? 1 : 0)) * EPI_BUF_BYTES <=
                       PIECES_PER_WARP * PIECE_BYTES,
                   "the last unit's epilogue chunks fit in each warp's share of the ring");
@@ -437,18 +449,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int64_t num_clusters = gridDim.x / C::CLUSTER;
     const int64_t units = unit_count(args);
 
-    auto full_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return base + C::OFF_BAR + 8u * (C::STAGES + s); };
-    auto acc_full_bar = [&](uint32_t b) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + b); };
+    // Ring barriers, one pair per group of C::G stages (g = stage / C::G).
+    auto full_bar = [&](uint32_t g) { return base + C::OFF_BAR + 8u * g; };
+    auto empty_bar = [&](uint32_t g) { return base + C::OFF_BAR + 8u * (C::GROUPS + g); };
+    auto acc_full_bar = [&](uint32_t b) { return base + C::OFF_BAR + 8u * (2u * C::GROUPS + b); };
     auto acc_empty_bar = [&](uint32_t b) {
-        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 2u + b);
+        return base + C::OFF_BAR + 8u * (2u * C::GROUPS + 2u + b);
     };
-    auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + e); };
+    auto epi_bar = [&](uint32_t e) { return base + C::OFF_BAR + 8u * (2u * C::GROUPS + 4u + e); };
     auto go_bar = [&](uint32_t q) {
-        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 4u + kEpilogueWarps + q);
+        return base + C::OFF_BAR + 8u * (2u * C::GROUPS + 4u + kEpilogueWarps + q);
     };
     auto done_bar = [&](uint32_t q) {
-        return base + C::OFF_BAR + 8u * (2u * C::STAGES + 8u + kEpilogueWarps + q);
+        return base + C::OFF_BAR + 8u * (2u * C::GROUPS + 8u + kEpilogueWarps + q);
     };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
@@ -457,9 +470,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     // ---- one-time setup -------------------------------------------------
     if (warp == 0 && lane == 0) {
-        for (uint32_t s = 0; s < uint32_t(C::STAGES); ++s) {
-            ptx::mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival
-            ptx::mbar_init(empty_bar(s), 1);  // the pair's one tcgen05.commit
+        for (uint32_t g = 0; g < uint32_t(C::GROUPS); ++g) {
+            ptx::mbar_init(full_bar(g), 1);   // the leader's expect_tx arrival
+            ptx::mbar_init(empty_bar(g), 1);  // the pair's one tcgen05.commit
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(acc_full_bar(b), 1);                                  // one commit
@@ -541,7 +554,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 else ptx::tma_load_2d_pair(dst, map, bar, x, y);
             }
         };
-        uint32_t s = 0, ph = 0;
+        uint32_t g = 0, ph = 0;  // ring group and its phase
         bool ok = true;
         for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
             const WorkUnit w = unit_of(args, u);
@@ -551,57 +564,64 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int32_t b_row = nt * C::BN + int32_t(rank) * C::B_ROWS;
             int kr0, kr1;
             kb_range<C::KS>(w, krank, kr0, kr1);
-            for (int kb = kr0; kb < kr1; ++kb) {
-                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, ac, kRoleProducer)) {
+            // Group by group: k-blocks kb .. kb + n - 1 into the group's stages
+            // (n < G only for the last group of a unit with an odd count).
+            for (int kb = kr0; kb < kr1; kb += C::G) {
+                const int n = (kr1 - kb < C::G) ? kr1 - kb : C::G;
+                if (!wait_bounded_warp(empty_bar(g), ph ^ 1u, ac, kRoleProducer)) {
                     ok = false;
                     break;
                 }
                 if (ptx::elect_one_sync()) {
-                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE_TX);
-                    const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
-                    const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
-                    const int32_t k0 = kb * C::BK;
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(g), uint32_t(n) * C::STAGE_TX);
                     // the leader's barrier (a shared::cluster address) for a pair
-                    const uint32_t fb = (C::CG == 1) ? full_bar(s) : ptx::map_to_rank(full_bar(s), 0u);
-                    load(a_dst, &tmap_a, fb, k0, a_row, pol_a);
-                    if constexpr (!C::B_MN) {
-                        load(b_dst, &tmap_b, fb, k0, b_row, pol_b);
-                    } else {
+                    const uint32_t fb = (C::CG == 1) ? full_bar(g) : ptx::map_to_rank(full_bar(g), 0u);
 #pragma unroll
-                        for (int c = 0; c < C::B_ROWS / 64; ++c)
-                            load(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, fb, b_row + 64 * c, k0, pol_b);
-                    }
-                    if constexpr (C::MX) {
-                        // The scales of k-block kb, into this CTA's shared memory,
-                        // completing with the operands: the A atom of this CTA's 128
-                        // rows (128 rows x 4 groups) and the tile's B block (the
-                        // image of its TMEM copy; both CTAs of a pair load it).
-                        const uint32_t sfa_dst = base + C::OFF_SFA + s * C::SFA_BYTES;
-                        const uint32_t sfb_dst = base + C::OFF_SFB + s * C::SFB_BYTES;
-                        const int32_t sfb_block = nt * args.k_blocks + kb;
-                        if constexpr (C::CG == 1) {
-                            ptx::tma_load_2d(sfa_dst, &tmap_sa, full_bar(s), kb * 128, a_row / 128);
-                            ptx::tma_load_2d(sfb_dst, &tmap_sb, full_bar(s), 0, sfb_block * 4);
+                    for (int j = 0; j < C::G; ++j) {
+                        if (j >= n) break;
+                        const uint32_t s = g * uint32_t(C::G) + uint32_t(j);
+                        const uint32_t a_dst = base + C::OFF_A + s * C::A_BYTES;
+                        const uint32_t b_dst = base + C::OFF_B + s * C::B_BYTES;
+                        const int32_t k0 = (kb + j) * C::BK;
+                        load(a_dst, &tmap_a, fb, k0, a_row, pol_a);
+                        if constexpr (!C::B_MN) {
+                            load(b_dst, &tmap_b, fb, k0, b_row, pol_b);
                         } else {
-                            const uint32_t fb = ptx::map_to_rank(full_bar(s), 0u);
-                            ptx::tma_load_2d_pair(sfa_dst, &tmap_sa, fb, kb * 128, a_row / 128);
-                            ptx::tma_load_2d_pair(sfb_dst, &tmap_sb, fb, 0, sfb_block * 4);
+#pragma unroll
+                            for (int c = 0; c < C::B_ROWS / 64; ++c)
+                                load(b_dst + c * C::MN_ATOM_BYTES, &tmap_b, fb, b_row + 64 * c, k0, pol_b);
+                        }
+                        if constexpr (C::MX) {
+                            // The scales of k-block kb, into this CTA's shared memory,
+                            // completing with the operands: the A atom of this CTA's 128
+                            // rows (128 rows x 4 groups) and the tile's B block (the
+                            // image of its TMEM copy; both CTAs of a pair load it).
+                            const uint32_t sfa_dst = base + C::OFF_SFA + s * C::SFA_BYTES;
+                            const uint32_t sfb_dst = base + C::OFF_SFB + s * C::SFB_BYTES;
+                            const int32_t sfb_block = nt * args.k_blocks + kb + j;
+                            if constexpr (C::CG == 1) {
+                                ptx::tma_load_2d(sfa_dst, &tmap_sa, fb, (kb + j) * 128, a_row / 128);
+                                ptx::tma_load_2d(sfb_dst, &tmap_sb, fb, 0, sfb_block * 4);
+                            } else {
+                                ptx::tma_load_2d_pair(sfa_dst, &tmap_sa, fb, (kb + j) * 128, a_row / 128);
+                                ptx::tma_load_2d_pair(sfb_dst, &tmap_sb, fb, 0, sfb_block * 4);
+                            }
                         }
                     }
                 }
                 __syncwarp();
-                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                if (++g == uint32_t(C::GROUPS)) { g = 0; ph ^= 1u; }
             }
         }
         if (ok) {
-            // Drain: every slot must have been released by the MMA, so no
+            // Drain: every group must have been released by the MMA, so no
             // tcgen05.commit arrives on this CTA's barriers after it exits.
-            for (int i = 0; i < C::STAGES; ++i) {
-                if (!wait_bounded_warp(empty_bar(s), ph ^ 1u, ac, kRoleDrain)) {
+            for (int i = 0; i < C::GROUPS; ++i) {
+                if (!wait_bounded_warp(empty_bar(g), ph ^ 1u, ac, kRoleDrain)) {
                     ok = false;
                     break;
                 }
-                if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                if (++g == uint32_t(C::GROUPS)) { g = 0; ph ^= 1u; }
             }
         }
         __syncwarp();
@@ -689,7 +709,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // the cluster's last unit, and this loop waited for each hand-back.
           }
         } else if (leader) {
-            uint32_t s = 0, ph = 0, ab = 0, aph = 0;
+            uint32_t g = 0, ph = 0, ab = 0, aph = 0;  // ring group and its phase
             uint32_t sfbuf = 0;  // MX: TMEM scale buffer of the next k-block
             bool ok = true;
             for (int64_t u = cluster_id; u < units && ok; u += num_clusters) {
@@ -701,7 +721,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * C::SLOT_COLS;
                 // One k-block's MMAs from stage st (with MX, after its scale
-                // copies into TMEM buffer sfb), then the commit that frees st.
+                // copies into TMEM buffer sfb).
                 auto issue_kblock = [&](uint32_t st, uint32_t sfb, bool first) {
                     const uint32_t a_addr = base + C::OFF_A + st * C::A_BYTES;
                     const uint32_t b_addr = base + C::OFF_B + st * C::B_BYTES;
@@ -730,27 +750,34 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         else
                             ptx::mma_f16<C::CG>(d_tmem, ad, bd, C::IDESC, acc);
                     }
-                    // slot free (in every CTA that received data for it) once these MMAs finish
-                    ptx::mma_commit<C::CG>(empty_bar(st), uint16_t(0x3u));
                 };
-                // One k-block per pass.  Waiting for two stages and issuing both
-                // (halving the per-pass barrier wait, vote, fence and commit)
-                // measured no faster: a 224-wide k-block takes ~508 cycles
-                // either way (448 tensor cycles), which fits the shared-memory
-                // traffic it needs per SM (44 KiB of MMA operand reads and 30 KiB
-                // of TMA writes) better than the issue loop's cost.
+                // One group of C::G k-blocks per pass: one wait, the group's
+                // MMAs, one commit that frees the group's stages (in every CTA
+                // that received data for them) once those MMAs finish.  With
+                // one k-block per pass a 2-CTA 224-wide k-block takes ~448-508
+                // cycles, at or near its 448 tensor cycles, and pairing its
+                // stages measured no faster; a 1-CTA 128-wide k-block (256
+                // tensor cycles) took ~515.
                 int kr0, kr1;
                 kb_range<C::KS>(w, krank, kr0, kr1);
-                for (int kb = kr0; kb < kr1; ++kb) {
-                    if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
+                for (int kb = kr0; kb < kr1; kb += C::G) {
+                    const int n = (kr1 - kb < C::G) ? kr1 - kb : C::G;
+                    if (!wait_bounded_warp(full_bar(g), ph, ac, kRoleMma)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    if (ptx::elect_one_sync()) issue_kblock(s, sfbuf, kb == kr0);
+                    if (ptx::elect_one_sync()) {
+#pragma unroll
+                        for (int j = 0; j < C::G; ++j)
+                            if (j < n)
+                                issue_kblock(g * uint32_t(C::G) + uint32_t(j), sfbuf ^ uint32_t(j & 1),
+                                             kb + j == kr0);
+                        ptx::mma_commit<C::CG>(empty_bar(g), uint16_t(0x3u));
+                    }
                     __syncwarp();
-                    sfbuf ^= 1u;
-                    if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                    sfbuf ^= uint32_t(n & 1);
+                    if (++g == uint32_t(C::GROUPS)) { g = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 if (ptx::elect_one_sync())

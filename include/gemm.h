@@ -94,7 +94,13 @@ const char* gemm_status_string(int status);
  *   cta_group     0 = automatic, 1 = one CTA per 128-row tile (tcgen05
  *                 cta_group::1), 2 = a 2-CTA cluster per 256-row tile
  *                 (cta_group::2, the two CTAs' tensor cores act as one).
- *   block_n       0 = automatic, else the N extent of a tile: 128 or 256.
+ *   block_n       0 = automatic, else the N extent of a tile: 32 or 64
+ *                 (1-CTA tiles: cta_group 2 with them is GEMM_ERR_OPTION;
+ *                 32 with B N x K only), 128, 192 or 224 (B N x K only) or
+ *                 256.  Narrow tiles spread a small problem over more SMs:
+ *                 the automatic plan takes them (32 wide, else 64) for
+ *                 16-bit problems of 8 to 63 64-wide K blocks whose 128-wide
+ *                 1-CTA tiles fit in one round and that still do.
  *   raster_group  0 = automatic, else the number of tiles per raster group
  *                 of the persistent scheduler, counted along the grouped
  *                 dimension (see raster_order).
@@ -143,10 +149,11 @@ const char* gemm_status_string(int status);
  *                 CTAs, one K-range each; each CTA owns an equal share of the
  *                 tile's columns, receives the others' FP32 partials of them
  *                 through distributed shared memory and stores their sum,
- *                 taken in CTA order (no workspace).  Automatic: the most
- *                 ranges that keep at least 16 of K's 64-wide blocks per
- *                 range, unless the workspace split (tail_split) would run
- *                 more ranges per tile.  16-bit inputs only.
+ *                 taken in CTA order (no workspace).  Automatic: when K has
+ *                 at least 64 of its 64-wide blocks, the most ranges that
+ *                 keep at least 16 blocks per range, unless the workspace
+ *                 split (tail_split) would run more ranges per tile.  16-bit
+ *                 inputs only.
  */
 typedef struct {
     int cta_group;

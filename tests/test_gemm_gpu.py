@@ -32,14 +32,17 @@ VARIANTS = [
      "consumers": 2},
     {"cta_group": 1, "block_n": 128, "cluster_ksplit": 4},
     {"cta_group": 1, "block_n": 256, "cluster_ksplit": 2},
+    {"cta_group": 1, "block_n": 64, "cluster_ksplit": 1},
+    {"cta_group": 1, "block_n": 32, "cluster_ksplit": 1},
+    {"cta_group": 1, "block_n": 64, "cluster_ksplit": 2},
 ]
 VID = ["cg2_n256", "cg1_n256", "cg2_n128", "cg1_n128", "cg2_n224", "cg2_n192", "cg1_n224",
-       "cg2_n256_2cons", "cg1_n128_ks4", "cg1_n256_ks2"]
+       "cg2_n256_2cons", "cg1_n128_ks4", "cg1_n256_ks2", "cg1_n64", "cg1_n32", "cg1_n64_ks2"]
 
 
 def k_major_only(variant, layout):
-    """Widths 192 and 224 exist for K-major B (A.Bt) only."""
-    return layout == "ab" and variant["block_n"] % 128 != 0
+    """Widths 32, 192 and 224 exist for K-major B (A.Bt) only."""
+    return layout == "ab" and variant["block_n"] % 128 != 0 and variant["block_n"] != 64
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -106,7 +109,7 @@ def test_exact_small_integers(variant, layout, dtype):
     assert np.array_equal(got, ref)
 
 
-RING_CASES = [(1, 224), (2, 224), (1, 256), (2, 256)]
+RING_CASES = [(1, 224), (2, 224), (1, 256), (2, 256), (1, 64), (1, 32)]
 
 
 @pytest.mark.parametrize("cg,bn", RING_CASES, ids=[f"cg{c}_n{b}" for c, b in RING_CASES])
@@ -119,7 +122,7 @@ def test_exact_across_ring_wraps(cg, bn, layout, dtype):
     # is an integer of magnitude <= 1024, exact in FP32 in any order, so the
     # oracle's one rounding of the exact sum is the only correct output: a
     # k-block skipped, repeated or read from a stale stage changes it.
-    if layout == "ab" and bn % 128:
+    if layout == "ab" and bn % 128 and bn != 64:
         pytest.skip("K-major B only")
     M, N, K = 640, 3 * bn - 40, 1024
     A, B = small_int_operands(M, N, K, layout, dtype, seed=cg * 1000 + bn, lim=1)
@@ -399,6 +402,48 @@ def test_automatic_k_split_parity(shape, layout, dtype):
     assert plan["tail_split"] >= 2
     parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + 7,
            options=NO_CLUSTER_SPLIT)
+
+
+def test_narrow_tile_options():
+    # 32- and 64-wide tiles are 1-CTA tiles; 32 takes K-major B only.
+    p = binding.gemm_plan(256, 256, 1024, 0, 0, {"block_n": 32})
+    assert (p["cta_group"], p["block_m"], p["block_n"], p["num_tiles"]) == (1, 128, 32, 16)
+    assert binding.gemm_plan(256, 256, 1024, 0, 1, {"block_n": 64})["block_n"] == 64
+    for opts, layout in (({"block_n": 64, "cta_group": 2}, 0), ({"block_n": 32}, 1),
+                         ({"block_n": 96}, 0)):
+        with pytest.raises(binding.GemmError) as e:
+            binding.gemm_plan(256, 256, 1024, 0, layout, opts)
+        assert e.value.status == -8
+
+
+def test_automatic_narrow_tiles_for_shallow_single_round_problems():
+    # 16 k-blocks on four 128 x 128 tiles: sixteen 32-wide tiles still fit one round.
+    p = binding.gemm_plan(256, 256, 1024, 0, 0)
+    assert (p["cta_group"], p["block_n"], p["num_tiles"], p["cluster_ksplit"]) == (1, 32, 16, 1)
+    assert p["stages"] % 2 == 0  # 1-CTA tiles of at most 128 columns pair their stages
+    # B K x N: 32-wide tiles take B N x K only, so 64
+    assert binding.gemm_plan(256, 256, 1024, 0, 1)["block_n"] == 64
+    # 32-wide tiles would take two rounds here: 64
+    q = binding.gemm_plan(1024, 1024, 2048, 0, 0)
+    assert (q["block_n"], q["num_tiles"]) == (64, 128)
+    # one k-block, or 64 and more: unchanged
+    assert binding.gemm_plan(128, 128, 64, 0, 0)["block_n"] == 128
+    assert binding.gemm_plan(256, 256, 4096, 0, 0)["block_n"] == 128
+    # an explicit width is kept
+    assert binding.gemm_plan(256, 256, 1024, 0, 0, {"block_n": 128})["block_n"] == 128
+
+
+@pytest.mark.parametrize("shape,layout,dtype", [
+    ((256, 256, 1024), "abt", "f16"),    # the 16-k-block workload: 32-wide tiles
+    ((300, 520, 1000), "abt", "bf16"),   # ragged rows, columns and K on 32-wide tiles
+    ((384, 640, 2000), "ab", "f16"),     # MN-major B: 64-wide tiles
+    ((1000, 1000, 2048), "abt", "f16"),  # 64-wide tiles, a ragged edge
+])
+def test_automatic_narrow_tile_parity(shape, layout, dtype):
+    M, N, K = shape
+    plan = binding.gemm_plan(M, N, K, 0 if dtype == "f16" else 1, 0 if layout == "abt" else 1)
+    assert plan["block_n"] in (32, 64)
+    parity(M, N, K, layout, dtype, "uniform" if dtype == "f16" else "normal", seed=K + 5)
 
 
 def test_in_cluster_k_split_plans():
