@@ -338,14 +338,15 @@ __device__ __forceinline__ uint64_t noswizzle_desc(uint32_t addr, uint32_t lbo, 
     return d;
 }
 
-// A CTA's abort state: its flag (in its shared memory, polled by every role;
-// `flag_addr` is its shared::cta address, the same offset in every CTA of the
-// cluster), the cluster's size and this CTA's rank in it, and the limit of
-// every wait.
+// A CTA's abort state in a cluster of N CTAs: its flag (in its shared memory,
+// polled by every role; `flag_addr` is its shared::cta address, the same
+// offset in every CTA of the cluster), this CTA's rank in the cluster, and the
+// limit of every wait.  N is a template parameter so that the waits inlined
+// into the hot loops carry no loop over ranks for 1- and 2-CTA clusters.
+template <int N>
 struct AbortCtl {
     volatile uint32_t* flag;
     uint32_t flag_addr;
-    uint32_t cluster_size;
     uint32_t my_rank;
     uint64_t limit_ns;
 };
@@ -353,16 +354,25 @@ struct AbortCtl {
 // Record the reason and raise the flag in every CTA of the cluster: a role of
 // another CTA may be the one that would wait for this CTA's work, and every
 // warp that sees the flag settles before it leaves (see the teardown).
-__device__ __forceinline__ void raise_abort(const AbortCtl& ac, uint32_t role) {
+template <int N>
+__device__ __forceinline__ void raise_abort(const AbortCtl<N>& ac, uint32_t role) {
     *ac.flag = 1u;
-    for (uint32_t r = 0; r < ac.cluster_size; ++r)
-        if (r != ac.my_rank) ptx::st_cluster_u32(ptx::map_to_rank(ac.flag_addr, r), 1u);
+    if constexpr (N == 2) {
+        ptx::st_cluster_u32(ptx::map_to_rank(ac.flag_addr, ac.my_rank ^ 1u), 1u);
+    } else if constexpr (N > 2) {
+#pragma unroll
+        for (uint32_t r = 0; r < uint32_t(N); ++r)
+            if (r != ac.my_rank) ptx::st_cluster_u32(ptx::map_to_rank(ac.flag_addr, r), 1u);
+    }
     atomicCAS(&g_gemm_status, 0u, kReasonTimeout | (role << 8));
 }
 
 // Wait for phase `parity` of `bar`, giving up after ac.limit_ns or when a role
-// of this CTA or of its pair has aborted.  Returns false on give-up.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortCtl& ac,
+// of this CTA or of another CTA of its cluster has aborted.  Returns false on
+// give-up.  (Kept inline: a wait's slow path is common in the hot loops, and
+// moving it out of line measured 4-6 % slower on the 2-CTA plans.)
+template <int N>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortCtl<N>& ac,
                                              uint32_t role) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::global_timer_ns();
@@ -380,7 +390,8 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 
 // wait_bounded for a whole converged warp: every lane waits (and acquires), and
 // all lanes return the same result.
-__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, const AbortCtl& ac,
+template <int N>
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, const AbortCtl<N>& ac,
                                                   uint32_t role) {
     const bool ok = wait_bounded(bar, parity, ac, role);
     return __all_sync(0xffffffffu, ok);
@@ -396,7 +407,8 @@ __device__ __forceinline__ void settle_after_abort() {
 
 // For a converged warp at the end of its role: if this CTA's abort flag is
 // up, settle (the whole warp takes one decision, read by lane 0).
-__device__ __forceinline__ void settle_if_aborted(const AbortCtl& ac) {
+template <int N>
+__device__ __forceinline__ void settle_if_aborted(const AbortCtl<N>& ac) {
     const uint32_t up = __shfl_sync(0xffffffffu, *ac.flag, 0);
     if (up) settle_after_abort();
     __syncwarp();
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     };
     volatile uint32_t* const abort_flag =
         reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
-    const AbortCtl ac{abort_flag, base + C::OFF_ABORT, uint32_t(C::CLUSTER), crank,
+    const AbortCtl<C::CLUSTER> ac{abort_flag, base + C::OFF_ABORT, crank,
                       args.wait_limit_ns};
 
     // ---- one-time setup -------------------------------------------------
@@ -567,13 +579,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // Group by group: k-blocks kb .. kb + n - 1 into the group's stages
             // (n < G only for the last group of a unit with an odd count).
             for (int kb = kr0; kb < kr1; kb += C::G) {
-                const int n = (kr1 - kb < C::G) ? kr1 - kb : C::G;
+                // (a compile-time 1 with one k-block per group: the 2-CTA loops
+                // have no cycles to spare)
+                const int n = (C::G == 1) ? 1 : ((kr1 - kb < C::G) ? kr1 - kb : C::G);
                 if (!wait_bounded_warp(empty_bar(g), ph ^ 1u, ac, kRoleProducer)) {
                     ok = false;
                     break;
                 }
                 if (ptx::elect_one_sync()) {
-                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(g), uint32_t(n) * C::STAGE_TX);
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(g), C::G == 1 ? C::STAGE_TX : uint32_t(n) * C::STAGE_TX);
                     // the leader's barrier (a shared::cluster address) for a pair
                     const uint32_t fb = (C::CG == 1) ? full_bar(g) : ptx::map_to_rank(full_bar(g), 0u);
 #pragma unroll
@@ -761,7 +775,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 int kr0, kr1;
                 kb_range<C::KS>(w, krank, kr0, kr1);
                 for (int kb = kr0; kb < kr1; kb += C::G) {
-                    const int n = (kr1 - kb < C::G) ? kr1 - kb : C::G;
+                    const int n = (C::G == 1) ? 1 : ((kr1 - kb < C::G) ? kr1 - kb : C::G);
                     if (!wait_bounded_warp(full_bar(g), ph, ac, kRoleMma)) {
                         ok = false;
                         break;
@@ -1313,7 +1327,7 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
         abort_flag = 0u;
         ptx::mbar_init(ptx::smem_addr(&bar), 1);
         ptx::fence_mbar_init();
-        const AbortCtl ac{&abort_flag, 0u, 1u, 0u, limit_ns};
+        const AbortCtl<1> ac{&abort_flag, 0u, 0u, limit_ns};
         wait_bounded(ptx::smem_addr(&bar), 0u, ac, kRoleSelfTest);
     }
 }
