@@ -645,12 +645,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (leader) {
             // Two consumers ("TIRx GEMM on Blackwell", V9): their accumulators
             // fill TMEM, so the next tile's MMAs can only start once the
-            // epilogue has drained them.  It drains consumer 0 first and hands
-            // each consumer back on its own barrier (acc_empty[h]); consumer 0
-            // then runs alone over the tile's first k-blocks (up to one ring),
-            // keeping their stages, while consumer 1 is still being drained;
-            // consumer 1 catches up on those stages, and the rest of the tile
-            // issues both consumers per k-block as one B tile serves both.
+            // epilogue has drained them.  Each consumer has its own full and
+            // empty accumulator barrier (acc_full[h], acc_empty[h]), and the
+            // tile is issued so that the drains overlap MMAs: consumer 0 runs
+            // alone over the tile's first k-blocks (up to one ring), keeping
+            // their stages, while consumer 1 is still being drained; consumer 1
+            // catches up on those stages; the middle issues both consumers per
+            // k-block as one B tile serves both; and the last k-blocks (up to
+            // one ring) go to consumer 0 first, so that its accumulator is
+            // complete and drained while consumer 1 finishes them.
             uint32_t s = 0, ph = 0, aph = 0;
             bool ok = true;
             auto issue = [&](uint32_t st, int h, bool first_kb) {
@@ -669,6 +672,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const WorkUnit w = unit_of(args, u);
                 const int nkb = w.kb1 - w.kb0;
                 const int lead = nkb < C::STAGES ? nkb : C::STAGES;
+                const int tail = (nkb - lead < C::STAGES) ? nkb - lead : C::STAGES;
                 const uint32_t s0 = s;
                 if (!wait_bounded_warp(acc_empty_bar(0), aph ^ 1u, ac, kRoleMma)) {
                     ok = false;
@@ -686,6 +690,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
+                if (tail == 0) {  // consumer 0 is complete
+                    if (ptx::elect_one_sync()) ptx::mma_commit<C::CG>(acc_full_bar(0), uint16_t(0x3u));
+                    __syncwarp();
+                }
                 if (!wait_bounded_warp(acc_empty_bar(1), aph ^ 1u, ac, kRoleMma)) {
                     ok = false;
                     break;
@@ -699,7 +707,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     __syncwarp();
                 }
-                for (int i = lead; i < nkb; ++i) {  // both consumers share each B tile
+                for (int i = lead; i < nkb - tail; ++i) {  // both consumers share each B tile
                     if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
                         ok = false;
                         break;
@@ -714,8 +722,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
+                if (tail > 0) {
+                    const uint32_t s1 = s;
+                    for (int i = 0; i < tail; ++i) {  // consumer 0 finishes first; stages kept
+                        if (!wait_bounded_warp(full_bar(s), ph, ac, kRoleMma)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        if (ptx::elect_one_sync()) issue(s, 0, false);
+                        __syncwarp();
+                        if (++s == uint32_t(C::STAGES)) { s = 0; ph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    if (ptx::elect_one_sync()) ptx::mma_commit<C::CG>(acc_full_bar(0), uint16_t(0x3u));
+                    __syncwarp();
+                    for (int i = 0; i < tail; ++i) {  // consumer 1 on the same stages, released
+                        const uint32_t st = (s1 + uint32_t(i)) % uint32_t(C::STAGES);
+                        if (ptx::elect_one_sync()) {
+                            issue(st, 1, false);
+                            ptx::mma_commit<C::CG>(empty_bar(st), uint16_t(0x3u));
+                        }
+                        __syncwarp();
+                    }
+                }
                 if (ptx::elect_one_sync())
-                    ptx::mma_commit<C::CG>(acc_full_bar(0), uint16_t(0x3u));  // both accumulators ready
+                    ptx::mma_commit<C::CG>(acc_full_bar(1), uint16_t(0x3u));  // consumer 1 is complete
                 __syncwarp();
                 aph ^= 1u;
             }
@@ -1096,8 +1128,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // current ones are converted and staged, and each 64-column
                     // chunk (or the last 32 columns of a 224-wide tile) leaves as
                     // one TMA store once both of its halves are staged.
+                    bool h_aborted = false;
 #pragma unroll 1
                     for (int h = 0; h < C::CONS; ++h) {
+                        if constexpr (C::CONS == 2) {
+                            if (h == 1) {
+                                // consumer 1's accumulator completes after consumer 0's
+                                uint32_t ok1 = 1u;
+                                if (lane == 0) ok1 = wait_bounded(acc_full_bar(1), aph, ac, kRoleEpilogue);
+                                ok1 = __shfl_sync(0xffffffffu, ok1, 0);
+                                if (!ok1) {
+                                    h_aborted = true;
+                                    break;
+                                }
+                                while (!ptx::mbar_try_wait(acc_full_bar(1), aph)) {
+                                }  // completed already: every lane's own acquire
+                                ptx::tc_fence_after();
+                            }
+                        }
                         const uint32_t th = taddr + uint32_t(h) * C::ACC_STRIDE;
                         const int32_t rh = row0 + 128 * h;
                         const bool last_h = (h == C::CONS - 1);
@@ -1131,6 +1179,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (u + 1 < U) ptx::tmem_wait_ld();
                         }
                     }
+                    if (h_aborted) break;
                 }
             } else if constexpr (C::KS == 1) {  // (no tail split with an in-cluster split)
                 // K-range of a tail tile.  Pass 1: write this range's FP32 partial
