@@ -1172,7 +1172,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             const bool narrow = C::HALF_CHUNK && (c == C::FULL_CHUNKS);  // 32 columns
                             if (first_half) {
                                 if (pace && c > 0) __nanosleep(kStorePaceNs);
-                                buf = stage_buffer(last_unit ? h * CHUNKS + c : -1);
+                                // In the cluster's last unit the ring is idle once every
+                                // MMA is done: with two consumers, only when consumer 1
+                                // is drained (consumer 0's drain overlaps its last MMAs).
+                                const bool ring_idle = last_unit && (C::CONS == 1 || h == C::CONS - 1);
+                                buf = stage_buffer(ring_idle ? h * CHUNKS + c : -1);
                             }
                             stage_half(cur, buf, narrow ? 32 : 64, first_half ? 0 : 1);
                             if (!first_half || narrow) issue_store(buf, col0 + 64 * c, rh, narrow ? 32 : 64);
