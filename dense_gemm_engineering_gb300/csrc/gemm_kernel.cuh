@@ -220,12 +220,21 @@ struct KernelConfig {
     static_assert(!B_MN || (B_ROWS % 64) == 0, "MN-major B is loaded in 64-column atoms");
     static_assert(SMEM_BYTES <= 232448, "exceeds 227 KiB of shared memory per CTA");
     // In-cluster K split: each other CTA's piece of a lane quarter (32 rows x
-    // BN / KS FP32 columns) lands in a slice of its own in the owner's ring.
+    // BN / KS FP32 columns) lands in a slice of its own in the owner's shared
+    // memory.  The first RECV_STG_SLOTS of a quarter's KS - 1 pieces go into the
+    // epilogue staging buffers of that quarter's warp (idle until the epilogue,
+    // which then stages its own output in the ring, at OFF_KS_OUT), so they
+    // need no hand-shake; the rest go into the operand ring, once its owner
+    // has said that its MMAs are done.
     static constexpr uint32_t RECV_SLICE_BYTES = 32u * uint32_t(BN / KS) * 4u;
+    static constexpr uint32_t RECV_STG_SLOTS = (KS > 1) ? (EPI_BUFS * EPI_BUF_BYTES) / RECV_SLICE_BYTES : 0u;
+    static constexpr uint32_t RECV_RING_SLOTS =
+        (uint32_t(KS - 1) > RECV_STG_SLOTS) ? uint32_t(KS - 1) - RECV_STG_SLOTS : 0u;
+    static constexpr uint32_t OFF_KS_OUT = OFF_A + ((RECV_RING_SLOTS * 4u * RECV_SLICE_BYTES + 1023u) & ~1023u);
     static_assert(KS == 1 || KS == 2 || KS == 4, "1, 2 or 4 K-ranges per cluster");
     static_assert(KS == 1 || (CG == 1 && CONS == 1 && !MX), "in-cluster K split: 1-CTA, 1-consumer tiles");
-    static_assert(uint32_t(KS - 1) * 4u * RECV_SLICE_BYTES <= RING_BYTES,
-                  "the other CTAs' pieces fit in the owner's ring");
+    static_assert(KS == 1 || OFF_KS_OUT + uint32_t(kEpilogueWarps) * 2u * EPI_BUF_BYTES <= OFF_A + RING_BYTES,
+                  "the pieces the ring receives and the output staging fit in the ring");
     static_assert(KS == 1 || (BN / KS) % 32 == 0, "each CTA owns whole 32-column units");
     // the epilogue stores 32-column boxes (the last chunk of a 224-wide tile,
     // or a CTA's share of a 128-wide tile split 4 ways)
@@ -1012,38 +1021,41 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (w.range < 0) {
                 if constexpr (C::KS > 1) {
                     // In-cluster K split, summed as a reduce-scatter: CTA k owns
-                    // columns [k W, (k+1) W) of the tile (W = BN / KS).  Once its
-                    // own MMAs are done its ring is idle (one unit per cluster):
-                    // it tells every other CTA so (their go[quarter]), waits
-                    // until every other CTA has said the same, writes its FP32
-                    // partial of each other CTA's columns for these 32 rows into
-                    // that CTA's ring over distributed shared memory and arrives
-                    // on that CTA's done[quarter].  Then it adds the others'
-                    // partials of its own columns to its own in CTA order (the
-                    // same sum, term for term, whichever CTA owns the columns)
-                    // and stores them.
+                    // columns [k W, (k+1) W) of the tile (W = BN / KS).  It writes
+                    // its FP32 partial of each other CTA's columns for these 32 rows
+                    // into that CTA's shared memory over distributed shared memory
+                    // and arrives on that CTA's done[quarter]; then it adds the
+                    // others' partials of its own columns to its own in CTA order
+                    // (the same sum, term for term, whichever CTA owns the columns)
+                    // and stores them.  The piece from the CTA s places after the
+                    // owner (mod KS) fills the owner's slot s - 1: the first slots
+                    // are its epilogue staging buffers, free from the start (one
+                    // unit per cluster); a slot in its operand ring is free only
+                    // once its own MMAs are done, which it announces on every other
+                    // CTA's go[quarter] -- the pieces that need no announcement are
+                    // written first.
                     constexpr int W = C::BN / C::KS;
                     constexpr int UW = W / 32;             // 32-column units it owns
                     constexpr int T = (C::KS - 1) * UW;    // units it sends
-                    // where CTA `src`'s piece of this quarter lands in CTA `dst`
-                    auto recv_slice = [&](uint32_t dst, uint32_t src) -> uint32_t {
-                        const uint32_t slot = src - (src > dst ? 1u : 0u);
-                        return base + C::OFF_A + (slot * 4u + quarter) * C::RECV_SLICE_BYTES;
+                    constexpr int T_STG = int(C::RECV_STG_SLOTS < uint32_t(C::KS - 1) ? C::RECV_STG_SLOTS
+                                                                                   : uint32_t(C::KS - 1)) * UW;
+                    constexpr bool NEED_GO = C::RECV_RING_SLOTS > 0;
+                    // the address, in any CTA, of the slot `slot` of this quarter
+                    auto recv_slot = [&](uint32_t slot) -> uint32_t {
+                        return slot < C::RECV_STG_SLOTS
+                                   ? buf0 + slot * C::RECV_SLICE_BYTES
+                                   : base + C::OFF_A + ((slot - C::RECV_STG_SLOTS) * 4u + quarter) * C::RECV_SLICE_BYTES;
                     };
+                    // the CTA that receives this CTA's piece in slot s
                     auto send_dst = [&](int t) -> uint32_t {
-                        const uint32_t r = uint32_t(t / UW);
-                        return r + (r >= krank ? 1u : 0u);
+                        return (krank + uint32_t(C::KS - 1 - t / UW)) % uint32_t(C::KS);
                     };
-                    if (lane == 0)
-                        for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
-                            if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(go_bar(quarter), r));
-                    uint32_t okg = 1u;
-                    if (lane == 0) okg = wait_bounded(go_bar(quarter), gph, ac, kRoleEpilogue);
-                    okg = __shfl_sync(0xffffffffu, okg, 0);
-                    if (!okg) break;
-                    while (!ptx::mbar_try_wait(go_bar(quarter), gph)) {
-                    }  // completed already: every lane's own acquire
-                    gph ^= 1u;
+                    if constexpr (NEED_GO) {
+                        if (lane == 0)
+                            for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
+                                if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(go_bar(quarter), r));
+                    }
+                    bool okg = true;
                     {
                         uint32_t ra[32], rb[32];
                         ptx::tmem_ld_32x32b_x32(taddr + send_dst(0) * W, ra);
@@ -1055,8 +1067,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (t + 1 < T)
                                 ptx::tmem_ld_32x32b_x32(taddr + send_dst(t + 1) * W + 32u * uint32_t((t + 1) % UW),
                                                         nxt);
+                            if (NEED_GO && t == T_STG) {  // the ring slots: wait for their owners
+                                uint32_t okw = 1u;
+                                if (lane == 0) okw = wait_bounded(go_bar(quarter), gph, ac, kRoleEpilogue);
+                                okw = __shfl_sync(0xffffffffu, okw, 0);
+                                if (!okw) {
+                                    okg = false;
+                                    if (t + 1 < T) ptx::tmem_wait_ld();
+                                    break;
+                                }
+                                while (!ptx::mbar_try_wait(go_bar(quarter), gph)) {
+                                }  // completed already: every lane's own acquire
+                                gph ^= 1u;
+                            }
                             const uint32_t dst = send_dst(t);
-                            const uint32_t sl = ptx::map_to_rank(recv_slice(dst, krank), dst);
+                            const uint32_t sl = ptx::map_to_rank(recv_slot(uint32_t(t / UW)), dst);
 #pragma unroll
                             for (int g = 0; g < 8; ++g)
                                 ptx::st_cluster_v4(sl + ((uint32_t(t % UW) * 8u + uint32_t(g)) * 32u + lane) * 16u,
@@ -1064,6 +1089,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (t + 1 < T) ptx::tmem_wait_ld();
                         }
                     }
+                    if (!okg) break;
                     ptx::fence_acq_rel_cluster();
                     __syncwarp();
                     if (lane == 0)
@@ -1082,6 +1108,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     while (!ptx::mbar_try_wait(done_bar(quarter), dph)) {
                     }  // completed already: every lane's own acquire
                     dph ^= 1u;
+                    // output staging: the ring past its receiving slots, a fresh
+                    // 4 KiB buffer per chunk (at most two per warp)
+                    const uint32_t out0 = base + C::OFF_KS_OUT + (warp - 2u) * 2u * C::EPI_BUF_BYTES;
                     uint32_t buf = 0;
 #pragma unroll
                     for (int v = 0; v < UW; ++v) {
@@ -1101,7 +1130,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 }
                                 continue;
                             }
-                            const uint32_t sl = recv_slice(krank, r);
+                            // CTA r's piece: r sits (r - krank) mod KS places after this CTA
+                            const uint32_t sl = recv_slot((r + uint32_t(C::KS) - krank) % uint32_t(C::KS) - 1u);
 #pragma unroll
                             for (int g = 0; g < 8; ++g) {
                                 float x[4];
@@ -1115,7 +1145,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) cur[i] = __float_as_uint(acc[i]);
                         const bool first_half = (v % 2 == 0);
-                        if (first_half) buf = stage_buffer(-1);  // (the ring holds the pieces)
+                        if (first_half) buf = out0 + uint32_t(v / 2) * C::EPI_BUF_BYTES;
                         stage_half(cur, buf, W == 32 ? 32 : 64, first_half ? 0 : 1);
                         if (!first_half || W == 32)
                             issue_store(buf, col0 + int32_t(krank) * W + 64 * (v / 2), row0, W == 32 ? 32 : 64);
