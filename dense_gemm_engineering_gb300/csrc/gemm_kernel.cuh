@@ -231,10 +231,13 @@ struct KernelConfig {
     static constexpr uint32_t RECV_RING_SLOTS =
         (uint32_t(KS - 1) > RECV_STG_SLOTS) ? uint32_t(KS - 1) - RECV_STG_SLOTS : 0u;
     static constexpr uint32_t OFF_KS_OUT = OFF_A + ((RECV_RING_SLOTS * 4u * RECV_SLICE_BYTES + 1023u) & ~1023u);
+    // ... and the pieces a CTA sends are staged in its own ring first, each
+    // slot's piece leaving as one bulk copy
+    static constexpr uint32_t OFF_KS_SEND = OFF_KS_OUT + uint32_t(kEpilogueWarps) * 2u * EPI_BUF_BYTES;
     static_assert(KS == 1 || KS == 2 || KS == 4, "1, 2 or 4 K-ranges per cluster");
     static_assert(KS == 1 || (CG == 1 && CONS == 1 && !MX), "in-cluster K split: 1-CTA, 1-consumer tiles");
-    static_assert(KS == 1 || OFF_KS_OUT + uint32_t(kEpilogueWarps) * 2u * EPI_BUF_BYTES <= OFF_A + RING_BYTES,
-                  "the pieces the ring receives and the output staging fit in the ring");
+    static_assert(KS == 1 || OFF_KS_SEND + uint32_t(KS - 1) * 4u * RECV_SLICE_BYTES <= OFF_A + RING_BYTES,
+                  "the pieces the ring receives, the output staging and the sent pieces fit in the ring");
     static_assert(KS == 1 || (BN / KS) % 32 == 0, "each CTA owns whole 32-column units");
     // the epilogue stores 32-column boxes (the last chunk of a 224-wide tile,
     // or a CTA's share of a 128-wide tile split 4 ways)
@@ -502,8 +505,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (uint32_t e = 0; e < uint32_t(kEpilogueWarps); ++e) ptx::mbar_init(epi_bar(e), 1);
         if constexpr (C::KS > 1) {
             for (uint32_t q = 0; q < 4u; ++q) {
-                ptx::mbar_init(go_bar(q), uint32_t(C::KS - 1));     // each other CTA's warp q
-                ptx::mbar_init(done_bar(q), uint32_t(C::KS - 1));
+                ptx::mbar_init(go_bar(q), uint32_t(C::KS - 1));  // each other CTA's warp q
+                ptx::mbar_init(done_bar(q), 1);  // warp q's expect_tx; the pieces complete its bytes
             }
         }
         *abort_flag = 0u;
@@ -1050,11 +1053,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     auto send_dst = [&](int t) -> uint32_t {
                         return (krank + uint32_t(C::KS - 1 - t / UW)) % uint32_t(C::KS);
                     };
-                    if constexpr (NEED_GO) {
-                        if (lane == 0)
+                    if (lane == 0) {
+                        // the KS - 1 pieces this warp will receive, as bytes on its done barrier
+                        // (they may already have begun to land: the count may go below zero)
+                        ptx::mbar_arrive_expect_tx(done_bar(quarter), uint32_t(C::KS - 1) * C::RECV_SLICE_BYTES);
+                        if constexpr (NEED_GO)
                             for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
                                 if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(go_bar(quarter), r));
                     }
+                    // this warp's staged copy of the piece for slot s
+                    auto send_slice = [&](uint32_t slot) -> uint32_t {
+                        return base + C::OFF_KS_SEND + (slot * 4u + quarter) * C::RECV_SLICE_BYTES;
+                    };
                     bool okg = true;
                     {
                         uint32_t ra[32], rb[32];
@@ -1067,34 +1077,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (t + 1 < T)
                                 ptx::tmem_ld_32x32b_x32(taddr + send_dst(t + 1) * W + 32u * uint32_t((t + 1) % UW),
                                                         nxt);
-                            if (NEED_GO && t == T_STG) {  // the ring slots: wait for their owners
-                                uint32_t okw = 1u;
-                                if (lane == 0) okw = wait_bounded(go_bar(quarter), gph, ac, kRoleEpilogue);
-                                okw = __shfl_sync(0xffffffffu, okw, 0);
-                                if (!okw) {
-                                    okg = false;
-                                    if (t + 1 < T) ptx::tmem_wait_ld();
-                                    break;
-                                }
-                                while (!ptx::mbar_try_wait(go_bar(quarter), gph)) {
-                                }  // completed already: every lane's own acquire
-                                gph ^= 1u;
-                            }
-                            const uint32_t dst = send_dst(t);
-                            const uint32_t sl = ptx::map_to_rank(recv_slot(uint32_t(t / UW)), dst);
+                            const uint32_t sl = send_slice(uint32_t(t / UW));
 #pragma unroll
                             for (int g = 0; g < 8; ++g)
-                                ptx::st_cluster_v4(sl + ((uint32_t(t % UW) * 8u + uint32_t(g)) * 32u + lane) * 16u,
-                                                   cur[4 * g], cur[4 * g + 1], cur[4 * g + 2], cur[4 * g + 3]);
+                                ptx::st_shared_v4(sl + ((uint32_t(t % UW) * 8u + uint32_t(g)) * 32u + lane) * 16u,
+                                                  cur[4 * g], cur[4 * g + 1], cur[4 * g + 2], cur[4 * g + 3]);
+                            if (t % UW == UW - 1) {  // the slot's piece is staged: send it
+                                if (NEED_GO && t / UW == T_STG / UW) {  // the ring slots: wait for their owners
+                                    uint32_t okw = 1u;
+                                    if (lane == 0) okw = wait_bounded(go_bar(quarter), gph, ac, kRoleEpilogue);
+                                    okw = __shfl_sync(0xffffffffu, okw, 0);
+                                    if (!okw) {
+                                        okg = false;
+                                        if (t + 1 < T) ptx::tmem_wait_ld();
+                                        break;
+                                    }
+                                    gph ^= 1u;
+                                }
+                                ptx::fence_proxy_async_smem();  // the staged piece, for the copy engine
+                                __syncwarp();
+                                if (lane == 0) {
+                                    const uint32_t dst = send_dst(t);
+                                    ptx::bulk_copy_s2cluster(ptx::map_to_rank(recv_slot(uint32_t(t / UW)), dst),
+                                                             sl, C::RECV_SLICE_BYTES,
+                                                             ptx::map_to_rank(done_bar(quarter), dst));
+                                }
+                            }
                             if (t + 1 < T) ptx::tmem_wait_ld();
                         }
                     }
                     if (!okg) break;
-                    ptx::fence_acq_rel_cluster();
-                    __syncwarp();
-                    if (lane == 0)
-                        for (uint32_t r = 0; r < uint32_t(C::KS); ++r)
-                            if (r != krank) ptx::mbar_arrive_cluster(ptx::map_to_rank(done_bar(quarter), r));
                     // this CTA's own columns: its partial from TMEM (the first
                     // load in flight while the others' pieces arrive)
                     const uint32_t town = taddr + krank * uint32_t(W);

@@ -259,6 +259,18 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 // Bulk (non-tensor) copy of `bytes` (a multiple of 16) from global memory to
 // this CTA's shared memory; completion is signalled on `bar` (complete_tx).
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA of the cluster (dst and bar: shared::cluster addresses there),
+// completing as transaction bytes on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
     asm volatile(
